@@ -1,0 +1,64 @@
+"""The oracle pins catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of ``oracle/oracle.c`` (a
+wrong head mapping, a wrong slot offset, a missing refcount update, a dropped
+softmax step, ...), builds it with gcc, and runs the pin suites against that
+build in a child process. Every mutant must make at least one pin fail. The
+committed oracle itself is never modified.
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_block_manager.py"]
+
+MUTANTS = {
+    "gqa_head_mapping": ("const int kvh = h / G;", "const int kvh = h % Hk;"),
+    "key_slot_offset": ("size_t kbase = (((size_t)phys * B + (size_t)(t % B))",
+                        "size_t kbase = (((size_t)phys * B + (size_t)((t + 1) % B))"),
+    "value_from_key_pool": ("o[e] += w * element(v_cache,", "o[e] += w * element(k_cache,"),
+    "missing_scale": ("x[t] = scale * dot;", "x[t] = dot;"),
+    "missing_normalisation": ("double w = x[t] / z;", "double w = x[t];"),
+    "missing_max_subtraction": ("x[t] = exp(x[t] - m);", "x[t] = exp(x[t]);"),
+    "free_list_order": ("int b = alloc_order ? alloc_order[num_blocks - 1 - i] : num_blocks - 1 - i;",
+                        "int b = alloc_order ? alloc_order[i] : i;"),
+    "slot_offset": ("long long slot = (long long)s->table[t / B] * B + t % B;",
+                    "long long slot = (long long)s->table[t / B] * B + (t + 1) % B;"),
+    "cow_keeps_source_count": ("bm->refcount[tail] -= 1;", ";"),
+    "cow_on_private_block": ("if (bm->refcount[tail] > 1) {", "if (bm->refcount[tail] >= 1) {"),
+    "fork_without_increment": ("bm->refcount[p->table[j]] += 1;", ";"),
+    "free_ignores_refcount": ("if (bm->refcount[b] == 0) bm->free_stack[bm->top++] = b;",
+                              "bm->free_stack[bm->top++] = b;"),
+    "copy_blocks_swapped": ("memcpy((char *)k_cache + (size_t)dst * blk_bytes, (char *)k_cache + (size_t)src * blk_bytes",
+                            "memcpy((char *)k_cache + (size_t)src * blk_bytes, (char *)k_cache + (size_t)dst * blk_bytes"),
+}
+
+
+def _run_mutant(name, tmpdir):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"{name}: pattern must occur exactly once"
+    c = os.path.join(tmpdir, f"{name}.c")
+    so = os.path.join(tmpdir, f"{name}.so")
+    with open(c, "w") as f:
+        f.write(text.replace(old, new))
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", so, c, "-lm"], check=True)
+    env = dict(os.environ, PKV_ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *PINS],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return name, r.returncode
+
+
+def test_every_mutant_is_caught(tmp_path):
+    names = sorted(MUTANTS)
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+        results = dict(ex.map(lambda n: _run_mutant(n, str(tmp_path)), names))
+    survivors = [n for n, rc in results.items() if rc == 0]
+    assert not survivors, f"pins did not catch: {survivors}"
+    # rc 1 = a test failed; anything else (crash, collection error) is not a pin.
+    assert all(rc == 1 for rc in results.values()), results
