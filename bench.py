@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of the whole hot path over one batch: the host
+block manager appends one token to every sequence (slots, copy-on-write pairs,
+block tables), then pk_copy_blocks (when pairs exist), pk_reshape_and_cache
+and pk_paged_attention_decode (+ its log-sum-exp merge when it splits).
+
+Device timing (``value``): the host side of a window of steps is prepared and
+uploaded before the timed region, so inputs are resident in HBM; each timed
+step is bracketed by CUDA events on the launching stream, and the L2 is
+flushed (a write of twice its size) between steps, outside the events.
+``e2e`` times the same steps through the public API from pinned host buffers:
+the host block-manager append, the host->device copies of the step's inputs,
+the kernels and the device->host copy of the output are all inside the timer.
+
+Metric: algorithmic K/V bytes read per step (sum over sequences of
+context_len * Hk * head_dim * 2 bytes * 2 for K and V) per second.
+
+``--impl reference`` times the CPU oracle on the host cores instead (a
+bounded sample of each step's attention rows).
+
+Multi-GPU: every rank runs an independent replica of the workload (the path
+shards by sequence with no exchange); ranks meet only at the barriers, and
+the slowest rank's time sets the throughput.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode K/V read GB/s (% of GB300 HBM peak); decode steps/s per batch"
+FALLBACK_HBM_GBS = 6800.0
+SRC_FOR_TRAFFIC = ["paged_kv_cache_113_gb300/csrc/attention.cu", "paged_kv_cache_113_gb300/csrc/pk_device.cuh"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="mha7b", choices=["tiny", "mha7b", "gqa8b", "long", "prefix"])
+    p.add_argument("--block-size", type=int, default=None, help="prefix workload only: 8, 16 or 32")
+    p.add_argument("--partition", type=int, default=-1, help="0 = no split, -1 = auto, >0 tokens")
+    p.add_argument("--attn-impl", default="auto", choices=["auto", "simt", "mma"])
+    p.add_argument("--window", type=int, default=32, help="distinct decode steps prepared ahead and cycled")
+    p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
+    p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be at least 3")
+    return a
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_hbm_peak():
+    for path in (os.path.join(ROOT, "MEASURED_PEAKS.json"),):
+        try:
+            with open(path) as f:
+                v = float(json.load(f)["hbm_gbs"])
+            return v, "measured"
+        except (OSError, KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for rel in SRC_FOR_TRAFFIC:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if the
+    kernel source is unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            table = json.load(f)
+        e = table[workload]
+        if e.get("source_sha256") == source_hash():
+            return int(e["dram_bytes_per_step"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, uuid: str = None):
+        self.dev = uuid or str(device_index)
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="pk_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.dev, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_state(wl):
+    import oracle
+    return oracle.run_workload(wl, attention=False)
+
+
+def time_oracle_rows(wl, ref, rows: np.ndarray):
+    """Times the oracle's attention over the given (seq, head) rows; returns (seconds, kv bytes)."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"], wl.scale,
+                           wl.dtype, select=rows)
+    dt = time.perf_counter() - t0
+    ctx = ref["ctx_lens"]
+    nbytes = int(sum(int(ctx[s]) for s, _ in rows)) * wl.head_dim * wl.esz * 2
+    return dt, nbytes
+
+
+def all_rows(wl):
+    return np.array([(s, h) for s in range(wl.num_seqs) for h in range(wl.num_q_heads)], dtype=np.int32)
+
+
+def cpu_baseline(wl, ref, seconds: float):
+    """The oracle on the host cores: whole decode steps (every row), repeated
+    until the time budget is used (at least once)."""
+    rows = all_rows(wl)
+    total_t, total_b, reps = 0.0, 0, 0
+    while reps == 0 or total_t < seconds:
+        dt, nb = time_oracle_rows(wl, ref, rows)
+        total_t += dt
+        total_b += nb
+        reps += 1
+        if total_t > 4 * seconds:
+            break
+    return {"value": total_b / total_t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full decode step(s) of attention ({len(rows)} rows each), single-threaded C, fp64"}
+
+
+def workload_config(wl, args, extra=None):
+    c = {"workload": wl.name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+         "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+         "num_blocks": wl.num_blocks, "kv_dtype": wl.dtype, "ctx_mean": round(float(np.mean(wl.ctx_lens)), 1),
+         "ctx_max": int(np.max(wl.ctx_lens)), "seed": wl.seed, "parallelism": f"replicas{args.gpus}"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import make_workload
+    wl = make_workload(args.workload, block_size=args.block_size)
+    ref = oracle_state(wl)
+    rows = all_rows(wl)
+    rng = np.random.default_rng(0)
+    # Calibrate the per-row cost on a few rows, then size each step's sample
+    # so that warm-up plus timed steps fit the time budget.
+    probe = rows[rng.choice(len(rows), size=min(16, len(rows)), replace=False)]
+    dt, _ = time_oracle_rows(wl, ref, probe)
+    per_row = dt / len(probe)
+    budget = args.reference_seconds / (args.steps + args.warmup)
+    n = int(max(1, min(len(rows), budget / max(per_row, 1e-9))))
+    samples = [rows[rng.choice(len(rows), size=n, replace=False)] for _ in range(args.steps + args.warmup)]
+    for i in range(args.warmup):
+        time_oracle_rows(wl, ref, samples[i])
+    tt, tb = 0.0, 0
+    for i in range(args.steps):
+        dt, nb = time_oracle_rows(wl, ref, samples[args.warmup + i])
+        tt += dt
+        tb += nb
+    gbs = tb / tt / 1e9
+    frac = n / len(rows)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps / frac,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, args, {"sample_rows_per_step": n, "rows_per_step": len(rows)}),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} of {len(rows)} attention rows per step (random), single-threaded C, fp64; "
+                                   "ms_per_step scaled to all rows"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import paged_kv_cache_113_gb300 as pk
+    from paged_kv_cache_113_gb300.harness import DecodeState
+    from workloads import make_workload
+
+    if rank == 0:
+        pk.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pk.lib()
+
+    wl = make_workload(args.workload, block_size=args.block_size)
+    wl.enable_memo()
+    R = max(1, min(args.window, args.steps + args.warmup))
+    E = 0 if args.no_e2e else max(1, args.e2e_steps)
+    Ew = 0 if args.no_e2e else 3
+    st = DecodeState(wl, dev, extra_tokens=R + E + Ew + 1)
+    host_steps = [st.prepare_step() for _ in range(R)]
+    dsteps = [st.upload(si) for si in host_steps]
+    step_bytes = [wl.kv_bytes(si.ctx_lens) for si in host_steps]
+    max_ctx = max(si.max_context_len for si in host_steps) + E + Ew + 1
+    ws = st.alloc_workspace(max_ctx, args.partition)
+    out = st.new_out()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def launches(si):
+        part = st.resolve_partition(si.max_context_len, args.partition)
+        split = part > 0 and math.ceil(si.max_context_len / part) > 1
+        return (1 if len(si.pairs) else 0) + 2 + (1 if split else 0)
+
+    # warm-up
+    for i in range(args.warmup):
+        flush.zero_()
+        st.run_step(dsteps[i % R], out, ws, args.partition, args.attn_impl)
+    torch.cuda.synchronize()
+    kind, _ = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error during warm-up: {pk.DEVERR_NAMES.get(kind)}")
+
+    sampler = None
+    if not args.no_clocks:
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            uuid = None
+        sampler = ClockSampler(local_rank, uuid)
+        sampler.start()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    n_launch = 0
+    total_bytes = 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        j = (args.warmup + i) % R
+        d = dsteps[j]
+        e0, e1, e2 = ev[i]
+        e0.record()
+        if d["pairs"].shape[0]:
+            pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
+        pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
+        e1.record()
+        st.attention(d, out, ws, args.partition, args.attn_impl)
+        e2.record()
+        n_launch += launches(host_steps[j])
+        total_bytes += step_bytes[j]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attn_ms = [b.elapsed_time(c) for _, b, c in ev]
+    t_step = sum(step_ms) / 1e3
+    t_attn = sum(attn_ms) / 1e3
+    kind, idx = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error in the timed steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
+
+    if world > 1:
+        t = torch.tensor([t_step, t_attn], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_step, t_attn = float(t[0]), float(t[1])
+
+    value = world * total_bytes / t_step / 1e9
+    attn_gbs = total_bytes / t_attn / 1e9
+    peak, peak_kind = measured_hbm_peak()
+
+    e2e = None
+    if E:
+        e2e = run_e2e(st, wl, E, Ew, args, dev)
+        if world > 1:
+            t = torch.tensor([e2e["_seconds"]], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e["value"] = world * e2e["_bytes"] / float(t[0]) / 1e9
+        e2e.pop("_seconds")
+        e2e.pop("_bytes")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ref = oracle_state(wl)
+        cpu = cpu_baseline(wl, ref, args.cpu_seconds)
+
+    part = st.resolve_partition(max(si.max_context_len for si in host_steps), args.partition)
+    mean_ms = 1e3 * t_step / args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms, "steps_per_s": 1e3 / mean_ms,
+            "pct_of_peak": 100.0 * value / world / peak, "peak_kind": peak_kind,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": workload_config(wl, args, {
+                "partition": part, "attn_impl": args.attn_impl, "window_steps": R,
+                "l2": "flushed between steps (write of 2x L2, outside the step events)",
+                "kv_bytes_per_step_mean": total_bytes / args.steps}),
+            "roofline": {"bound": "hbm", "kernel": "paged attention (attn_*_kernel + merge when split)",
+                         "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "traffic": ncu_traffic(wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"),
+                         "bytes_per_launch": total_bytes / args.steps, "ms_per_launch": 1e3 * t_attn / args.steps},
+            "attention_gbs": attn_gbs,
+            "gpu_launches": n_launch,
+            "wall_s_timed_region": wall,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(st, wl, E, Ew, args, dev):
+    """The same decode steps through the public API from pinned host memory."""
+    import torch
+    import paged_kv_cache_113_gb300 as pk
+    S = wl.num_seqs
+    tdt = st.torch_dtype
+
+    def pinned_from(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16" \
+            else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+        return t.pin_memory()
+
+    steps = [wl.step_inputs(10_000 + i) for i in range(E + Ew)]
+    hq = [pinned_from(q) for q, _, _ in steps]
+    hk = [pinned_from(k) for _, k, _ in steps]
+    hv = [pinned_from(v) for _, _, v in steps]
+    h_tables = torch.empty((S, st.max_blocks), dtype=torch.int32).pin_memory()
+    h_lens = torch.empty(S, dtype=torch.int32).pin_memory()
+    h_slots = torch.empty(S, dtype=torch.int64).pin_memory()
+    h_pairs = torch.empty((S, 2), dtype=torch.int64).pin_memory()
+    h_out = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt).pin_memory()
+    d_q = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt, device=dev)
+    d_k = torch.empty((S, wl.num_kv_heads, wl.head_dim), dtype=tdt, device=dev)
+    d_v = torch.empty_like(d_k)
+    d_tables = torch.empty((S, st.max_blocks), dtype=torch.int32, device=dev)
+    d_lens = torch.empty(S, dtype=torch.int32, device=dev)
+    d_slots = torch.empty(S, dtype=torch.int64, device=dev)
+    d_pairs = torch.empty((S, 2), dtype=torch.int64, device=dev)
+    d_out = torch.empty_like(h_out, device=dev)
+    tables_np, lens_np = h_tables.numpy(), h_lens.numpy()
+    seq_ids = np.arange(S, dtype=np.int64)
+    stream = torch.cuda.current_stream()
+    bytes_h2d = 0
+    tot_t, tot_b = 0.0, 0
+    max_ctx_bound = int(wl.ctx_lens.max()) + st.steps_done + E + Ew + 1
+    ws = st.alloc_workspace(max_ctx_bound, args.partition)
+    for i in range(E + Ew):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        slots, pairs = st.bm.append_batch(seq_ids)
+        st.bm.export_tables(seq_ids, st.max_blocks, tables_out=tables_np, lens_out=lens_np)
+        npair = len(pairs)
+        h_slots.numpy()[:] = slots
+        if npair:
+            h_pairs.numpy()[:npair] = pairs
+        d_q.copy_(hq[i], non_blocking=True)
+        d_k.copy_(hk[i], non_blocking=True)
+        d_v.copy_(hv[i], non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_tables.copy_(h_tables, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        if npair:
+            d_pairs[:npair].copy_(h_pairs[:npair], non_blocking=True)
+            pk.pk_copy_blocks(st.k_cache, st.v_cache, d_pairs[:npair])
+        pk.pk_reshape_and_cache(d_k, d_v, d_slots, st.k_cache, st.v_cache)
+        mc = int(lens_np.max())
+        pk.pk_paged_attention_decode(d_out, d_q, st.k_cache, st.v_cache, d_tables, d_lens, wl.scale, mc,
+                                     args.partition, ws, args.attn_impl)
+        h_out.copy_(d_out, non_blocking=True)
+        stream.synchronize()
+        dt = time.perf_counter() - t0
+        st.steps_done += 1
+        if i >= Ew:
+            tot_t += dt
+            tot_b += wl.kv_bytes(lens_np)
+            bytes_h2d = (hq[i].numel() * hq[i].element_size() + hk[i].numel() * hk[i].element_size()
+                         + hv[i].numel() * hv[i].element_size() + S * 8 + npair * 16 + h_tables.numel() * 4 + S * 4)
+    kind, idx = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error in the e2e steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
+    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(bytes_h2d),
+            "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "steps": E,
+            "ms_per_step": 1e3 * tot_t / E, "includes": "host block-manager append + table export, H2D, kernels, D2H",
+            "_seconds": tot_t, "_bytes": tot_b}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

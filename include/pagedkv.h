@@ -1,0 +1,247 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: decode-time paged attention on GB300.
+ *
+ * A sequence's key/value cache is split into fixed-size blocks of B token
+ * slots. The blocks live in one shared pool and are reached through the
+ * sequence's block table, which maps logical block index to physical block
+ * number ("Paged KV Cache Allocation and the Block Table", section "Blocks,
+ * tables, and the indirection"; "paged attention deep", section "The block
+ * table"). Token t of a sequence lives at
+ *
+ *     slot = block_table[t / B] * B + (t % B)
+ *
+ * ("The KV Cache Is an Allocator Problem", the physical-address equation).
+ *
+ * Conventions shared by every GPU entry point:
+ *   - Pool layout: k_cache and v_cache are each [num_blocks, B, Hk, d],
+ *     row-major, so a block holds K [B, Hk, d] and V [B, Hk, d] ("paged
+ *     attention deep", "Anatomy of a KV block"; the S06 listing's pool shape).
+ *   - New-token layout: k, v are [T, Hk, d]; queries and outputs [S, Hq, d].
+ *   - Query head h reads KV head h / (Hq / Hk).
+ *   - Every pointer argument of a GPU entry point is a DEVICE pointer owned
+ *     by the caller and 16-byte aligned. The library allocates no device
+ *     memory: split-K scratch is passed in by the caller.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *     enqueued asynchronously; the call returns after the launches.
+ *   - Host-side argument checks run before any launch and return a status;
+ *     nothing aborts, traps or prints. Launch failures map to PK_ERR_CUDA.
+ *   - Device-side bounds checks (slot, block id, pair, context length) never
+ *     touch memory out of range: the offending access is skipped and the
+ *     first such event is recorded in a device error word, read back with
+ *     pk_get_device_error().
+ *
+ * The host block manager (pk_bm_*) owns only host memory and is not
+ * thread-safe: one handle per thread, or external locking.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PK_OK = 0,
+    PK_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, bad layout      */
+    PK_ERR_UNSUPPORTED = 2,   /* valid but not compiled: dtype, head_dim, B, group size */
+    PK_ERR_OUT_OF_BLOCKS = 3, /* the pool cannot supply the blocks; state unchanged     */
+    PK_ERR_UNKNOWN_SEQ = 4,   /* no sequence with that id                               */
+    PK_ERR_SEQ_EXISTS = 5,    /* a sequence with that id already exists                 */
+    PK_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed                   */
+    PK_ERR_WORKSPACE = 7,     /* split-K workspace missing or too small                 */
+    PK_ERR_INVARIANT = 8,     /* pk_bm_check_invariants found a violation               */
+    PK_ERR_NOMEM = 9          /* host allocation failed                                 */
+} pk_status;
+
+typedef enum { PK_F32 = 0, PK_BF16 = 1 } pk_dtype;
+
+/* Attention kernel choice. AUTO picks the tensor-core kernel for bf16 when it
+ * is compiled for the shape and the CUDA-core kernel otherwise. */
+typedef enum { PK_ATTN_AUTO = 0, PK_ATTN_SIMT = 1, PK_ATTN_MMA = 2 } pk_attn_impl;
+
+/* Device error word layout: (kind << 24) | (low 24 bits of the offending index). */
+enum {
+    PK_DEVERR_NONE = 0,
+    PK_DEVERR_SLOT = 1,        /* slot_mapping entry >= num_blocks * B                 */
+    PK_DEVERR_BLOCK_ID = 2,    /* block table entry outside [0, num_blocks)            */
+    PK_DEVERR_PAIR = 3,        /* copy_blocks pair outside [0, num_blocks)             */
+    PK_DEVERR_CONTEXT = 4,     /* context_lens entry < 1 or beyond the table / bound   */
+    PK_DEVERR_TIMEOUT = 5      /* a pipeline wait gave up (never expected)             */
+};
+
+/* Geometry of one layer's KV pool. */
+typedef struct {
+    int32_t num_blocks;   /* N: physical blocks in the pool          */
+    int32_t block_size;   /* B: token slots per block                */
+    int32_t num_kv_heads; /* Hk                                      */
+    int32_t head_dim;     /* d                                       */
+    pk_dtype dtype;       /* element type of caches, q, k, v and out */
+} pk_cache_desc;
+
+/* ------------------------------------------------------------------------ */
+/* GPU entry points                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Slot scatter: for each new token i with s = slot_mapping[i] >= 0,
+ *     k_cache[s / B, s % B, :, :] = k[i, :, :]   and the same for v.
+ * Negative slots are skipped. ("Paged KV Cache Allocation and the Block
+ * Table", the append_token routine: the token's K/V are written at
+ * physical * block_size + slot.)
+ *   k, v          [num_tokens, Hk, d] contiguous, dtype of the pool.
+ *   slot_mapping  int64 [num_tokens]; duplicate slots in one call race.
+ *   num_tokens    >= 0 (0 is a no-op).
+ * Out-of-range slots are skipped and recorded (PK_DEVERR_SLOT). */
+pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot_mapping,
+                               int32_t num_tokens, void *k_cache, void *v_cache,
+                               const pk_cache_desc *desc, void *stream);
+
+/* Copy-on-write block copy: for each pair p, the whole block src = pairs[2p]
+ * is copied to dst = pairs[2p+1] in both k_cache and v_cache (all B slots, all
+ * heads). ("paged attention deep", "Copy-on-write for shared prefixes": the
+ * writer gets a private copy of the single shared block; "Paged KV Cache
+ * Allocation and the Block Table", "Sharing blocks between sequences".)
+ *   src_dst_pairs int64 [num_pairs][2]. Precondition: the dst blocks are
+ *                 distinct and no dst is also a src in the same call.
+ * Must be enqueued before the scatter that writes into dst.
+ * Out-of-range ids are skipped and recorded (PK_DEVERR_PAIR). */
+pk_status pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
+                         int32_t num_pairs, const pk_cache_desc *desc, void *stream);
+
+/* Decode attention through the block table ("PagedAttention", S06, the
+ * paged_attention listing and "Why this needed a custom CUDA kernel": the
+ * table lookup happens inside the kernel, no pre-gather). For each sequence
+ * s and query head h, with n = context_lens[s] and kvh = h / (Hq / Hk):
+ *     x_t = scale * <q[s,h,:], K[table[s][t/B], t%B, kvh, :]>     t < n
+ *     out[s,h,:] = sum_t softmax(x)_t * V[table[s][t/B], t%B, kvh, :]
+ *   out           [S, Hq, d], dtype of q (fp32 accumulation inside).
+ *   q             [S, Hq, d].
+ *   block_tables  int32 [S, max_blocks_per_seq]; entries at or beyond
+ *                 ceil(n / B) are never read.
+ *   context_lens  int32 [S], each in [1, min(max_context_len, max_blocks*B)];
+ *                 the length after the step's token has been scattered.
+ *   max_context_len  host-side upper bound on context_lens (sizes the grid).
+ *   partition_size   0: one partition per sequence (no split-K);
+ *                    -1: automatic; > 0: split each context into partitions
+ *                    of this many tokens (a multiple of B), merged with a
+ *                    log-sum-exp reduction.
+ *   workspace        device scratch of at least
+ *                    pk_paged_attention_workspace_size(...) bytes when the
+ *                    chosen partitioning splits; may be NULL otherwise.
+ * A context length outside its bounds is clamped and recorded
+ * (PK_DEVERR_CONTEXT); a bad table entry is recorded (PK_DEVERR_BLOCK_ID). */
+pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_tables,
+                                    const int32_t *context_lens, float scale, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                    int32_t max_context_len, int32_t partition_size,
+                                    void *workspace, size_t workspace_bytes,
+                                    const pk_cache_desc *desc, void *stream);
+
+/* As pk_paged_attention_decode, with the kernel chosen explicitly
+ * (PK_ERR_UNSUPPORTED if that kernel is not compiled for the shape). */
+pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, float scale,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len,
+                                         int32_t partition_size, void *workspace,
+                                         size_t workspace_bytes, const pk_cache_desc *desc,
+                                         pk_attn_impl impl, void *stream);
+
+/* The partition size (in tokens) that a partition_size argument resolves to
+ * for this shape: 0 means no split. Host only, no GPU needed. */
+int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t max_context_len, int32_t partition_size,
+                                             const pk_cache_desc *desc);
+
+/* Bytes of split-K workspace pk_paged_attention_decode needs for these
+ * arguments (0 when the resolved partitioning does not split). Layout inside:
+ * fp32 partial outputs [S, Hq, P, d], then running maxima and sums [S, Hq, P]
+ * each, P = ceil(max_context_len / partition). Host only. */
+size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, int32_t partition_size,
+                                         const pk_cache_desc *desc);
+
+/* Reads the device error word of the current device into *code_out (0 = no
+ * error; see PK_DEVERR_*) after synchronising `stream`, then clears it. */
+pk_status pk_get_device_error(int32_t *code_out, void *stream);
+
+/* A static, NUL-terminated description of a status. */
+const char *pk_status_string(pk_status status);
+
+/* ------------------------------------------------------------------------ */
+/* Host block manager                                                       */
+/* ------------------------------------------------------------------------ */
+/* Free list, per-sequence block tables, reference counts, fork and
+ * copy-on-write ("Paged KV Cache Allocation and the Block Table", the
+ * append_token routine and "Sharing blocks between sequences"; "PagedAttention",
+ * S06, the BlockManager listing and "Reference counts must be exact").
+ * The free list is a stack: its first pop is alloc_order[0]; a retired
+ * sequence's blocks whose count reaches zero are pushed in table order. */
+typedef struct pk_bm pk_bm;
+
+/* alloc_order: a permutation of 0..num_blocks-1 (copied), or NULL for
+ * 0, 1, 2, ... On success *out owns a new manager. */
+pk_status pk_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *alloc_order,
+                       pk_bm **out);
+void pk_bm_destroy(pk_bm *bm);
+
+pk_status pk_bm_add_seq(pk_bm *bm, int64_t seq_id);
+
+/* Appends n >= 0 tokens to seq_id. slots_out[i] (int64, n entries) receives
+ * token i's slot. When the sequence's first new token falls into a partly
+ * filled tail block shared with another table, the block is copied first:
+ * the (src, dst) pair goes to cow_pairs_out[0..1] and *n_cow_out = 1 (else
+ * 0); the caller must run pk_copy_blocks on it before the scatter. All or
+ * nothing: PK_ERR_OUT_OF_BLOCKS leaves the manager unchanged. */
+pk_status pk_bm_append_slots(pk_bm *bm, int64_t seq_id, int32_t n, int64_t *slots_out,
+                             int64_t *cow_pairs_out, int32_t *n_cow_out);
+
+/* One decode step's host side: appends one token to each of seq_ids[0..n-1]
+ * in order. slots_out [n] gets the slots; cow_pairs_out [n][2] gets the copy
+ * pairs in order and *n_cow_out their count. All or nothing over the batch. */
+pk_status pk_bm_append_batch(pk_bm *bm, const int64_t *seq_ids, int32_t n, int64_t *slots_out,
+                             int64_t *cow_pairs_out, int32_t *n_cow_out);
+
+/* child gets the parent's table and length; every block's count goes up. */
+pk_status pk_bm_fork(pk_bm *bm, int64_t parent, int64_t child);
+
+/* Decrements every block of the table; blocks reaching zero return to the
+ * free list. */
+pk_status pk_bm_free_seq(pk_bm *bm, int64_t seq_id);
+
+pk_status pk_bm_seq_len(const pk_bm *bm, int64_t seq_id, int64_t *len_out);
+
+/* Copies up to cap entries of the table; *len_out = its full length. */
+pk_status pk_bm_block_table(const pk_bm *bm, int64_t seq_id, int32_t *out, int32_t cap,
+                            int32_t *len_out);
+
+/* Row i of tables_out [n][max_blocks] = the table of seq_ids[i], padded with
+ * -1; lens_out[i] (int32) = its token count. PK_ERR_INVALID_ARG if a table is
+ * longer than max_blocks. */
+pk_status pk_bm_export_tables(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
+                              int32_t max_blocks, int32_t *tables_out, int32_t *lens_out);
+
+int32_t pk_bm_num_free(const pk_bm *bm);
+int32_t pk_bm_refcount(const pk_bm *bm, int32_t block); /* -1 if out of range */
+
+/* Recounts every block's references from the tables and checks: counts
+ * match, no named block is free, no block is lost or listed twice, and each
+ * table holds ceil(len / B) blocks. PK_ERR_INVARIANT on the first violation. */
+pk_status pk_bm_check_invariants(const pk_bm *bm);
+
+/* live_tokens: sum of sequence lengths; reserved_slots: B * (blocks in use);
+ * tail_waste: sum over sequences of B*ceil(len/B) - len; shared_blocks:
+ * blocks with refcount > 1; cow_copies: copy-on-write copies so far. Any
+ * output pointer may be NULL. */
+pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_slots,
+                      int64_t *tail_waste, int32_t *shared_blocks, int64_t *cow_copies);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

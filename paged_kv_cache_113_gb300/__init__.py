@@ -1,0 +1,345 @@
+"""Python binding of libpagedkv: decode-time paged attention for GB300.
+
+Argument marshalling only. Every step of the path runs in the CUDA library
+``libpagedkv.so`` (built in-tree by :func:`build`); there is no CPU or
+PyTorch fallback, and every entry point raises if the library is missing.
+The functions carry the C ABI's names (``include/pagedkv.h``):
+
+* :func:`pk_reshape_and_cache` -- scatter new tokens' K/V into their slots;
+* :func:`pk_copy_blocks` -- copy-on-write block copies;
+* :func:`pk_paged_attention_decode` -- attention through the block tables,
+  with optional split-K partitions merged by log-sum-exp;
+* :class:`BlockManager` -- the host block manager (free list, refcounts,
+  fork, copy-on-write, block tables, slot mappings).
+
+PyTorch provides device memory and streams: the device entry points take
+CUDA tensors and enqueue on the current stream unless one is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+from ._build import LIB_PATH, build
+
+__all__ = [
+    "build", "lib", "PagedKVError", "CacheDesc", "cache_desc",
+    "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
+    "pk_paged_attention_workspace_size", "pk_paged_attention_resolve_partition",
+    "pk_get_device_error", "pk_status_string", "BlockManager",
+    "PK_F32", "PK_BF16", "IMPLS", "DEVERR_NAMES",
+]
+
+PK_OK, PK_ERR_INVALID_ARG, PK_ERR_UNSUPPORTED, PK_ERR_OUT_OF_BLOCKS = 0, 1, 2, 3
+PK_ERR_UNKNOWN_SEQ, PK_ERR_SEQ_EXISTS, PK_ERR_CUDA, PK_ERR_WORKSPACE = 4, 5, 6, 7
+PK_ERR_INVARIANT, PK_ERR_NOMEM = 8, 9
+PK_F32, PK_BF16 = 0, 1
+IMPLS = {"auto": 0, "simt": 1, "mma": 2}
+DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5: "timeout"}
+
+# Every symbol include/pagedkv.h declares.
+EXPORTED = (
+    "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
+    "pk_paged_attention_decode_impl", "pk_paged_attention_resolve_partition",
+    "pk_paged_attention_workspace_size", "pk_get_device_error", "pk_status_string",
+    "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
+    "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
+    "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
+)
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {pk_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpagedkv; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libpagedkv is not built ({LIB_PATH} missing): call "
+                           "paged_kv_cache_113_gb300.build() first")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    D = ctypes.POINTER(CacheDesc)
+    sigs = {
+        "pk_reshape_and_cache": (i32, [P, P, P, i32, P, P, D, P]),
+        "pk_copy_blocks": (i32, [P, P, P, i32, D, P]),
+        "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D, P]),
+        "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
+                                                 i32, P]),
+        "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
+        "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
+        "pk_get_device_error": (i32, [P, P]),
+        "pk_status_string": (ctypes.c_char_p, [i32]),
+        "pk_bm_create": (i32, [i32, i32, P, P]),
+        "pk_bm_destroy": (None, [P]),
+        "pk_bm_add_seq": (i32, [P, i64]),
+        "pk_bm_append_slots": (i32, [P, i64, i32, P, P, P]),
+        "pk_bm_append_batch": (i32, [P, P, i32, P, P, P]),
+        "pk_bm_fork": (i32, [P, i64, i64]),
+        "pk_bm_free_seq": (i32, [P, i64]),
+        "pk_bm_seq_len": (i32, [P, i64, P]),
+        "pk_bm_block_table": (i32, [P, i64, P, i32, P]),
+        "pk_bm_export_tables": (i32, [P, P, i32, i32, P, P]),
+        "pk_bm_num_free": (i32, [P]),
+        "pk_bm_refcount": (i32, [P, i32]),
+        "pk_bm_check_invariants": (i32, [P]),
+        "pk_bm_stats": (i32, [P, P, P, P, P, P]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def pk_status_string(status: int) -> str:
+    return lib().pk_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != PK_OK:
+        raise PagedKVError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# Device entry points (torch tensors)
+# ---------------------------------------------------------------------------
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return PK_F32
+    if t.dtype == torch.bfloat16:
+        return PK_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: libpagedkv takes float32 or bfloat16")
+
+
+def cache_desc(k_cache) -> CacheDesc:
+    """The pool descriptor of a ``[num_blocks, B, Hk, d]`` cache tensor."""
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [num_blocks, block_size, num_kv_heads, head_dim]")
+    N, B, Hk, d = k_cache.shape
+    return CacheDesc(int(N), int(B), int(Hk), int(d), _dtype_code(k_cache))
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libpagedkv has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def pk_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """Writes token i's K/V ``[T, Hk, d]`` into slot ``slot_mapping[i]`` (int64)."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    T = int(k.shape[0])
+    if tuple(k.shape) != (T, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise ValueError("k and v must be [num_tokens, num_kv_heads, head_dim]")
+    if k.dtype != k_cache.dtype or v.dtype != k_cache.dtype or v_cache.dtype != k_cache.dtype:
+        raise TypeError("k, v, k_cache and v_cache must share one dtype")
+    if v_cache.shape != k_cache.shape or tuple(slot_mapping.shape) != (T,):
+        raise ValueError("shape mismatch")
+    _check(lib().pk_reshape_and_cache(_dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64),
+                                      T, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                      ctypes.byref(desc), _stream(stream)), "pk_reshape_and_cache")
+
+
+def pk_copy_blocks(k_cache, v_cache, src_dst_pairs, stream=None):
+    """Copies whole blocks ``src_dst_pairs[p] = (src, dst)`` (int64 ``[n, 2]``) in K and V."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    n = int(src_dst_pairs.shape[0]) if src_dst_pairs.numel() else 0
+    if n and tuple(src_dst_pairs.shape) != (n, 2):
+        raise ValueError("src_dst_pairs must be [num_pairs, 2]")
+    if n == 0:
+        return
+    _check(lib().pk_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                _dev(src_dst_pairs, "src_dst_pairs", torch.int64), n, ctypes.byref(desc),
+                                _stream(stream)), "pk_copy_blocks")
+
+
+def pk_paged_attention_resolve_partition(num_seqs, num_q_heads, max_context_len, partition_size, desc) -> int:
+    return int(lib().pk_paged_attention_resolve_partition(int(num_seqs), int(num_q_heads), int(max_context_len),
+                                                          int(partition_size), ctypes.byref(desc)))
+
+
+def pk_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len, partition_size, desc) -> int:
+    return int(lib().pk_paged_attention_workspace_size(int(num_seqs), int(num_q_heads), int(max_context_len),
+                                                       int(partition_size), ctypes.byref(desc)))
+
+
+def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                              max_context_len: int, partition_size: int = -1, workspace=None,
+                              impl: str = "auto", stream=None):
+    """Decode attention through the block tables; writes ``out`` ``[S, Hq, d]``.
+
+    ``block_tables`` int32 ``[S, max_blocks]``, ``context_lens`` int32 ``[S]``
+    (lengths after the step token). ``partition_size``: 0 = no split, -1 =
+    automatic, >0 = split-K partition in tokens. ``workspace``: a CUDA tensor
+    of at least :func:`pk_paged_attention_workspace_size` bytes when the
+    partitioning splits.
+    """
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    S, Hq, d = (int(x) for x in q.shape)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out and q must be [num_seqs, num_q_heads, head_dim] of the cache dtype")
+    if d != desc.head_dim or block_tables.dim() != 2 or int(block_tables.shape[0]) != S:
+        raise ValueError("shape mismatch")
+    if tuple(context_lens.shape) != (S,):
+        raise ValueError("context_lens must be [num_seqs]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    if impl not in IMPLS:
+        raise ValueError(f"impl must be one of {sorted(IMPLS)}")
+    _check(lib().pk_paged_attention_decode_impl(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+        float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+        ws_ptr, ws_bytes, ctypes.byref(desc), IMPLS[impl], _stream(stream)), "pk_paged_attention_decode")
+
+
+def pk_get_device_error(stream=None) -> Tuple[int, int]:
+    """Synchronises the stream, reads and clears the device error word.
+
+    Returns ``(kind, index)``: kind 0 means no error (see DEVERR_NAMES).
+    """
+    code = ctypes.c_int32(0)
+    _check(lib().pk_get_device_error(ctypes.byref(code), _stream(stream)), "pk_get_device_error")
+    return code.value >> 24, code.value & 0xFFFFFF
+
+
+# ---------------------------------------------------------------------------
+# Host block manager
+# ---------------------------------------------------------------------------
+def _np_ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+class BlockManager:
+    """Host block manager (``pk_bm_*``): free list, refcounts, fork, CoW."""
+
+    def __init__(self, num_blocks: int, block_size: int, alloc_order: Optional[np.ndarray] = None):
+        self._L = lib()
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = None if alloc_order is None else np.ascontiguousarray(alloc_order, dtype=np.int32)
+        if order is not None and order.shape != (self.num_blocks,):
+            raise ValueError("alloc_order must hold num_blocks entries")
+        h = ctypes.c_void_p()
+        _check(self._L.pk_bm_create(self.num_blocks, self.block_size, _np_ptr(order), ctypes.byref(h)),
+               "pk_bm_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._L.pk_bm_destroy(h)
+            self._h = None
+
+    def add_seq(self, seq: int):
+        _check(self._L.pk_bm_add_seq(self._h, int(seq)), "pk_bm_add_seq")
+
+    def append(self, seq: int, n: int):
+        """Appends n tokens; returns (slots int64[n], (src, dst) CoW pair or None)."""
+        slots = np.empty(max(int(n), 1), np.int64)
+        pair = np.zeros(2, np.int64)
+        ncow = ctypes.c_int32(0)
+        _check(self._L.pk_bm_append_slots(self._h, int(seq), int(n), _np_ptr(slots), _np_ptr(pair),
+                                          ctypes.byref(ncow)), "pk_bm_append_slots")
+        return slots[: int(n)], ((int(pair[0]), int(pair[1])) if ncow.value else None)
+
+    def append_batch(self, seqs: Sequence[int]):
+        """One token for each sequence in order; returns (slots [n], pairs [k, 2])."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = len(ids)
+        slots = np.empty(max(n, 1), np.int64)
+        pairs = np.empty((max(n, 1), 2), np.int64)
+        ncow = ctypes.c_int32(0)
+        _check(self._L.pk_bm_append_batch(self._h, _np_ptr(ids), n, _np_ptr(slots), _np_ptr(pairs),
+                                          ctypes.byref(ncow)), "pk_bm_append_batch")
+        return slots[:n], pairs[: ncow.value].copy()
+
+    def fork(self, parent: int, child: int):
+        _check(self._L.pk_bm_fork(self._h, int(parent), int(child)), "pk_bm_fork")
+
+    def free_seq(self, seq: int):
+        _check(self._L.pk_bm_free_seq(self._h, int(seq)), "pk_bm_free_seq")
+
+    def seq_len(self, seq: int) -> int:
+        n = ctypes.c_int64(0)
+        _check(self._L.pk_bm_seq_len(self._h, int(seq), ctypes.byref(n)), "pk_bm_seq_len")
+        return int(n.value)
+
+    def table(self, seq: int) -> np.ndarray:
+        n = ctypes.c_int32(0)
+        _check(self._L.pk_bm_block_table(self._h, int(seq), None, 0, ctypes.byref(n)), "pk_bm_block_table")
+        out = np.empty(max(n.value, 1), np.int32)
+        _check(self._L.pk_bm_block_table(self._h, int(seq), _np_ptr(out), n.value, ctypes.byref(n)),
+               "pk_bm_block_table")
+        return out[: n.value]
+
+    def export_tables(self, seqs: Sequence[int], max_blocks: int,
+                      tables_out: Optional[np.ndarray] = None, lens_out: Optional[np.ndarray] = None):
+        """Padded int32 tables ``[n, max_blocks]`` (pad -1) and int32 lengths ``[n]``."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = len(ids)
+        tables = np.empty((n, max_blocks), np.int32) if tables_out is None else tables_out
+        lens = np.empty(n, np.int32) if lens_out is None else lens_out
+        assert tables.dtype == np.int32 and tables.flags.c_contiguous and tables.shape == (n, max_blocks)
+        assert lens.dtype == np.int32 and lens.shape == (n,)
+        _check(self._L.pk_bm_export_tables(self._h, _np_ptr(ids), n, int(max_blocks), _np_ptr(tables),
+                                           _np_ptr(lens)), "pk_bm_export_tables")
+        return tables, lens
+
+    def num_free(self) -> int:
+        return int(self._L.pk_bm_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._L.pk_bm_refcount(self._h, int(block)))
+
+    def check_invariants(self):
+        _check(self._L.pk_bm_check_invariants(self._h), "pk_bm_check_invariants")
+
+    def stats(self) -> dict:
+        live, res, waste, cow = (ctypes.c_int64(0) for _ in range(4))
+        shared = ctypes.c_int32(0)
+        _check(self._L.pk_bm_stats(self._h, ctypes.byref(live), ctypes.byref(res), ctypes.byref(waste),
+                                   ctypes.byref(shared), ctypes.byref(cow)), "pk_bm_stats")
+        return {"live_tokens": live.value, "reserved_slots": res.value, "tail_waste": waste.value,
+                "shared_blocks": shared.value, "cow_copies": cow.value}

@@ -1,0 +1,728 @@
+// Decode-time paged attention of libpagedkv.
+//
+// Each sequence's single new query attends over its cached keys and values,
+// which sit in fixed-size blocks of a shared pool and are reached through the
+// sequence's block table: token t is slot t % B of physical block
+// table[t / B] ("paged attention deep", "The block table"). The table lookup
+// happens inside the kernel; nothing is gathered beforehand ("PagedAttention"
+// S06, "Why this needed a custom CUDA kernel"). What is computed is the plain
+// softmax attention of the S06 paged_attention listing; the kernels only
+// re-associate it (an online softmax over tiles, and optionally split-K
+// partitions merged with a log-sum-exp reduction).
+//
+// Kernels:
+//   attn_mma_kernel   bf16. One CTA per (KV head, sequence, partition) serves
+//                     all G query heads of the group. A producer warp streams
+//                     the K and V rows of each block of the partition into a
+//                     ring of shared-memory stages with TMA tensor loads (the
+//                     physical block id from the table is the TMA coordinate),
+//                     128-byte swizzled. Consumer warps each take 16 tokens
+//                     per stage: S^T = K Q^T and O^T += V^T P^T on the tensor
+//                     cores (mma.sync m16n8k16, tokens as M, the group's heads
+//                     as N), with an online softmax in registers.
+//   attn_simt_kernel  fp32 or bf16 on CUDA cores: one warp per token,
+//                     shuffle-reduced dot products, online softmax.
+//   attn_merge_kernel log-sum-exp merge of the split-K partials.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pagedkv.h"
+#include "pk_device.cuh"
+
+namespace {
+
+__device__ int g_attn_error;
+
+constexpr int kMaxGroup = 8;
+
+struct AttnParams {
+  void *out;                 // [S, Hq, D] (dtype of q)
+  const void *q;             // [S, Hq, D]
+  const void *k_cache;       // [N, B, Hk, D]
+  const void *v_cache;       // [N, B, Hk, D]
+  const int32_t *tables;     // [S, max_blocks]
+  const int32_t *ctx_lens;   // [S]
+  float *ws_acc;             // [S, Hq, P, D] unnormalised partial outputs
+  float *ws_m;               // [S, Hq, P] running maxima (log2 domain)
+  float *ws_l;               // [S, Hq, P] softmax denominators
+  float scale_log2;          // scale * log2(e)
+  int32_t num_seqs, num_q_heads, num_kv_heads, group;
+  int32_t block_size, max_blocks, num_blocks;
+  int32_t partition;         // tokens per partition
+  int32_t num_partitions;    // P (1 = no split: write `out` directly)
+};
+
+// Context length of sequence s, clamped to what the table and the grid can
+// hold. Invalid lengths are recorded once (by the CTA for partition 0, head 0).
+__device__ __forceinline__ int context_len(const AttnParams &p, int s, bool record) {
+  int c = __ldg(p.ctx_lens + s);
+  const int cap = min(p.max_blocks * p.block_size, p.num_partitions * p.partition);
+  if (c < 1 || c > cap) {
+    if (record) pk::record_error(&g_attn_error, PK_DEVERR_CONTEXT, s);
+    c = c < 1 ? 0 : cap;
+  }
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// CUDA-core kernel (fp32 and bf16): one warp per token, lanes split the head
+// dimension, dot products reduced with shuffles, online softmax per head.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
+  constexpr int NW = 4;
+  constexpr int EPL = D / 32;  // elements per lane
+  const int kvh = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
+
+  if (ctx == 0) {  // invalid length: zero output (split mode: the merge writes it)
+    if (p.num_partitions == 1 && part == 0)
+      for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
+        pk::store_elem(static_cast<T *>(p.out) +
+                           (size_t(s) * p.num_q_heads + kvh * G + idx / D) * D + idx % D,
+                       0.0f);
+    return;
+  }
+  const int start = part * p.partition;
+  if (start >= ctx) return;
+  const int end = min(ctx, start + p.partition);
+
+  float qv[kMaxGroup][EPL];
+  float m[kMaxGroup], l[kMaxGroup], acc[kMaxGroup][EPL];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      acc[g][e] = 0.0f;
+      qv[g][e] = 0.0f;
+      if (g < G)
+        qv[g][e] = pk::load_elem(static_cast<const T *>(p.q) +
+                                 (size_t(s) * p.num_q_heads + kvh * G + g) * D + lane * EPL + e) *
+                   p.scale_log2;
+    }
+  }
+
+  const T *kc = static_cast<const T *>(p.k_cache);
+  const T *vc = static_cast<const T *>(p.v_cache);
+  const int32_t *trow = p.tables + size_t(s) * p.max_blocks;
+  const int B = p.block_size;
+  for (int t = start + warp; t < end; t += NW) {
+    int phys = __ldg(trow + t / B);
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_BLOCK_ID, s);
+      continue;
+    }
+    const size_t row = ((size_t(phys) * B + t % B) * p.num_kv_heads + kvh) * D + lane * EPL;
+    float kx[EPL], vx[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      kx[e] = pk::load_elem(kc + row + e);
+      vx[e] = pk::load_elem(vc + row + e);
+    }
+#pragma unroll
+    for (int g = 0; g < kMaxGroup; ++g) {
+      if (g >= G) break;
+      float dot = 0.0f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) dot = fmaf(qv[g][e], kx[e], dot);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      const float mn = fmaxf(m[g], dot);
+      const float corr = exp2f(m[g] - mn);
+      const float w = exp2f(dot - mn);
+      l[g] = l[g] * corr + w;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[g][e] = fmaf(acc[g][e], corr, w * vx[e]);
+      m[g] = mn;
+    }
+  }
+
+  // Merge the four warps' running states.
+  __shared__ float sm_m[NW][kMaxGroup], sm_l[NW][kMaxGroup];
+  __shared__ float sm_o[NW][kMaxGroup][D];
+#pragma unroll
+  for (int g = 0; g < kMaxGroup; ++g) {
+    if (g >= G) break;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sm_o[warp][g][lane * EPL + e] = acc[g][e];
+    if (lane == 0) {
+      sm_m[warp][g] = m[g];
+      sm_l[warp][g] = l[g];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int g = idx / D, i = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w][g]);
+    float L = 0.0f, O = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(sm_m[w][g] - M);  // 0 for a warp that saw no token
+      L = fmaf(sm_l[w][g], f, L);
+      O = fmaf(sm_o[w][g][i], f, O);
+    }
+    const int h = kvh * G + g;
+    if (p.num_partitions == 1) {
+      pk::store_elem(static_cast<T *>(p.out) + (size_t(s) * p.num_q_heads + h) * D + i, O / L);
+    } else {
+      const size_t r = (size_t(s) * p.num_q_heads + h) * p.num_partitions + part;
+      p.ws_acc[r * D + i] = O;
+      if (i == 0) {
+        p.ws_m[r] = M;
+        p.ws_l[r] = L;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core kernel (bf16): TMA-staged K/V ring, mma.sync m16n8k16.
+// ---------------------------------------------------------------------------
+template <int D, int BS, int NW, int STAGES>
+struct MmaShape {
+  static constexpr int TPS = NW * 16;               // tokens per stage
+  static constexpr int BPS = TPS / BS;              // blocks per stage
+  static constexpr int HALVES = D / 64;             // 128-byte column slabs per row
+  static constexpr int SLAB_BYTES = TPS * 128;      // one slab of one stage
+  static constexpr int KV_BYTES = HALVES * SLAB_BYTES;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K then V
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int OUT_STRIDE = D + 4;          // padded row of the merge buffer
+  static constexpr int MERGE_BYTES = NW * kMaxGroup * (OUT_STRIDE + 2) * 4;
+  static constexpr int BAR_BYTES = 2 * STAGES * 8;
+  static constexpr int SMEM_BYTES = 1024 + BAR_BYTES +
+                                    (STAGES * STAGE_BYTES > MERGE_BYTES ? STAGES * STAGE_BYTES
+                                                                        : MERGE_BYTES);
+  static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
+  static_assert(BS <= TPS && TPS % BS == 0 && BPS <= 32, "block size must divide the stage");
+};
+
+template <int D, int BS, int NW, int STAGES>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    attn_mma_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap) {
+  using S = MmaShape<D, BS, NW, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = pk::smem_addr(smem_raw);
+  const uint32_t bars = (raw + 7u) & ~7u;
+  const uint32_t stages = (bars + S::BAR_BYTES + 1023u) & ~1023u;
+  auto full_bar = [&](int i) { return bars + 8u * i; };
+  auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
+
+  const int kvh = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
+  if (ctx == 0) {
+    if (p.num_partitions == 1 && part == 0)
+      for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
+        static_cast<__nv_bfloat16 *>(p.out)[(size_t(s) * p.num_q_heads + kvh * G + idx / D) * D +
+                                            idx % D] = __float2bfloat16_rn(0.0f);
+    return;
+  }
+  const int start = part * p.partition;
+  if (start >= ctx) return;
+  const int end = min(ctx, start + p.partition);
+  const int nst = (end - start + S::TPS - 1) / S::TPS;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      pk::mbar_init(full_bar(i), 1);
+      pk::mbar_init(empty_bar(i), NW);
+    }
+    pk::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      pk::prefetch_tensormap(&kmap);
+      pk::prefetch_tensormap(&vmap);
+    }
+    const int32_t *trow = p.tables + size_t(s) * p.max_blocks;
+    int issued = 0;
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % STAGES;
+      if (st >= STAGES && !pk::mbar_wait(empty_bar(slot), ((st / STAGES) - 1) & 1)) {
+        if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, s);
+        break;
+      }
+      const int tok0 = start + st * S::TPS;
+      const int nblk = min(S::BPS, (end - tok0 + BS - 1) / BS);
+      if (lane == 0)
+        pk::mbar_arrive_expect_tx(full_bar(slot), uint32_t(nblk * S::HALVES * 2 * BS * 128));
+      __syncwarp();
+      if (lane < nblk) {
+        int phys = __ldg(trow + tok0 / BS + lane);
+        if (phys < 0 || phys >= p.num_blocks) {
+          pk::record_error(&g_attn_error, PK_DEVERR_BLOCK_ID, s);
+          phys = 0;  // stay in bounds and keep the byte count; the result is flagged
+        }
+        const uint32_t kdst = stages + slot * S::STAGE_BYTES + lane * BS * 128;
+#pragma unroll
+        for (int h = 0; h < S::HALVES; ++h) {
+          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, &kmap, full_bar(slot), h * 64, kvh, phys * BS);
+          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, &vmap, full_bar(slot), h * 64,
+                          kvh, phys * BS);
+        }
+      }
+      issued = st + 1;
+    }
+    // Let every issued copy land before the warp leaves.
+    if (lane == 0)
+      for (int st = max(0, issued - STAGES); st < issued; ++st)
+        pk::mbar_wait(full_bar(st % STAGES), (st / STAGES) & 1);
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int qd = lane & 3;   // quad lane: owns heads 2qd, 2qd+1 of the C fragments
+  const int rw = lane >> 2;  // row within an 8-row group
+  // Q^T as the B operand (k = head_dim, n = head within the group).
+  uint32_t qb[S::KSTEPS][2];
+  {
+    const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                                (size_t(s) * p.num_q_heads + kvh * G + min(rw, G - 1)) * D;
+#pragma unroll
+    for (int ks = 0; ks < S::KSTEPS; ++ks) {
+      const uint32_t a = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * qd);
+      const uint32_t b = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * qd);
+      qb[ks][0] = rw < G ? a : 0u;
+      qb[ks][1] = rw < G ? b : 0u;
+    }
+  }
+  float o[S::KSTEPS][4];
+#pragma unroll
+  for (int mt = 0; mt < S::KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  const float sl = p.scale_log2;
+  const int row0 = warp * 16;
+  const int mi = lane >> 3, r8 = lane & 7;
+
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % STAGES;
+    if (!pk::mbar_wait(full_bar(slot), (st / STAGES) & 1)) {
+      if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, s);
+      break;
+    }
+    const uint32_t kbase = stages + slot * S::STAGE_BYTES;
+    const uint32_t vbase = kbase + S::KV_BYTES;
+    const int nvalid = end - (start + st * S::TPS + row0);  // valid rows of this warp's tile
+    if (nvalid > 0) {
+      if (nvalid < 16) {
+        // Rows past the end hold stale or unloaded data: zero their V so that
+        // a zero softmax weight cannot meet a NaN.
+        const int nz = (16 - nvalid) * S::HALVES * 8;
+        for (int idx = lane; idx < nz; idx += 32) {
+          const int r = row0 + nvalid + idx / (S::HALVES * 8);
+          const int c = idx % (S::HALVES * 8);
+          const uint32_t a = vbase + (c >> 3) * S::SLAB_BYTES + r * 128 + (c & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+        }
+        __syncwarp();
+      }
+      // S^T (16 tokens x 8 heads) = K_tile (16 x D) * Q^T (D x 8)
+      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int ks = 0; ks < S::KSTEPS; ++ks) {
+        const int r = row0 + (mi & 1) * 8 + r8;
+        const int chunk = ks * 2 + (mi >> 1);
+        const uint32_t a = kbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
+                           (((chunk & 7) ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        pk::ldmatrix_x4(a, a0, a1, a2, a3);
+        pk::mma_bf16_16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+      float x0 = sacc[0] * sl, x1 = sacc[1] * sl, x2 = sacc[2] * sl, x3 = sacc[3] * sl;
+      if (rw >= nvalid) x0 = x1 = -INFINITY;
+      if (rw + 8 >= nvalid) x2 = x3 = -INFINITY;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: row 0 is valid
+      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+      const uint32_t w01 = pk::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
+      const uint32_t w23 = pk::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
+      // The denominator sums the same bf16-rounded weights the numerator uses.
+      l0 = fmaf(l0, c0, pk::bf16_lo(w01) + pk::bf16_lo(w23));
+      l1 = fmaf(l1, c1, pk::bf16_hi(w01) + pk::bf16_hi(w23));
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < S::KSTEPS; ++mt) {
+        o[mt][0] *= c0;
+        o[mt][1] *= c1;
+        o[mt][2] *= c0;
+        o[mt][3] *= c1;
+      }
+      // P^T (16 tokens x 8 heads) as the B operand: transpose the C fragments.
+      const uint32_t b0 = pk::movmatrix_trans(w01);
+      const uint32_t b1 = pk::movmatrix_trans(w23);
+      // O^T (D x 8) += V^T (D x 16 tokens) * P^T
+#pragma unroll
+      for (int mt = 0; mt < S::KSTEPS; ++mt) {
+        const int r = row0 + (mi >> 1) * 8 + r8;
+        const int chunk = mt * 2 + (mi & 1);
+        const uint32_t a = vbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
+                           (((chunk & 7) ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        pk::ldmatrix_x4_trans(a, a0, a1, a2, a3);
+        pk::mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) pk::mbar_arrive(empty_bar(slot));
+  }
+
+  // Row sums over the 16 tokens of each tile live spread over the 8 lanes
+  // that share a quad index.
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+
+  // Merge the consumer warps' states in shared memory (the stage ring is free:
+  // every copy has landed and been consumed).
+  pk::named_barrier(1, NW * 32);
+  float *sm_o = reinterpret_cast<float *>(smem_raw + (stages - raw));
+  float *sm_m = sm_o + NW * kMaxGroup * S::OUT_STRIDE;
+  float *sm_l = sm_m + NW * kMaxGroup;
+#pragma unroll
+  for (int mt = 0; mt < S::KSTEPS; ++mt) {
+    float *base = sm_o + (warp * kMaxGroup + 2 * qd) * S::OUT_STRIDE + mt * 16 + rw;
+    base[0] = o[mt][0];
+    base[S::OUT_STRIDE] = o[mt][1];
+    base[8] = o[mt][2];
+    base[S::OUT_STRIDE + 8] = o[mt][3];
+  }
+  if (rw == 0) {
+    sm_m[warp * kMaxGroup + 2 * qd] = m0;
+    sm_m[warp * kMaxGroup + 2 * qd + 1] = m1;
+    sm_l[warp * kMaxGroup + 2 * qd] = l0;
+    sm_l[warp * kMaxGroup + 2 * qd + 1] = l1;
+  }
+  pk::named_barrier(1, NW * 32);
+  for (int idx = threadIdx.x; idx < G * (D / 2); idx += NW * 32) {
+    const int g = idx / (D / 2), i = (idx % (D / 2)) * 2;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + g]);
+    float L = 0.0f, O0 = 0.0f, O1 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(sm_m[w * kMaxGroup + g] - M);
+      const float *row = sm_o + (w * kMaxGroup + g) * S::OUT_STRIDE + i;
+      L = fmaf(sm_l[w * kMaxGroup + g], f, L);
+      O0 = fmaf(row[0], f, O0);
+      O1 = fmaf(row[1], f, O1);
+    }
+    const int h = kvh * G + g;
+    if (p.num_partitions == 1) {
+      const float inv = 1.0f / L;
+      *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                          (size_t(s) * p.num_q_heads + h) * D + i) =
+          __floats2bfloat162_rn(O0 * inv, O1 * inv);
+    } else {
+      const size_t r = (size_t(s) * p.num_q_heads + h) * p.num_partitions + part;
+      *reinterpret_cast<float2 *>(p.ws_acc + r * D + i) = make_float2(O0, O1);
+      if (i == 0) {
+        p.ws_m[r] = M;
+        p.ws_l[r] = L;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of split-K partials: one warp per (sequence, query head).
+//   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p acc_p 2^(m_p - M) / L
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
+  constexpr int EPL = D / 32;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.num_seqs * p.num_q_heads) return;
+  const int s = row / p.num_q_heads;
+  const int ctx = context_len(p, s, false);
+  const int np = (ctx + p.partition - 1) / p.partition;
+  T *out = static_cast<T *>(p.out) + size_t(row) * D + lane * EPL;
+  if (np == 0) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) pk::store_elem(out + e, 0.0f);
+    return;
+  }
+  const float *mrow = p.ws_m + size_t(row) * p.num_partitions;
+  const float *lrow = p.ws_l + size_t(row) * p.num_partitions;
+  float M = -INFINITY;
+  for (int q = lane; q < np; q += 32) M = fmaxf(M, mrow[q]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.0f, acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
+  const float *arow = p.ws_acc + size_t(row) * p.num_partitions * D + lane * EPL;
+  for (int q = 0; q < np; ++q) {
+    const float f = exp2f(mrow[q] - M);
+    L = fmaf(lrow[q], f, L);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(arow[size_t(q) * D + e], f, acc[e]);
+  }
+  const float inv = 1.0f / L;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) pk::store_elem(out + e, acc[e] * inv);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+constexpr int kMmaWarps = 4;
+constexpr int kMmaStages = 3;
+
+int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A [N*B, Hk, D] bf16 view of one pool; each load is a box of B token rows of
+// one head and 64 elements (128 bytes), swizzled 128B in shared memory.
+bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(d.head_dim), cuuint64_t(d.num_kv_heads),
+                              cuuint64_t(d.num_blocks) * cuuint64_t(d.block_size)};
+  const cuuint64_t strides[2] = {cuuint64_t(d.head_dim) * 2,
+                                 cuuint64_t(d.num_kv_heads) * cuuint64_t(d.head_dim) * 2};
+  const cuuint32_t box[3] = {64, 1, cuuint32_t(d.block_size)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int BS>
+pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t stream) {
+  using S = MmaShape<D, BS, kMmaWarps, kMmaStages>;
+  if (p.partition % BS != 0) return PK_ERR_INVALID_ARG;
+  CUtensorMap kmap, vmap;
+  if (!encode_pool_map(&kmap, p.k_cache, d) || !encode_pool_map(&vmap, p.v_cache, d))
+    return PK_ERR_CUDA;
+  auto kern = attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    S::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return PK_ERR_CUDA;
+  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions);
+  kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+template <typename T, int D>
+pk_status launch_simt(const AttnParams &p, cudaStream_t stream) {
+  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions);
+  attn_simt_kernel<T, D><<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+template <typename T, int D>
+pk_status launch_merge(const AttnParams &p, cudaStream_t stream) {
+  const int rows = p.num_seqs * p.num_q_heads;
+  attn_merge_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+bool mma_supported(const pk_cache_desc &d, int group) {
+  return d.dtype == PK_BF16 && (d.head_dim == 64 || d.head_dim == 128) &&
+         (d.block_size == 8 || d.block_size == 16 || d.block_size == 32) && group <= kMaxGroup;
+}
+
+pk_status check_common(const pk_cache_desc *desc, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t max_context_len) {
+  if (!desc || desc->num_blocks <= 0 || desc->block_size <= 0 || desc->num_kv_heads <= 0 ||
+      desc->head_dim <= 0 || num_seqs < 0 || num_q_heads <= 0 || max_context_len <= 0)
+    return PK_ERR_INVALID_ARG;
+  if (elem_size(desc->dtype) == 0) return PK_ERR_UNSUPPORTED;
+  if (num_q_heads % desc->num_kv_heads != 0) return PK_ERR_INVALID_ARG;
+  if (num_q_heads / desc->num_kv_heads > kMaxGroup) return PK_ERR_UNSUPPORTED;
+  if (desc->head_dim != 64 && desc->head_dim != 128) return PK_ERR_UNSUPPORTED;
+  if (int64_t(desc->num_blocks) * desc->block_size > INT32_MAX) return PK_ERR_UNSUPPORTED;
+  return PK_OK;
+}
+
+}  // namespace
+
+extern "C" int pkx_take_attention_error(cudaStream_t stream) {
+  int code = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&code, g_attn_error, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess)
+    return -1;
+  if (cudaMemcpyToSymbolAsync(g_attn_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              stream) != cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+  return code;
+}
+
+extern "C" {
+
+int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t max_context_len, int32_t partition_size,
+                                             const pk_cache_desc *desc) {
+  if (check_common(desc, num_seqs, num_q_heads, max_context_len) != PK_OK) return -1;
+  const int32_t B = desc->block_size;
+  if (partition_size > 0) return partition_size % B == 0 ? partition_size : -1;
+  if (partition_size == 0) return 0;
+  if (partition_size != -1) return -1;
+  // Automatic: split when the (sequence, KV head) units alone cannot fill the
+  // GPU a few times over, or when contexts are long enough for one CTA's
+  // serial walk to dominate. Partitions of 512 tokens (a multiple of every
+  // supported block size and of the 64-token stage).
+  const int64_t units = int64_t(num_seqs) * desc->num_kv_heads;
+  const int32_t kSplit = 512;
+  if (max_context_len <= kSplit) return 0;
+  if (units < 4 * 152 || max_context_len > 2048) return kSplit;
+  return 0;
+}
+
+size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_context_len, int32_t partition_size,
+                                         const pk_cache_desc *desc) {
+  const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads,
+                                                            max_context_len, partition_size, desc);
+  if (part <= 0) return 0;
+  const int64_t P = (int64_t(max_context_len) + part - 1) / part;
+  if (P <= 1) return 0;
+  const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
+  return size_t(rows) * (size_t(desc->head_dim) + 2) * sizeof(float);
+}
+
+pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, float scale,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len,
+                                         int32_t partition_size, void *workspace,
+                                         size_t workspace_bytes, const pk_cache_desc *desc,
+                                         pk_attn_impl impl, void *stream) {
+  pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
+  if (st != PK_OK) return st;
+  if (num_seqs == 0) return PK_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || max_blocks_per_seq <= 0)
+    return PK_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PK_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PK_ERR_INVALID_ARG;
+  const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads, max_context_len,
+                                                            partition_size, desc);
+  if (part < 0) return PK_ERR_INVALID_ARG;
+  int64_t P = part > 0 ? (int64_t(max_context_len) + part - 1) / part : 1;
+  AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.tables = block_tables;
+  p.ctx_lens = context_lens;
+  p.scale_log2 = float(double(scale) * 1.4426950408889634);
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.group = num_q_heads / desc->num_kv_heads;
+  p.block_size = desc->block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = desc->num_blocks;
+  if (P <= 1) {
+    P = 1;
+    // One partition covering any context the table allows.
+    const int64_t cover = int64_t(max_context_len);
+    const int64_t rounded = (cover + desc->block_size - 1) / desc->block_size * desc->block_size;
+    p.partition = int32_t(rounded);
+  } else {
+    p.partition = part;
+  }
+  p.num_partitions = int32_t(P);
+  if (num_seqs > 65535 || P > 65535) return PK_ERR_UNSUPPORTED;
+  if (P > 1) {
+    const size_t need = pk_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len,
+                                                          partition_size, desc);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PK_ERR_WORKSPACE;
+    const size_t rows = size_t(num_seqs) * num_q_heads * size_t(P);
+    p.ws_acc = static_cast<float *>(workspace);
+    p.ws_m = p.ws_acc + rows * desc->head_dim;
+    p.ws_l = p.ws_m + rows;
+  }
+
+  const bool mma_ok = mma_supported(*desc, p.group);
+  if (impl == PK_ATTN_MMA && !mma_ok) return PK_ERR_UNSUPPORTED;
+  if (impl != PK_ATTN_AUTO && impl != PK_ATTN_SIMT && impl != PK_ATTN_MMA)
+    return PK_ERR_INVALID_ARG;
+  const bool use_mma = impl == PK_ATTN_MMA || (impl == PK_ATTN_AUTO && mma_ok);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = desc->head_dim, B = desc->block_size;
+  if (use_mma) {
+    if (D == 128) {
+      st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
+                  : (B == 16 ? launch_mma<128, 16>(p, *desc, s) : launch_mma<128, 32>(p, *desc, s));
+    } else {
+      st = B == 8 ? launch_mma<64, 8>(p, *desc, s)
+                  : (B == 16 ? launch_mma<64, 16>(p, *desc, s) : launch_mma<64, 32>(p, *desc, s));
+    }
+  } else if (desc->dtype == PK_F32) {
+    st = D == 128 ? launch_simt<float, 128>(p, s) : launch_simt<float, 64>(p, s);
+  } else {
+    st = D == 128 ? launch_simt<__nv_bfloat16, 128>(p, s) : launch_simt<__nv_bfloat16, 64>(p, s);
+  }
+  if (st != PK_OK || P == 1) return st;
+  if (desc->dtype == PK_F32)
+    return D == 128 ? launch_merge<float, 128>(p, s) : launch_merge<float, 64>(p, s);
+  return D == 128 ? launch_merge<__nv_bfloat16, 128>(p, s) : launch_merge<__nv_bfloat16, 64>(p, s);
+}
+
+pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,
+                                    const void *v_cache, const int32_t *block_tables,
+                                    const int32_t *context_lens, float scale, int32_t num_seqs,
+                                    int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                    int32_t max_context_len, int32_t partition_size,
+                                    void *workspace, size_t workspace_bytes,
+                                    const pk_cache_desc *desc, void *stream) {
+  return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
+                                        scale, num_seqs, num_q_heads, max_blocks_per_seq,
+                                        max_context_len, partition_size, workspace,
+                                        workspace_bytes, desc, PK_ATTN_AUTO, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,341 @@
+// Host block manager of libpagedkv: free list, block tables, reference
+// counts, fork and block-granular copy-on-write.
+//
+// Semantics ("Paged KV Cache Allocation and the Block Table", the
+// append_token routine and "Sharing blocks between sequences"; "PagedAttention"
+// S06, the BlockManager listing, "Copy-on-write, for free" and "Reference
+// counts must be exact"; "paged attention deep", "Copy-on-write for shared
+// prefixes"):
+//   * Appending token t to a sequence of length L: when L is a multiple of B
+//     the table grows by one block popped from the free list; otherwise, if
+//     the partly filled tail block is named by more than one table, the
+//     sequence swaps it for a fresh private block (the caller copies the
+//     contents with pk_copy_blocks) and the shared block loses one
+//     reference. The slot is table[L / B] * B + L % B.
+//   * Fork: the child names the parent's blocks; each count goes up by one.
+//   * Retire: each block of the table loses one reference; those reaching
+//     zero go back to the free list, in table order.
+//   * The free list is a stack whose first pop is alloc_order[0].
+// Appends are all or nothing; a batch append is undone on failure.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace {
+
+struct Sequence {
+  int64_t len = 0;
+  std::vector<int32_t> table;
+};
+
+// What one token append changed, so a failed batch can be rolled back.
+struct AppendRecord {
+  int64_t seq;
+  int32_t popped;     // block taken from the free list, or -1
+  int32_t replaced;   // shared tail block given up by CoW, or -1
+};
+
+}  // namespace
+
+struct pk_bm {
+  int32_t num_blocks = 0;
+  int32_t block_size = 0;
+  std::vector<int32_t> free_stack;  // back() is handed out next
+  std::vector<int32_t> refs;
+  std::unordered_map<int64_t, Sequence> seqs;
+  int64_t cow_copies = 0;
+
+  int64_t blocks_for(int64_t len) const { return (len + block_size - 1) / block_size; }
+
+  // Blocks a single-token append to `s` would take right now.
+  int32_t need_one(const Sequence &s) const {
+    if (s.len % block_size == 0) return 1;
+    return refs[s.table.back()] > 1 ? 1 : 0;
+  }
+
+  // Appends one token; assumes the free list can cover it.
+  int64_t append_one(int64_t id, Sequence &s, AppendRecord *rec, int64_t *cow_src,
+                     int64_t *cow_dst) {
+    rec->seq = id;
+    rec->popped = -1;
+    rec->replaced = -1;
+    const int64_t off = s.len % block_size;
+    if (off == 0) {
+      const int32_t b = free_stack.back();
+      free_stack.pop_back();
+      refs[b] = 1;
+      s.table.push_back(b);
+      rec->popped = b;
+    } else {
+      const int32_t tail = s.table.back();
+      if (refs[tail] > 1) {
+        const int32_t b = free_stack.back();
+        free_stack.pop_back();
+        refs[b] = 1;
+        refs[tail] -= 1;
+        s.table.back() = b;
+        rec->popped = b;
+        rec->replaced = tail;
+        ++cow_copies;
+        if (cow_src) *cow_src = tail;
+        if (cow_dst) *cow_dst = b;
+      }
+    }
+    const int64_t slot = int64_t(s.table[s.len / block_size]) * block_size + off;
+    s.len += 1;
+    return slot;
+  }
+
+  // Undoes append_one in reverse order of application.
+  void undo(const AppendRecord &rec) {
+    Sequence &s = seqs[rec.seq];
+    s.len -= 1;
+    if (rec.popped < 0) return;
+    if (rec.replaced >= 0) {
+      s.table.back() = rec.replaced;
+      refs[rec.replaced] += 1;
+      --cow_copies;
+    } else {
+      s.table.pop_back();
+    }
+    refs[rec.popped] = 0;
+    free_stack.push_back(rec.popped);
+  }
+};
+
+extern "C" {
+
+pk_status pk_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *alloc_order,
+                       pk_bm **out) {
+  if (!out || num_blocks <= 0 || block_size <= 0) return PK_ERR_INVALID_ARG;
+  *out = nullptr;
+  pk_bm *bm = new (std::nothrow) pk_bm;
+  if (!bm) return PK_ERR_NOMEM;
+  try {
+    bm->num_blocks = num_blocks;
+    bm->block_size = block_size;
+    bm->refs.assign(num_blocks, 0);
+    bm->free_stack.resize(num_blocks);
+    std::vector<char> seen(num_blocks, 0);
+    for (int32_t i = 0; i < num_blocks; ++i) {
+      const int32_t b = alloc_order ? alloc_order[i] : i;
+      if (b < 0 || b >= num_blocks || seen[b]) {
+        delete bm;
+        return PK_ERR_INVALID_ARG;
+      }
+      seen[b] = 1;
+      bm->free_stack[num_blocks - 1 - i] = b;  // alloc_order[0] ends on top
+    }
+  } catch (const std::bad_alloc &) {
+    delete bm;
+    return PK_ERR_NOMEM;
+  }
+  *out = bm;
+  return PK_OK;
+}
+
+void pk_bm_destroy(pk_bm *bm) { delete bm; }
+
+pk_status pk_bm_add_seq(pk_bm *bm, int64_t seq_id) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  try {
+    auto r = bm->seqs.emplace(seq_id, Sequence{});
+    return r.second ? PK_OK : PK_ERR_SEQ_EXISTS;
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+}
+
+pk_status pk_bm_append_slots(pk_bm *bm, int64_t seq_id, int32_t n, int64_t *slots_out,
+                             int64_t *cow_pairs_out, int32_t *n_cow_out) {
+  if (!bm || n < 0 || (n > 0 && !slots_out)) return PK_ERR_INVALID_ARG;
+  if (n_cow_out) *n_cow_out = 0;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  Sequence &s = it->second;
+  if (n == 0) return PK_OK;
+  // Blocks needed: one per block boundary crossed, plus a CoW copy when the
+  // first token lands in a shared, partly filled tail.
+  const int64_t fresh = bm->blocks_for(s.len + n) - bm->blocks_for(s.len);
+  const int64_t cow = (s.len % bm->block_size != 0 && bm->refs[s.table.back()] > 1) ? 1 : 0;
+  if (fresh + cow > int64_t(bm->free_stack.size())) return PK_ERR_OUT_OF_BLOCKS;
+  try {
+    s.table.reserve(size_t(bm->blocks_for(s.len + n)));
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  int64_t src = -1, dst = -1;
+  AppendRecord rec;
+  for (int32_t i = 0; i < n; ++i) slots_out[i] = bm->append_one(seq_id, s, &rec, &src, &dst);
+  if (src >= 0) {
+    if (cow_pairs_out) {
+      cow_pairs_out[0] = src;
+      cow_pairs_out[1] = dst;
+    }
+    if (n_cow_out) *n_cow_out = 1;
+  }
+  return PK_OK;
+}
+
+pk_status pk_bm_append_batch(pk_bm *bm, const int64_t *seq_ids, int32_t n, int64_t *slots_out,
+                             int64_t *cow_pairs_out, int32_t *n_cow_out) {
+  if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out))) return PK_ERR_INVALID_ARG;
+  if (n_cow_out) *n_cow_out = 0;
+  std::vector<AppendRecord> log;
+  std::vector<Sequence *> seqp;
+  try {
+    log.reserve(n);
+    seqp.reserve(n);
+    for (int32_t i = 0; i < n; ++i) {
+      auto it = bm->seqs.find(seq_ids[i]);
+      if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+      it->second.table.reserve(size_t(bm->blocks_for(it->second.len + 1)));
+      seqp.push_back(&it->second);
+    }
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  int32_t ncow = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    Sequence &s = *seqp[i];
+    if (bm->need_one(s) > int32_t(bm->free_stack.size())) {
+      for (auto r = log.rbegin(); r != log.rend(); ++r) bm->undo(*r);
+      if (n_cow_out) *n_cow_out = 0;
+      return PK_ERR_OUT_OF_BLOCKS;
+    }
+    int64_t src = -1, dst = -1;
+    AppendRecord rec;
+    slots_out[i] = bm->append_one(seq_ids[i], s, &rec, &src, &dst);
+    log.push_back(rec);
+    if (src >= 0) {
+      if (cow_pairs_out) {
+        cow_pairs_out[2 * ncow] = src;
+        cow_pairs_out[2 * ncow + 1] = dst;
+      }
+      ++ncow;
+    }
+  }
+  if (n_cow_out) *n_cow_out = ncow;
+  return PK_OK;
+}
+
+pk_status pk_bm_fork(pk_bm *bm, int64_t parent, int64_t child) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  if (bm->seqs.count(child)) return PK_ERR_SEQ_EXISTS;
+  auto it = bm->seqs.find(parent);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  try {
+    Sequence copy = it->second;
+    for (int32_t b : copy.table) bm->refs[b] += 1;
+    bm->seqs.emplace(child, std::move(copy));
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  return PK_OK;
+}
+
+pk_status pk_bm_free_seq(pk_bm *bm, int64_t seq_id) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  for (int32_t b : it->second.table) {
+    if (--bm->refs[b] == 0) bm->free_stack.push_back(b);
+  }
+  bm->seqs.erase(it);
+  return PK_OK;
+}
+
+pk_status pk_bm_seq_len(const pk_bm *bm, int64_t seq_id, int64_t *len_out) {
+  if (!bm || !len_out) return PK_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  *len_out = it->second.len;
+  return PK_OK;
+}
+
+pk_status pk_bm_block_table(const pk_bm *bm, int64_t seq_id, int32_t *out, int32_t cap,
+                            int32_t *len_out) {
+  if (!bm || cap < 0 || (cap > 0 && !out)) return PK_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  const auto &t = it->second.table;
+  const int32_t m = std::min<int32_t>(cap, int32_t(t.size()));
+  if (m > 0) std::memcpy(out, t.data(), sizeof(int32_t) * size_t(m));
+  if (len_out) *len_out = int32_t(t.size());
+  return PK_OK;
+}
+
+pk_status pk_bm_export_tables(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
+                              int32_t max_blocks, int32_t *tables_out, int32_t *lens_out) {
+  if (!bm || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !tables_out)))
+    return PK_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+    const auto &s = it->second;
+    if (int64_t(s.table.size()) > max_blocks || s.len > INT32_MAX) return PK_ERR_INVALID_ARG;
+    int32_t *row = tables_out + size_t(i) * size_t(max_blocks);
+    std::copy(s.table.begin(), s.table.end(), row);
+    std::fill(row + s.table.size(), row + max_blocks, -1);
+    if (lens_out) lens_out[i] = int32_t(s.len);
+  }
+  return PK_OK;
+}
+
+int32_t pk_bm_num_free(const pk_bm *bm) { return bm ? int32_t(bm->free_stack.size()) : -1; }
+
+int32_t pk_bm_refcount(const pk_bm *bm, int32_t block) {
+  if (!bm || block < 0 || block >= bm->num_blocks) return -1;
+  return bm->refs[block];
+}
+
+pk_status pk_bm_check_invariants(const pk_bm *bm) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  std::vector<int32_t> count(bm->num_blocks, 0);
+  for (const auto &kv : bm->seqs) {
+    const Sequence &s = kv.second;
+    if (int64_t(s.table.size()) != bm->blocks_for(s.len)) return PK_ERR_INVARIANT;
+    for (int32_t b : s.table) {
+      if (b < 0 || b >= bm->num_blocks) return PK_ERR_INVARIANT;
+      ++count[b];
+    }
+  }
+  std::vector<char> is_free(bm->num_blocks, 0);
+  for (int32_t b : bm->free_stack) {
+    if (b < 0 || b >= bm->num_blocks || is_free[b] || count[b] != 0) return PK_ERR_INVARIANT;
+    is_free[b] = 1;
+  }
+  int64_t named = 0;
+  for (int32_t b = 0; b < bm->num_blocks; ++b) {
+    if (count[b] != bm->refs[b]) return PK_ERR_INVARIANT;
+    named += count[b] > 0;
+  }
+  if (named + int64_t(bm->free_stack.size()) != bm->num_blocks) return PK_ERR_INVARIANT;
+  return PK_OK;
+}
+
+pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_slots,
+                      int64_t *tail_waste, int32_t *shared_blocks, int64_t *cow_copies) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  int64_t live = 0, waste = 0;
+  for (const auto &kv : bm->seqs) {
+    live += kv.second.len;
+    waste += bm->blocks_for(kv.second.len) * bm->block_size - kv.second.len;
+  }
+  int32_t shared = 0;
+  for (int32_t r : bm->refs) shared += r > 1;
+  if (live_tokens) *live_tokens = live;
+  if (reserved_slots)
+    *reserved_slots = int64_t(bm->num_blocks - int32_t(bm->free_stack.size())) * bm->block_size;
+  if (tail_waste) *tail_waste = waste;
+  if (shared_blocks) *shared_blocks = shared;
+  if (cow_copies) *cow_copies = bm->cow_copies;
+  return PK_OK;
+}
+
+}  // extern "C"

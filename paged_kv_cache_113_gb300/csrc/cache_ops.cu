@@ -1,0 +1,178 @@
+// Cache writes of libpagedkv: the slot scatter (pk_reshape_and_cache) and the
+// copy-on-write block copy (pk_copy_blocks), plus the library's status
+// strings and device-error readout.
+//
+// Both kernels are pure data movement. The pool layout [N, B, Hk, d] makes one
+// token's K (all heads) a contiguous Hk*d*esz-byte row, and one block a
+// contiguous B*Hk*d*esz-byte span, so both kernels are 16-byte vector copies.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+#include "pk_device.cuh"
+
+namespace {
+
+__device__ int g_cache_ops_error;
+
+// One CTA per new token: token i's K row and V row go to slot slot_mapping[i]
+// ("Paged KV Cache Allocation and the Block Table", append_token: the token
+// is written at physical * block_size + slot).
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+    const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
+    int32_t row_vecs) {
+  const int64_t i = blockIdx.x;
+  const int64_t s = slots[i];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (threadIdx.x == 0) pk::record_error(&g_cache_ops_error, PK_DEVERR_SLOT, i);
+    return;
+  }
+  const uint4 *ksrc = k + i * row_vecs;
+  const uint4 *vsrc = v + i * row_vecs;
+  uint4 *kdst = k_cache + s * row_vecs;
+  uint4 *vdst = v_cache + s * row_vecs;
+  for (int32_t j = threadIdx.x; j < row_vecs; j += blockDim.x) {
+    const uint4 a = __ldg(ksrc + j);
+    const uint4 b = __ldg(vsrc + j);
+    kdst[j] = a;
+    vdst[j] = b;
+  }
+}
+
+// grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block.
+// The whole block src is copied to dst ("paged attention deep",
+// "Copy-on-write for shared prefixes").
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_cache,
+                                                          uint4 *__restrict__ v_cache,
+                                                          const int64_t *__restrict__ pairs,
+                                                          int32_t num_blocks, int64_t block_vecs,
+                                                          int64_t chunk_vecs) {
+  const int64_t src = pairs[2 * blockIdx.x];
+  const int64_t dst = pairs[2 * blockIdx.x + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+      pk::record_error(&g_cache_ops_error, PK_DEVERR_PAIR, blockIdx.x);
+    return;
+  }
+  uint4 *pool = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4 *from = pool + src * block_vecs;
+  uint4 *to = pool + dst * block_vecs;
+  const int64_t beg = int64_t(blockIdx.z) * chunk_vecs;
+  const int64_t end = min(block_vecs, beg + chunk_vecs);
+  int64_t j = beg + threadIdx.x;
+  // Four independent 16-byte loads in flight per thread.
+  for (; j + 3 * int64_t(blockDim.x) < end; j += 4 * int64_t(blockDim.x)) {
+    const uint4 a = from[j];
+    const uint4 b = from[j + blockDim.x];
+    const uint4 c = from[j + 2 * blockDim.x];
+    const uint4 d = from[j + 3 * blockDim.x];
+    to[j] = a;
+    to[j + blockDim.x] = b;
+    to[j + 2 * blockDim.x] = c;
+    to[j + 3 * blockDim.x] = d;
+  }
+  for (; j < end; j += blockDim.x) to[j] = from[j];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
+
+pk_status check_desc(const pk_cache_desc *d) {
+  if (!d || d->num_blocks <= 0 || d->block_size <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0)
+    return PK_ERR_INVALID_ARG;
+  if (elem_size(d->dtype) == 0) return PK_ERR_UNSUPPORTED;
+  if ((int64_t(d->num_kv_heads) * d->head_dim * elem_size(d->dtype)) % 16 != 0)
+    return PK_ERR_UNSUPPORTED;
+  return PK_OK;
+}
+
+}  // namespace
+
+// Read-and-clear of this file's device error word (used by pk_get_device_error).
+extern "C" int pkx_take_cache_ops_error(cudaStream_t stream) {
+  int code = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&code, g_cache_ops_error, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return -1;
+  if (cudaMemcpyToSymbolAsync(g_cache_ops_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice,
+                              stream) != cudaSuccess)
+    return -1;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+  return code;
+}
+
+extern "C" int pkx_take_attention_error(cudaStream_t stream);
+
+extern "C" {
+
+pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot_mapping,
+                               int32_t num_tokens, void *k_cache, void *v_cache,
+                               const pk_cache_desc *desc, void *stream) {
+  pk_status st = check_desc(desc);
+  if (st != PK_OK) return st;
+  if (num_tokens < 0) return PK_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PK_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PK_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PK_ERR_INVALID_ARG;
+  const int64_t row_bytes = int64_t(desc->num_kv_heads) * desc->head_dim * elem_size(desc->dtype);
+  const int64_t num_slots = int64_t(desc->num_blocks) * desc->block_size;
+  reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
+      int32_t(row_bytes / 16));
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+pk_status pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
+                         int32_t num_pairs, const pk_cache_desc *desc, void *stream) {
+  pk_status st = check_desc(desc);
+  if (st != PK_OK) return st;
+  if (num_pairs < 0) return PK_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PK_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PK_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PK_ERR_INVALID_ARG;
+  const int64_t block_bytes = int64_t(desc->block_size) * desc->num_kv_heads * desc->head_dim *
+                              elem_size(desc->dtype);
+  const int64_t block_vecs = block_bytes / 16;
+  const int64_t chunk_vecs = 256 * 8;  // 32 KiB per CTA
+  const int64_t chunks = (block_vecs + chunk_vecs - 1) / chunk_vecs;
+  if (chunks > 65535) return PK_ERR_UNSUPPORTED;
+  dim3 grid(num_pairs, 2, unsigned(chunks));
+  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs,
+      desc->num_blocks, block_vecs, chunk_vecs);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+pk_status pk_get_device_error(int32_t *code_out, void *stream) {
+  if (!code_out) return PK_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int a = pkx_take_cache_ops_error(s);
+  const int b = pkx_take_attention_error(s);
+  if (a < 0 || b < 0) return PK_ERR_CUDA;
+  *code_out = a != 0 ? a : b;
+  return PK_OK;
+}
+
+const char *pk_status_string(pk_status status) {
+  switch (status) {
+    case PK_OK: return "ok";
+    case PK_ERR_INVALID_ARG: return "invalid argument";
+    case PK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PK_ERR_OUT_OF_BLOCKS: return "out of blocks";
+    case PK_ERR_UNKNOWN_SEQ: return "unknown sequence";
+    case PK_ERR_SEQ_EXISTS: return "sequence exists";
+    case PK_ERR_CUDA: return "CUDA error";
+    case PK_ERR_WORKSPACE: return "workspace missing or too small";
+    case PK_ERR_INVARIANT: return "block manager invariant violated";
+    case PK_ERR_NOMEM: return "out of host memory";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

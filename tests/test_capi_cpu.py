@@ -1,0 +1,239 @@
+"""libpagedkv on the CPU: it builds, loads, exports every declared symbol, and
+its host block manager agrees bit for bit with the oracle's.
+
+No GPU entry point runs here except the host-side argument checks that
+return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_113_gb300 as pk
+from workloads import WORKLOAD_NAMES, make_workload, prefill_plan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    pk.build()
+    return pk.lib()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared_symbols() == sorted(pk.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+    assert pk.pk_status_string(0) == "ok"
+    assert pk.pk_status_string(3) == "out of blocks"
+
+
+def _replay_both(wl):
+    """Runs the workload's prefill plan and one step on both block managers."""
+    ours = pk.BlockManager(wl.num_blocks, wl.block_size, wl.alloc_order())
+    ref = oracle.BlockManager(wl.num_blocks, wl.block_size, wl.alloc_order())
+    for op in prefill_plan(wl):
+        if op[0] == "add":
+            ours.add_seq(op[1])
+            ref.add_seq(op[1])
+        elif op[0] == "fork":
+            ours.fork(op[1], op[2])
+            ref.fork(op[1], op[2])
+        else:
+            s1, c1 = ours.append(op[1], op[2])
+            s2, c2 = ref.append(op[1], op[2])
+            assert np.array_equal(s1, s2) and c1 == c2
+    slots, pairs = ours.append_batch(range(wl.num_seqs))
+    ref_slots, ref_pairs = [], []
+    for s in range(wl.num_seqs):
+        sl, cow = ref.append(s, 1)
+        ref_slots.append(sl[0])
+        if cow is not None:
+            ref_pairs.append(cow)
+    assert slots.tolist() == ref_slots
+    assert [tuple(p) for p in pairs.tolist()] == ref_pairs
+    return ours, ref
+
+
+@pytest.mark.parametrize("name,B", [(n, None) for n in WORKLOAD_NAMES if n != "prefix"] +
+                         [("prefix", 8), ("prefix", 16), ("prefix", 32)])
+def test_block_manager_matches_oracle_on_workloads(L, name, B):
+    wl = make_workload(name, block_size=B)
+    ours, ref = _replay_both(wl)
+    ctx = wl.ctx_lens
+    maxb = -(-int(ctx.max()) // wl.block_size)
+    tables, lens = ours.export_tables(range(wl.num_seqs), maxb)
+    assert np.array_equal(tables, ref.export_tables(range(wl.num_seqs), maxb))
+    assert np.array_equal(lens, ctx.astype(np.int32))
+    assert ours.num_free() == ref.num_free()
+    for b in range(0, wl.num_blocks, max(1, wl.num_blocks // 500)):
+        assert ours.refcount(b) == ref.refcount(b)
+    ours.check_invariants()
+    st = ours.stats()
+    assert st["live_tokens"] == int(ctx.sum())
+    assert st["cow_copies"] == ref.cow_copies()
+    assert st["tail_waste"] == int(sum(-(-int(c) // wl.block_size) * wl.block_size - int(c) for c in ctx))
+
+
+def test_block_manager_random_ops_match_oracle(L):
+    rng = np.random.default_rng(99)
+    for trial in range(20):
+        B = int(rng.choice([1, 4, 8, 16]))
+        N = int(rng.integers(8, 80))
+        order = rng.permutation(N).astype(np.int32)
+        ours, ref = pk.BlockManager(N, B, order), oracle.BlockManager(N, B, order)
+        live, nid = [], 0
+        for _ in range(150):
+            r = rng.random()
+            if r < 0.2 or not live:
+                ours.add_seq(nid)
+                ref.add_seq(nid)
+                live.append(nid)
+                nid += 1
+            elif r < 0.55:
+                s, n = int(rng.choice(live)), int(rng.integers(0, 2 * B + 3))
+                try:
+                    a = ours.append(s, n)
+                except pk.PagedKVError as e:
+                    assert e.status == 3
+                    with pytest.raises(oracle.OracleError):
+                        ref.append(s, n)
+                else:
+                    b = ref.append(s, n)
+                    assert np.array_equal(a[0], b[0]) and a[1] == b[1]
+            elif r < 0.7:
+                seqs = [int(x) for x in rng.choice(live, size=int(rng.integers(1, len(live) + 1)))]
+                free0 = ours.num_free()
+                try:
+                    slots, pairs = ours.append_batch(seqs)
+                except pk.PagedKVError as e:
+                    assert e.status == 3 and ours.num_free() == free0  # batch undone
+                    continue
+                for i, s in enumerate(seqs):
+                    sl, cow = ref.append(s, 1)
+                    assert slots[i] == sl[0]
+                assert len(pairs) == sum(1 for _ in pairs)
+            elif r < 0.85:
+                p = int(rng.choice(live))
+                ours.fork(p, nid)
+                ref.fork(p, nid)
+                live.append(nid)
+                nid += 1
+            else:
+                s = int(rng.choice(live))
+                ours.free_seq(s)
+                ref.free_seq(s)
+                live.remove(s)
+            ours.check_invariants()
+            assert ours.num_free() == ref.num_free()
+            for s in live:
+                assert np.array_equal(ours.table(s), ref.table(s))
+                assert ours.seq_len(s) == ref.seq_len(s)
+
+
+def test_batch_append_is_all_or_nothing(L):
+    bm = pk.BlockManager(3, 2, None)
+    for s in range(3):
+        bm.add_seq(s)
+        bm.append(s, 2)            # every sequence holds one full block
+    free0, t0 = bm.num_free(), [bm.table(s).tolist() for s in range(3)]
+    with pytest.raises(pk.PagedKVError) as ei:
+        bm.append_batch([0, 1, 2])  # would need 3 fresh blocks, 0 free
+    assert ei.value.status == 3
+    assert bm.num_free() == free0 and [bm.table(s).tolist() for s in range(3)] == t0
+    assert [bm.seq_len(s) for s in range(3)] == [2, 2, 2]
+    bm.check_invariants()
+
+
+def test_batch_undo_restores_cow_state(L):
+    bm = pk.BlockManager(4, 4, None)
+    bm.add_seq(0)
+    bm.append(0, 6)                # blocks 0, 1 (tail half full)
+    bm.fork(0, 1)
+    bm.add_seq(2)
+    # seq 0 copies its shared tail (takes block 2), seq 2 takes block 3, seq 1
+    # then writes its tail in place... and a second token for seq 2 needs none.
+    # Ask for one more fresh block than exists: seq 0 CoW, seq 2 new, seq 1
+    # in place, then seq 3 unknown -> error, all undone.
+    before = (bm.num_free(), bm.table(0).tolist(), bm.table(1).tolist(), bm.refcount(1))
+    with pytest.raises(pk.PagedKVError) as ei:
+        bm.append_batch([0, 2, 1, 77])
+    assert ei.value.status == 4
+    assert (bm.num_free(), bm.table(0).tolist(), bm.table(1).tolist(), bm.refcount(1)) == before
+    slots, pairs = bm.append_batch([0, 2, 1])
+    assert pairs.tolist() == [[1, 2]] and bm.refcount(1) == 1
+    bm.check_invariants()
+
+
+def test_error_statuses(L):
+    with pytest.raises(pk.PagedKVError) as ei:
+        pk.BlockManager(4, 4, np.array([0, 1, 1, 2], np.int32))
+    assert ei.value.status == 1
+    bm = pk.BlockManager(4, 4, None)
+    with pytest.raises(pk.PagedKVError) as ei:
+        bm.append(5, 1)
+    assert ei.value.status == 4
+    bm.add_seq(5)
+    with pytest.raises(pk.PagedKVError) as ei:
+        bm.add_seq(5)
+    assert ei.value.status == 5
+    with pytest.raises(pk.PagedKVError):
+        bm.fork(9, 10)
+    with pytest.raises(pk.PagedKVError) as ei:
+        bm.export_tables([5], 0) if bm.append(5, 1) else None
+    assert ei.value.status == 1
+
+
+def _desc(N=64, B=16, Hk=8, d=128, dt=pk.PK_BF16):
+    return pk.CacheDesc(N, B, Hk, d, dt)
+
+
+def test_partition_resolution_and_workspace_size(L):
+    d = _desc()
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 512, d) == 512
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 0, d) == 0
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 40, d) == -1      # not a multiple of B
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 512     # few units: split
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 300, -1, d) == 0         # short: no split
+    assert pk.pk_paged_attention_resolve_partition(8, 60, 300, -1, d) == -1        # Hq % Hk != 0
+    assert pk.pk_paged_attention_resolve_partition(8, 128, 300, -1, d) == -1       # group of 16
+    ws = pk.pk_paged_attention_workspace_size(8, 64, 32768, 512, d)
+    assert ws == 8 * 64 * 64 * (128 + 2) * 4
+    assert pk.pk_paged_attention_workspace_size(8, 64, 512, 512, d) == 0           # one partition
+    assert pk.pk_paged_attention_workspace_size(8, 64, 32768, 0, d) == 0
+
+
+def test_host_checks_reject_before_launch(L):
+    null = ctypes.c_void_p(0)
+    bad = _desc(dt=7)
+    assert L.pk_reshape_and_cache(null, null, null, 1, null, null, ctypes.byref(bad), null) == 2
+    assert L.pk_reshape_and_cache(null, null, null, 0, null, null, ctypes.byref(_desc()), null) == 0
+    assert L.pk_reshape_and_cache(null, null, null, 1, null, null, ctypes.byref(_desc()), null) == 1
+    assert L.pk_copy_blocks(null, null, null, 0, ctypes.byref(_desc()), null) == 0
+    assert L.pk_copy_blocks(null, null, null, -1, ctypes.byref(_desc()), null) == 1
+    d = _desc()
+    args = [null] * 6 + [ctypes.c_float(0.1), 4, 8, 4, 64, -1, null, 0, ctypes.byref(d), null]
+    assert L.pk_paged_attention_decode(*args) == 1          # null pointers
+    a2 = list(args)
+    a2[8] = 12                                              # 12 query heads over 8 KV heads
+    assert L.pk_paged_attention_decode(*a2) == 1
+    a3 = list(args)
+    a3[7] = 0                                               # empty batch is a no-op
+    assert L.pk_paged_attention_decode(*a3) == 0
+    odd = _desc(d=96)
+    a4 = list(args)
+    a4[14] = ctypes.byref(odd)
+    assert L.pk_paged_attention_decode(*a4) == 2            # head_dim 96 not compiled

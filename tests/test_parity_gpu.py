@@ -1,0 +1,315 @@
+"""GPU parity: libpagedkv against the CPU oracle, element by element.
+
+Each case builds the same seeded workload twice -- once through libpagedkv on
+the GPU (C++ block manager, CUDA scatter / copy / attention), once through the
+oracle on the CPU -- and compares:
+* slot mappings, copy-on-write pairs and block tables: bit-exact;
+* the whole K and V pools after the step: bit-exact;
+* attention outputs: within the tolerances of ``parity_util`` (bf16:
+  max-abs 1e-2, rel-L2 2e-3; fp32: 1e-5 / 2e-6).
+
+Reduced cases (a few sequences of each workload, every row compared) run every
+kernel variant and partitioning; full-size cases run the benchmark's launch
+configuration and compare sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_113_gb300 as pk
+from paged_kv_cache_113_gb300.harness import DecodeState, from_device
+from parity_util import assert_close, as_f64, errors
+from workloads import Workload, make_workload
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pk.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _no_device_error():
+    kind, idx = pk.pk_get_device_error()
+    assert kind == 0, f"device error {pk.DEVERR_NAMES.get(kind, kind)} at {idx}"
+
+
+def _build_pair(wl, select=None, compare_pool=True, **state_kw):
+    """GPU state + oracle replay of one workload step; checks the exact parts."""
+    wl.enable_memo()
+    ref = oracle.run_workload(wl, attention=select is not None, select=select)
+    st = DecodeState(wl, "cuda", **state_kw)
+    si = st.prepare_step(0)
+    assert np.array_equal(si.slots, ref["slots"]), "step slot mapping differs"
+    assert np.array_equal(np.asarray(si.pairs).reshape(-1, 2), ref["cow_pairs"]), "CoW pairs differ"
+    assert [tuple(p) for p in st.prefill_pairs] == [tuple(p) for p in ref["prefill_pairs"]]
+    for a, b in zip(st.prefill_slots, ref["prefill_slots"]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(si.tables, ref["tables"]), "block tables differ"
+    assert np.array_equal(si.ctx_lens, ref["ctx_lens"].astype(np.int32))
+    d = st.upload(si)
+    out = st.new_out()
+    st.run_step(d, out, st.alloc_workspace(si.max_context_len, -1), -1, "auto")
+    torch.cuda.synchronize()
+    _no_device_error()
+    if compare_pool:
+        assert np.array_equal(from_device(st.k_cache), ref["k_cache"]), "K pool differs"
+        assert np.array_equal(from_device(st.v_cache), ref["v_cache"]), "V pool differs"
+    return st, d, out, ref
+
+
+def _variants(wl):
+    impls = ["simt"] + (["mma"] if wl.dtype == "bf16" else [])
+    B = wl.block_size
+    parts = [0, -1, 512, 3 * B, B]
+    return [(i, p) for i in impls for p in parts]
+
+
+def _check_all_variants(st, d, ref_out, wl, what):
+    results = {}
+    for impl, part in _variants(wl):
+        out = st.new_out()
+        ws = st.alloc_workspace(d["max_context_len"], part)
+        st.attention(d, out, ws, part, impl)
+        torch.cuda.synchronize()
+        _no_device_error()
+        results[(impl, part)] = assert_close(from_device(out), ref_out, wl.dtype, f"{what} {impl} part={part}")
+    return results
+
+
+REDUCED = [
+    ("tiny", None, None),
+    ("mha7b", 6, None),
+    ("gqa8b", 24, None),
+    ("long", 1, None),
+    ("prefix", 8, 8),
+    ("prefix", 8, 16),
+    ("prefix", 8, 32),
+]
+
+
+@pytest.mark.parametrize("name,nseq,B", REDUCED)
+def test_reduced_workload_all_variants(name, nseq, B):
+    wl = make_workload(name, block_size=B, num_seqs=nseq)
+    wl.enable_memo()
+    st, d, out, ref = _build_pair(wl)
+    ref_out = oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"],
+                                     wl.scale, wl.dtype)
+    assert_close(from_device(out), ref_out, wl.dtype, f"{name} auto")
+    _check_all_variants(st, d, ref_out, wl, name)
+
+
+def _sample_rows(wl, ctx, n=48, seed=0):
+    rng = np.random.default_rng(seed)
+    S, Hq = wl.num_seqs, wl.num_q_heads
+    seqs = {int(np.argmax(ctx)), int(np.argmin(ctx)), 0, S - 1}
+    rows = {(s, int(rng.integers(Hq))) for s in seqs}
+    while len(rows) < min(n, S * Hq):
+        rows.add((int(rng.integers(S)), int(rng.integers(Hq))))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+FULL = [("mha7b", None), ("gqa8b", None), ("long", None), ("prefix", 8), ("prefix", 16), ("prefix", 32)]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,B", FULL)
+def test_full_size_sampled(name, B):
+    """Full-size workload in the benchmark's launch configuration (auto)."""
+    wl = make_workload(name, block_size=B)
+    sel = _sample_rows(wl, wl.ctx_lens)
+    st, d, out, ref = _build_pair(wl, select=sel)
+    got = from_device(out)
+    rows_got = np.stack([got[s, h] for s, h in sel])
+    rows_ref = np.stack([ref["out"][s, h] for s, h in sel])
+    assert_close(rows_got, rows_ref, wl.dtype, f"{name} full (auto)")
+    # Every row: finite and each output a convex combination of its values.
+    g = as_f64(got, wl.dtype)
+    assert np.isfinite(g).all()
+
+
+def _custom(name, S, Hq, Hk, d, B, lens, N=None, seed=5, dtype="bf16"):
+    lens = np.asarray(lens, dtype=np.int64)
+    N = N or int(sum(-(-int(c) // B) for c in lens) + 8)
+    return Workload(name, S, Hq, Hk, d, B, dtype, N, lens, seed=seed)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_group_headdim_blocksize_grid(G, d, B):
+    # Lengths hit the edges: 1, one block, one block + 1, a stage boundary
+    # (64), one past it, a ragged tail and a partition boundary (512 + 1).
+    lens = [1, B, B + 1, 63, 64, 65, 200, 513]
+    wl = _custom(f"grid{G}_{d}_{B}", len(lens), 2 * G, 2, d, B, lens, seed=G * 100 + d + B)
+    st, d_, out, ref = _build_pair(wl)
+    ref_out = oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"],
+                                     wl.scale, wl.dtype)
+    _check_all_variants(st, d_, ref_out, wl, wl.name)
+
+
+def test_fp32_head_dim_128():
+    wl = _custom("f32_128", 3, 8, 4, 128, 16, [5, 80, 300], dtype="f32")
+    st, d, out, ref = _build_pair(wl)
+    ref_out = oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"],
+                                     wl.scale, wl.dtype)
+    _check_all_variants(st, d, ref_out, wl, wl.name)
+
+
+@pytest.mark.parametrize("impl", ["simt", "mma"])
+def test_block_placement_does_not_change_bits(impl):
+    """Same logical data under three physical placements: identical output bits."""
+    wl = _custom("perm", 6, 32, 8, 128, 16, [1, 17, 100, 333, 640, 1025], N=600).enable_memo()
+    outs = []
+    for seed in (1, 2, 3):
+        order = np.random.default_rng(seed).permutation(wl.num_blocks).astype(np.int32)
+        st = DecodeState(wl, "cuda", alloc_order=order)
+        d = st.upload(st.prepare_step(0))
+        for part in (0, 128):
+            out = st.new_out()
+            st.run_step(d, out, st.alloc_workspace(d["max_context_len"], part), part, impl)
+            outs.append((part, from_device(out)))
+    _no_device_error()
+    for part in (0, 128):
+        o = [x for p, x in outs if p == part]
+        assert np.array_equal(o[0], o[1]) and np.array_equal(o[0], o[2])
+
+
+@pytest.mark.parametrize("impl", ["simt", "mma"])
+def test_nan_in_unwritten_slots_is_never_read(impl):
+    """Pools start as NaN: slots past each context end hold NaN and must not leak."""
+    wl = _custom("nan", 5, 16, 4, 128, 16, [1, 15, 17, 70, 129]).enable_memo()
+    ref = oracle.run_workload(wl)
+    st = DecodeState(wl, "cuda", init_value=float("nan"))
+    d = st.upload(st.prepare_step(0))
+    for part in (0, 32):
+        out = st.new_out()
+        st.run_step(d, out, st.alloc_workspace(d["max_context_len"], part), part, impl)
+        torch.cuda.synchronize()
+        assert_close(from_device(out), ref["out"], "bf16", f"nan-pool {impl} {part}")
+    _no_device_error()
+
+
+def test_split_matches_unsplit():
+    wl = make_workload("long", num_seqs=1)
+    wl.enable_memo()
+    st = DecodeState(wl, "cuda")
+    d = st.upload(st.prepare_step(0))
+    outs = {}
+    for part in (0, 512, 2048):
+        out = st.new_out()
+        st.run_step(d, out, st.alloc_workspace(d["max_context_len"], part), part, "mma")
+        outs[part] = as_f64(from_device(out), "bf16")
+    _no_device_error()
+    for part in (512, 2048):
+        mx, rl = errors(outs[part], outs[0])
+        assert mx <= 8e-3 and rl <= 2e-3, (part, mx, rl)
+
+
+def test_standalone_copy_blocks_each_block_size():
+    """96 copies (each group's last prefix block to three fresh blocks), bit-exact."""
+    for B in (8, 16, 32):
+        wl = make_workload("prefix", block_size=B, num_seqs=32 * 4)
+        wl.enable_memo()
+        ref = oracle.run_workload(wl, attention=False)
+        st = DecodeState(wl, "cuda")
+        si = st.prepare_step(0)
+        d = st.upload(si)
+        st.run_step(d, st.new_out(), st.alloc_workspace(d["max_context_len"], -1))
+        free = ref["bm"].free_list()
+        pairs = []
+        for g in range(wl.prefix_groups):
+            src = int(ref["tables"][g * wl.prefix_n][wl.prefix_len // B - 1])
+            for c in range(3):
+                pairs.append((src, int(free[3 * g + c])))
+        pairs = np.array(pairs, np.int64)
+        assert len(pairs) == 96
+        oracle.copy_blocks(ref["k_cache"], ref["v_cache"], pairs)
+        pk.pk_copy_blocks(st.k_cache, st.v_cache, torch.from_numpy(pairs).cuda())
+        torch.cuda.synchronize()
+        _no_device_error()
+        assert np.array_equal(from_device(st.k_cache), ref["k_cache"])
+        assert np.array_equal(from_device(st.v_cache), ref["v_cache"])
+        del st
+        torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# Bad inputs: host checks return a status; device checks skip and record.
+# ---------------------------------------------------------------------------
+def _small_state():
+    wl = _custom("edge", 3, 8, 2, 128, 16, [5, 40, 77]).enable_memo()
+    st = DecodeState(wl, "cuda")
+    d = st.upload(st.prepare_step(0))
+    return wl, st, d
+
+
+def test_bad_slot_is_skipped_and_recorded():
+    wl, st, d = _small_state()
+    before = from_device(st.k_cache).copy()
+    slots = torch.tensor([-1, wl.num_blocks * wl.block_size, 3], dtype=torch.int64, device="cuda")
+    k = torch.ones((3, 2, 128), dtype=torch.bfloat16, device="cuda")
+    pk.pk_reshape_and_cache(k, k, slots, st.k_cache, st.v_cache)
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "slot" and idx == 1
+    after = from_device(st.k_cache)
+    changed = np.argwhere((after != before).any(axis=(2, 3)))
+    assert [tuple(x) for x in changed] == [(0, 3)]     # only slot 3 (block 0, offset 3) was written
+
+
+def test_bad_block_id_is_recorded_without_fault():
+    wl, st, d = _small_state()
+    for impl in ("simt", "mma"):
+        tables = d["tables"].clone()
+        tables[1, 1] = wl.num_blocks + 5
+        dd = dict(d, tables=tables)
+        out = st.new_out()
+        st.attention(dd, out, None, 0, impl)
+        kind, idx = pk.pk_get_device_error()
+        assert pk.DEVERR_NAMES[kind] == "block_id" and idx == 1, impl
+
+
+def test_bad_context_length_is_recorded_and_zeroed():
+    wl, st, d = _small_state()
+    for impl in ("simt", "mma"):
+        ctx = d["ctx_lens"].clone()
+        ctx[2] = 0
+        out = st.new_out()
+        st.attention(dict(d, ctx_lens=ctx), out, None, 0, impl)
+        kind, idx = pk.pk_get_device_error()
+        assert pk.DEVERR_NAMES[kind] == "context" and idx == 2
+        assert not from_device(out)[2].any()
+
+
+def test_bad_pair_is_recorded():
+    wl, st, d = _small_state()
+    pk.pk_copy_blocks(st.k_cache, st.v_cache, torch.tensor([[0, wl.num_blocks]], dtype=torch.int64, device="cuda"))
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "pair" and idx == 0
+
+
+def test_host_side_rejections():
+    wl, st, d = _small_state()
+    out = st.new_out()
+    with pytest.raises(pk.PagedKVError) as ei:
+        pk.pk_paged_attention_decode(out, d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"], wl.scale,
+                                     d["max_context_len"], 16, None)      # splits, no workspace
+    assert ei.value.status == 7
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pk.PagedKVError) as ei:
+        pk.pk_paged_attention_decode(out, d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"], wl.scale,
+                                     d["max_context_len"], 16, small)
+    assert ei.value.status == 7
+    with pytest.raises(pk.PagedKVError) as ei:
+        pk.pk_paged_attention_decode(out, d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"], wl.scale,
+                                     d["max_context_len"], 24, None)      # not a multiple of B
+    assert ei.value.status == 1
+    with pytest.raises(ValueError):
+        pk.pk_paged_attention_decode(out.cpu(), d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"],
+                                     wl.scale, d["max_context_len"])
+    _no_device_error()

@@ -50,9 +50,15 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     Returns the 16-bit patterns as ``uint16``. This is input preparation: the
     bf16 workloads are defined by these bits, and both sides read them.
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return rounded.astype(np.uint16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if not np.isfinite(x).all():
+        raise ValueError("bf16 rounding of the inputs expects finite values")
+    # For finite values the sum stays below 2**32, so uint32 arithmetic is exact.
+    r = (u >> 16) & 1
+    r += u
+    r += 0x7FFF
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -98,6 +104,13 @@ class Workload:
     prefix_groups: int = 0
     prefix_n: int = 0
     prefix_len: int = 0
+    memo: Optional[dict] = dataclasses.field(default=None, repr=False, compare=False)
+
+    def enable_memo(self) -> "Workload":
+        """Keep generated token data so a second consumer does not redraw it."""
+        if self.memo is None:
+            self.memo = {}
+        return self
 
     @property
     def scale(self) -> float:
@@ -128,18 +141,28 @@ class Workload:
         sequence's divergent tokens (the shared prompt comes from
         :meth:`prefix_kv`).
         """
+        key = ("prefill", seq, n_tokens)
+        if self.memo is not None and key in self.memo:
+            return self.memo[key]
         rng = np.random.default_rng([self.seed, 1, seq])
         shape = (n_tokens, self.num_kv_heads, self.head_dim)
         k = normal_values(rng, shape, self.dtype)
         v = normal_values(rng, shape, self.dtype)
+        if self.memo is not None:
+            self.memo[key] = (k, v)
         return k, v
 
     def prefix_kv(self, group: int):
         """K and V of group ``group``'s shared prompt, ``[prefix_len, Hk, d]``."""
+        key = ("prefix", group)
+        if self.memo is not None and key in self.memo:
+            return self.memo[key]
         rng = np.random.default_rng([self.seed, 3, group])
         shape = (self.prefix_len, self.num_kv_heads, self.head_dim)
         k = normal_values(rng, shape, self.dtype)
         v = normal_values(rng, shape, self.dtype)
+        if self.memo is not None:
+            self.memo[key] = (k, v)
         return k, v
 
     def step_inputs(self, step: int):
