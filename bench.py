@@ -74,6 +74,27 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def reduce_max(values):
+    """Element-wise maximum over ranks (identity without a process group).
+
+    The slowest rank's time sets the whole job's throughput. Works on the
+    gloo (CPU tensors) and nccl (CUDA tensors) backends."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_throughput(world: int, bytes_per_rank: float, seconds_max: float) -> float:
+    """Whole-job GB/s: every rank processes the same replica, so the job moves
+    world * bytes_per_rank in the slowest rank's time."""
+    return world * bytes_per_rank / seconds_max / 1e9
+
+
 def measured_hbm_peak():
     for path in (os.path.join(ROOT, "MEASURED_PEAKS.json"),):
         try:
@@ -343,22 +364,15 @@ def run_ours(args):
     if kind:
         raise RuntimeError(f"device error in the timed steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
 
-    if world > 1:
-        t = torch.tensor([t_step, t_attn], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_attn = float(t[0]), float(t[1])
-
-    value = world * total_bytes / t_step / 1e9
+    t_step, t_attn = reduce_max([t_step, t_attn])
+    value = job_throughput(world, total_bytes, t_step)
     attn_gbs = total_bytes / t_attn / 1e9
     peak, peak_kind = measured_hbm_peak()
 
     e2e = None
     if E:
         e2e = run_e2e(st, wl, E, Ew, args, dev)
-        if world > 1:
-            t = torch.tensor([e2e["_seconds"]], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e["value"] = world * e2e["_bytes"] / float(t[0]) / 1e9
+        e2e["value"] = job_throughput(world, e2e["_bytes"], reduce_max([e2e["_seconds"]])[0])
         e2e.pop("_seconds")
         e2e.pop("_bytes")
 

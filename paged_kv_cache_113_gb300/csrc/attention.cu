@@ -19,7 +19,8 @@
 //                     128-byte swizzled. Consumer warps each take 16 tokens
 //                     per stage: S^T = K Q^T and O^T += V^T P^T on the tensor
 //                     cores (mma.sync m16n8k16, tokens as M, the group's heads
-//                     as N), with an online softmax in registers.
+//                     as N), with an online softmax in registers; the softmax
+//                     weights enter PV as a bf16 hi + lo pair.
 //   attn_simt_kernel  fp32 or bf16 on CUDA cores: one warp per token,
 //                     shuffle-reduced dot products, online softmax.
 //   attn_merge_kernel log-sum-exp merge of the split-K partials.
@@ -357,11 +358,16 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       }
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: row 0 is valid
       const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      const uint32_t w01 = pk::pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
-      const uint32_t w23 = pk::pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
-      // The denominator sums the same bf16-rounded weights the numerator uses.
-      l0 = fmaf(l0, c0, pk::bf16_lo(w01) + pk::bf16_lo(w23));
-      l1 = fmaf(l1, c1, pk::bf16_hi(w01) + pk::bf16_hi(w23));
+      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+      // Softmax weights enter the PV product as a bf16 pair hi + lo: rounding
+      // them to one bf16 would put ~2^-9 relative error on every output.
+      const uint32_t w01 = pk::pack_bf16x2(p0, p1);
+      const uint32_t w23 = pk::pack_bf16x2(p2, p3);
+      const uint32_t r01 = pk::pack_bf16x2(p0 - pk::bf16_lo(w01), p1 - pk::bf16_hi(w01));
+      const uint32_t r23 = pk::pack_bf16x2(p2 - pk::bf16_lo(w23), p3 - pk::bf16_hi(w23));
+      l0 = fmaf(l0, c0, p0 + p2);
+      l1 = fmaf(l1, c1, p1 + p3);
       m0 = mn0;
       m1 = mn1;
 #pragma unroll
@@ -374,6 +380,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       // P^T (16 tokens x 8 heads) as the B operand: transpose the C fragments.
       const uint32_t b0 = pk::movmatrix_trans(w01);
       const uint32_t b1 = pk::movmatrix_trans(w23);
+      const uint32_t e0 = pk::movmatrix_trans(r01);
+      const uint32_t e1 = pk::movmatrix_trans(r23);
       // O^T (D x 8) += V^T (D x 16 tokens) * P^T
 #pragma unroll
       for (int mt = 0; mt < S::KSTEPS; ++mt) {
@@ -384,6 +392,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         uint32_t a0, a1, a2, a3;
         pk::ldmatrix_x4_trans(a, a0, a1, a2, a3);
         pk::mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+        pk::mma_bf16_16816(o[mt], a0, a1, a2, a3, e0, e1);
       }
     }
     __syncwarp();
