@@ -151,6 +151,34 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
                                          size_t workspace_bytes, const pk_cache_desc *desc,
                                          pk_attn_impl impl, void *stream);
 
+/* Allocation-free decode attention. The pages have no counterpart: this is a
+ * library convenience for callers that cannot allocate device memory -- a
+ * serving engine whose memory planner already gave nearly all HBM to the KV
+ * pool, a host framework's operator hook that supplies only input and output
+ * buffers, or a latency-critical loop that cannot pay for cudaMalloc/cudaFree
+ * and their implicit synchronisation.
+ * Same arguments and result as pk_paged_attention_decode, minus the
+ * workspace: the split-K scratch is a static device array of
+ * PK_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * the process exits. The call allocates nothing.
+ *   - Returns PK_ERR_WORKSPACE, before any launch, when the partitioning
+ *     needs more scratch than PK_STATIC_WORKSPACE_BYTES
+ *     (see pk_paged_attention_workspace_size).
+ *   - The first call on a device looks up the array's device address for
+ *     that device (with the device current); make that first call before
+ *     any stream capture.
+ *   - All calls on a device share the one array, and it keeps the last
+ *     call's contents (nothing in it needs to start at zero). Calls whose
+ *     work overlaps on the GPU (e.g. on two streams) race on it. */
+#define PK_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
+pk_status pk_paged_attention_decode_static(void *out, const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *block_tables,
+                                           const int32_t *context_lens, float scale,
+                                           int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t max_blocks_per_seq, int32_t max_context_len,
+                                           int32_t partition_size, const pk_cache_desc *desc,
+                                           void *stream);
+
 /* The partition size (in tokens) that a partition_size argument resolves to
  * for this shape: 0 means no split. Host only, no GPU needed. */
 int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_heads,

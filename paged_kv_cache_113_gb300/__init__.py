@@ -38,12 +38,14 @@ PK_ERR_UNKNOWN_SEQ, PK_ERR_SEQ_EXISTS, PK_ERR_CUDA, PK_ERR_WORKSPACE = 4, 5, 6, 
 PK_ERR_INVARIANT, PK_ERR_NOMEM = 8, 9
 PK_F32, PK_BF16 = 0, 1
 IMPLS = {"auto": 0, "simt": 1, "mma": 2}
+PK_STATIC_WORKSPACE_BYTES = 64 << 20  # the static split-K scratch of pk_paged_attention_decode_static
 DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5: "timeout"}
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = (
     "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
-    "pk_paged_attention_decode_impl", "pk_paged_attention_resolve_partition",
+    "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static",
+    "pk_paged_attention_resolve_partition",
     "pk_paged_attention_workspace_size", "pk_get_device_error", "pk_status_string",
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
@@ -83,6 +85,7 @@ def lib() -> ctypes.CDLL:
         "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D, P]),
         "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
                                                  i32, P]),
+        "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),
         "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
         "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
         "pk_get_device_error": (i32, [P, P]),
@@ -232,6 +235,26 @@ def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_le
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
         float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
         ws_ptr, ws_bytes, ctypes.byref(desc), IMPLS[impl], _stream(stream)), "pk_paged_attention_decode")
+
+
+def pk_paged_attention_decode_static(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                     max_context_len: int, partition_size: int = -1, stream=None):
+    """As :func:`pk_paged_attention_decode`, for callers that cannot allocate
+    device memory: the split-K scratch is the library's static device array
+    (``PK_STATIC_WORKSPACE_BYTES``), shared by every call on a device, so
+    calls whose work overlaps on the GPU race on it."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    S, Hq, d = (int(x) for x in q.shape)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out and q must be [num_seqs, num_q_heads, head_dim] of the cache dtype")
+    if d != desc.head_dim or block_tables.dim() != 2 or int(block_tables.shape[0]) != S:
+        raise ValueError("shape mismatch")
+    _check(lib().pk_paged_attention_decode_static(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+        float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+        ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_static")
 
 
 def pk_get_device_error(stream=None) -> Tuple[int, int]:

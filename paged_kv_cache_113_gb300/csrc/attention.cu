@@ -735,3 +735,68 @@ pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cach
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the decode attention
+// ---------------------------------------------------------------------------
+// Some callers cannot allocate device memory at all: a serving engine whose
+// memory planner has already handed nearly all HBM to the KV pool and forbids
+// ad-hoc allocations, a host framework's custom-operator hook that passes in
+// only input and output buffers, or a latency-critical loop that cannot
+// afford cudaMalloc/cudaFree and their implicit device-wide synchronisation.
+// For them the split-K scratch lives in the file-scope array below. Every GPU
+// that loads this library holds it (PK_STATIC_WORKSPACE_BYTES) until the
+// process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_workspace[PK_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+
+// Device address of g_static_workspace on `device` (which must be current).
+// In host code the array's name is only a host-side stand-in, so the address
+// comes from cudaGetSymbolAddress, looked up once per device and kept.
+cudaError_t static_workspace_address(int device, void **out) {
+  static std::mutex mu;
+  static void *addr[kMaxStaticDevices] = {};
+  if (device < 0 || device >= kMaxStaticDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[device]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess) return e;
+    addr[device] = p;
+  }
+  *out = addr[device];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" pk_status pk_paged_attention_decode_static(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, float scale, int32_t num_seqs,
+    int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_context_len,
+    int32_t partition_size, const pk_cache_desc *desc, void *stream) {
+  pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
+  if (st != PK_OK) return st;
+  const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads,
+                                                            max_context_len, partition_size, desc);
+  if (part < 0) return PK_ERR_INVALID_ARG;
+  const size_t need = pk_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len,
+                                                        partition_size, desc);
+  if (need > PK_STATIC_WORKSPACE_BYTES) return PK_ERR_WORKSPACE;
+  void *ws = nullptr;
+  if (need > 0) {
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PK_ERR_CUDA;
+    if (static_workspace_address(device, &ws) != cudaSuccess) return PK_ERR_CUDA;
+  }
+  // Nothing in the scratch needs clearing: every partial the merge reads is
+  // written earlier in the same call.
+  return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
+                                        scale, num_seqs, num_q_heads, max_blocks_per_seq,
+                                        max_context_len, partition_size, ws,
+                                        need > 0 ? size_t(PK_STATIC_WORKSPACE_BYTES) : 0, desc,
+                                        PK_ATTN_AUTO, stream);
+}
