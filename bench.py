@@ -50,7 +50,7 @@ SRC_FOR_TRAFFIC = ["paged_kv_cache_113_gb300/csrc/attention.cu", "paged_kv_cache
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="mha7b", choices=["tiny", "mha7b", "gqa8b", "long", "prefix"])
@@ -62,6 +62,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-graphs", action="store_true", help="launch the timed steps eagerly, not as CUDA graphs")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -133,9 +134,9 @@ def ncu_traffic(workload: str):
 # Clocks sampler (nvidia-smi during the timed region)
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int, uuid: str = None):
         self.dev = uuid or str(device_index)
@@ -153,7 +154,9 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
 
-    def stop(self):
+    def stop(self, t_begin: float, t_end: float):
+        """Summary of the samples taken between wall-clock times t_begin and t_end."""
+        import datetime
         if self.proc is None:
             return {"samples": 0, "note": "nvidia-smi unavailable"}
         time.sleep(0.1)
@@ -166,19 +169,23 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 8:
+                if len(parts) < 9:
                     continue
                 try:
-                    rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
                 except ValueError:
                     continue
         os.unlink(self.path)
-        if not rows:
-            return {"samples": 0}
+        inside = [r for r in rows if t_begin <= r[0] <= t_end]
+        used = inside or [r for r in rows if r[0] >= t_begin][:1]
+        if not used:
+            return {"samples": 0, "samples_in_region": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, flags in rows for i, fl in enumerate(flags) if fl.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({names[i] for _, _, _, flags in used for i, fl in enumerate(flags)
+                          if fl.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples_in_region": len(inside), "samples": len(rows)}
 
 
 # ---------------------------------------------------------------------------
@@ -199,6 +206,21 @@ def time_oracle_rows(wl, ref, rows: np.ndarray):
     ctx = ref["ctx_lens"]
     nbytes = int(sum(int(ctx[s]) for s, _ in rows)) * wl.head_dim * wl.esz * 2
     return dt, nbytes
+
+
+def unique_kv_bytes(wl, si) -> int:
+    """K/V bytes of the distinct physical slots a step reads (shared prefix
+    blocks count once); equals the algorithmic bytes without sharing."""
+    B = wl.block_size
+    ctx = si.ctx_lens.astype(np.int64)
+    slots = []
+    for s in range(len(ctx)):
+        n = int(ctx[s])
+        nb = -(-n // B)
+        blocks = si.tables[s, :nb].astype(np.int64)
+        sl = (blocks[:, None] * B + np.arange(B)[None, :]).reshape(-1)[:n]
+        slots.append(sl)
+    return int(np.unique(np.concatenate(slots)).size) * wl.num_kv_heads * wl.head_dim * wl.esz * 2
 
 
 def all_rows(wl):
@@ -301,18 +323,38 @@ def run_ours(args):
     host_steps = [st.prepare_step() for _ in range(R)]
     dsteps = [st.upload(si) for si in host_steps]
     step_bytes = [wl.kv_bytes(si.ctx_lens) for si in host_steps]
+    step_unique = [unique_kv_bytes(wl, si) for si in host_steps]
     max_ctx = max(si.max_context_len for si in host_steps) + E + Ew + 1
     ws = st.alloc_workspace(max_ctx, args.partition)
     out = st.new_out()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+
+    class _Flush:
+        """Evicts L2 between steps: writes 2x L2, then reads 2x L2 so that the
+        next step starts on a cold and clean L2 (no dirty lines to write back)."""
+
+        @staticmethod
+        def zero_():
+            flush_buf.zero_()
+            flush_buf.sum()
+
+    flush = _Flush()
 
     def launches(si):
         part = st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
         return (1 if len(si.pairs) else 0) + 2 + (1 if split else 0)
 
-    # warm-up
+    def cache_writes(d):
+        if d["pairs"].shape[0]:
+            pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
+        pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
+
+    def attend(d):
+        st.attention(d, out, ws, args.partition, args.attn_impl)
+
+    # warm-up (eager; also performs the library's one-time set-up)
     for i in range(args.warmup):
         flush.zero_()
         st.run_step(dsteps[i % R], out, ws, args.partition, args.attn_impl)
@@ -320,6 +362,20 @@ def run_ours(args):
     kind, _ = pk.pk_get_device_error()
     if kind:
         raise RuntimeError(f"device error during warm-up: {pk.DEVERR_NAMES.get(kind)}")
+
+    # Each window step as two CUDA graphs (cache writes; attention + merge), so
+    # the timed region holds GPU work only, as a decode loop would run it.
+    graphs = None
+    if not args.no_graphs:
+        graphs = []
+        for d in dsteps:
+            g_w, g_a = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_w):
+                cache_writes(d)
+            with torch.cuda.graph(g_a):
+                attend(d)
+            graphs.append((g_w, g_a))
+        torch.cuda.synchronize()
 
     sampler = None
     if not args.no_clocks:
@@ -333,29 +389,36 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     n_launch = 0
     total_bytes = 0
+    total_unique = 0
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    clock0 = time.time()
     for i in range(args.steps):
         flush.zero_()
         j = (args.warmup + i) % R
         d = dsteps[j]
         e0, e1, e2 = ev[i]
         e0.record()
-        if d["pairs"].shape[0]:
-            pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
-        pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
+        if graphs:
+            graphs[j][0].replay()
+        else:
+            cache_writes(d)
         e1.record()
-        st.attention(d, out, ws, args.partition, args.attn_impl)
+        if graphs:
+            graphs[j][1].replay()
+        else:
+            attend(d)
         e2.record()
         n_launch += launches(host_steps[j])
         total_bytes += step_bytes[j]
+        total_unique += step_unique[j]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - wall0
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop(clock0, time.time()) if sampler else None
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     attn_ms = [b.elapsed_time(c) for _, b, c in ev]
     t_step = sum(step_ms) / 1e3
@@ -392,14 +455,17 @@ def run_ours(args):
             "data": "synthetic",
             "config": workload_config(wl, args, {
                 "partition": part, "attn_impl": args.attn_impl, "window_steps": R,
-                "l2": "flushed between steps (write of 2x L2, outside the step events)",
-                "kv_bytes_per_step_mean": total_bytes / args.steps}),
+                "l2": "flushed between steps: 2x L2 written then 2x L2 read (cold, clean L2), outside the step events",
+                "kv_bytes_per_step_mean": total_bytes / args.steps,
+                "kv_unique_bytes_per_step_mean": total_unique / args.steps,
+                "launch": "CUDA graphs per step" if graphs else "eager"}),
             "roofline": {"bound": "hbm", "kernel": "paged attention (attn_*_kernel + merge when split)",
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": ncu_traffic(wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"),
                          "bytes_per_launch": total_bytes / args.steps, "ms_per_launch": 1e3 * t_attn / args.steps},
             "attention_gbs": attn_gbs,
+            "attention_unique_gbs": total_unique / t_attn / 1e9,
             "gpu_launches": n_launch,
             "wall_s_timed_region": wall,
             "clocks": clocks,

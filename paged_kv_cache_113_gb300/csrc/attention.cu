@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
   const int start = part * p.partition;
   if (start >= ctx) return;
   const int end = min(ctx, start + p.partition);
+  // A sequence that fits one partition is final here; the merge skips it.
+  const bool single = ctx <= p.partition;
 
   float qv[kMaxGroup][EPL];
   float m[kMaxGroup], l[kMaxGroup], acc[kMaxGroup][EPL];
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
       O = fmaf(sm_o[w][g][i], f, O);
     }
     const int h = kvh * G + g;
-    if (p.num_partitions == 1) {
+    if (single) {
       pk::store_elem(static_cast<T *>(p.out) + (size_t(s) * p.num_q_heads + h) * D + i, O / L);
     } else {
       const size_t r = (size_t(s) * p.num_q_heads + h) * p.num_partitions + part;
@@ -253,10 +255,25 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       pk::prefetch_tensormap(&kmap);
       pk::prefetch_tensormap(&vmap);
     }
-    const int32_t *trow = p.tables + size_t(s) * p.max_blocks;
+    // The partition's table entries are read ahead in coalesced 32-entry
+    // chunks (one entry per lane, one chunk in reserve), so no stage waits on
+    // a dependent global load before its copies can be issued.
+    const int32_t *trow = p.tables + size_t(s) * p.max_blocks + start / BS;
+    const int nb = (end - start + BS - 1) / BS;  // blocks of this partition
+    int cur = lane < nb ? __ldg(trow + lane) : 0;
+    int nxt = 32 + lane < nb ? __ldg(trow + 32 + lane) : 0;
+    int chunk = 0;
     int issued = 0;
     for (int st = 0; st < nst; ++st) {
       const int slot = st % STAGES;
+      const int b0 = st * S::BPS;  // first block of the stage, within the partition
+      if (b0 >= 32 * (chunk + 1)) {
+        ++chunk;
+        cur = nxt;
+        const int j = 32 * (chunk + 1) + lane;
+        nxt = j < nb ? __ldg(trow + j) : 0;
+      }
+      const int mine = __shfl_sync(0xffffffffu, cur, (b0 & 31) + min(lane, S::BPS - 1));
       if (st >= STAGES && !pk::mbar_wait(empty_bar(slot), ((st / STAGES) - 1) & 1)) {
         if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, s);
         break;
@@ -267,7 +284,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         pk::mbar_arrive_expect_tx(full_bar(slot), uint32_t(nblk * S::HALVES * 2 * BS * 128));
       __syncwarp();
       if (lane < nblk) {
-        int phys = __ldg(trow + tok0 / BS + lane);
+        int phys = mine;
         if (phys < 0 || phys >= p.num_blocks) {
           pk::record_error(&g_attn_error, PK_DEVERR_BLOCK_ID, s);
           phys = 0;  // stay in bounds and keep the byte count; the result is flagged
@@ -335,8 +352,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         }
         __syncwarp();
       }
-      // S^T (16 tokens x 8 heads) = K_tile (16 x D) * Q^T (D x 8)
-      float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // S^T (16 tokens x 8 heads) = K_tile (16 x D) * Q^T (D x 8), as two
+      // independent accumulation chains (even and odd k-steps).
+      float sacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
       for (int ks = 0; ks < S::KSTEPS; ++ks) {
         const int r = row0 + (mi & 1) * 8 + r8;
@@ -345,9 +363,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                            (((chunk & 7) ^ (r & 7)) << 4);
         uint32_t a0, a1, a2, a3;
         pk::ldmatrix_x4(a, a0, a1, a2, a3);
-        pk::mma_bf16_16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        pk::mma_bf16_16816(sacc[ks & 1], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
       }
-      float x0 = sacc[0] * sl, x1 = sacc[1] * sl, x2 = sacc[2] * sl, x3 = sacc[3] * sl;
+      float x0 = (sacc[0][0] + sacc[1][0]) * sl, x1 = (sacc[0][1] + sacc[1][1]) * sl;
+      float x2 = (sacc[0][2] + sacc[1][2]) * sl, x3 = (sacc[0][3] + sacc[1][3]) * sl;
       if (rw >= nvalid) x0 = x1 = -INFINITY;
       if (rw + 8 >= nvalid) x2 = x3 = -INFINITY;
       float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -382,18 +401,23 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       const uint32_t b1 = pk::movmatrix_trans(w23);
       const uint32_t e0 = pk::movmatrix_trans(r01);
       const uint32_t e1 = pk::movmatrix_trans(r23);
-      // O^T (D x 8) += V^T (D x 16 tokens) * P^T
+      // O^T (D x 8) += V^T (D x 16 tokens) * P^T: all hi products first, then
+      // all lo products, so consecutive MMAs never share an accumulator.
+      uint32_t va[S::KSTEPS][4];
 #pragma unroll
       for (int mt = 0; mt < S::KSTEPS; ++mt) {
         const int r = row0 + (mi >> 1) * 8 + r8;
         const int chunk = mt * 2 + (mi & 1);
         const uint32_t a = vbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
                            (((chunk & 7) ^ (r & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        pk::ldmatrix_x4_trans(a, a0, a1, a2, a3);
-        pk::mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
-        pk::mma_bf16_16816(o[mt], a0, a1, a2, a3, e0, e1);
+        pk::ldmatrix_x4_trans(a, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
       }
+#pragma unroll
+      for (int mt = 0; mt < S::KSTEPS; ++mt)
+        pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], b0, b1);
+#pragma unroll
+      for (int mt = 0; mt < S::KSTEPS; ++mt)
+        pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], e0, e1);
     }
     __syncwarp();
     if (lane == 0) pk::mbar_arrive(empty_bar(slot));
@@ -443,7 +467,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       O1 = fmaf(row[1], f, O1);
     }
     const int h = kvh * G + g;
-    if (p.num_partitions == 1) {
+    if (ctx <= p.partition) {  // a single partition: final output, no merge
       const float inv = 1.0f / L;
       *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                           (size_t(s) * p.num_q_heads + h) * D + i) =
@@ -478,6 +502,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
     for (int e = 0; e < EPL; ++e) pk::store_elem(out + e, 0.0f);
     return;
   }
+  if (np == 1) return;  // written directly by the attention kernel
   const float *mrow = p.ws_m + size_t(row) * p.num_partitions;
   const float *lrow = p.ws_l + size_t(row) * p.num_partitions;
   float M = -INFINITY;
@@ -502,8 +527,16 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-constexpr int kMmaWarps = 4;
-constexpr int kMmaStages = 3;
+// Consumer warps and pipeline stages of the tensor-core kernel (each stage
+// holds 16 tokens per consumer warp). Overridable at build time for tuning.
+#ifndef PK_MMA_WARPS
+#define PK_MMA_WARPS 4
+#endif
+#ifndef PK_MMA_STAGES
+#define PK_MMA_STAGES 3
+#endif
+constexpr int kMmaWarps = PK_MMA_WARPS;
+constexpr int kMmaStages = PK_MMA_STAGES;
 
 int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
 
@@ -616,15 +649,18 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
   if (partition_size > 0) return partition_size % B == 0 ? partition_size : -1;
   if (partition_size == 0) return 0;
   if (partition_size != -1) return -1;
-  // Automatic: split when the (sequence, KV head) units alone cannot fill the
-  // GPU a few times over, or when contexts are long enough for one CTA's
-  // serial walk to dominate. Partitions of 512 tokens (a multiple of every
-  // supported block size and of the 64-token stage).
+  // Automatic: every partition costs a CTA prologue/epilogue and merge
+  // traffic, so split only when the (sequence, KV head) units cannot fill the
+  // GPU several times over (measured on GB300: 64 sequences x 32 heads and
+  // 256 x 8 run fastest unsplit; 8 x 8 heads of 32K tokens fastest with
+  // 2048-token partitions). Aim for ~1024 work items, partitions a power of two
+  // of at least 512 tokens (multiples of every block size and stage).
   const int64_t units = int64_t(num_seqs) * desc->num_kv_heads;
-  const int32_t kSplit = 512;
-  if (max_context_len <= kSplit) return 0;
-  if (units < 4 * 152 || max_context_len > 2048) return kSplit;
-  return 0;
+  if (units >= 512 || max_context_len <= 512) return 0;
+  int64_t part = 512;
+  while (part * 2 < max_context_len && units * ((max_context_len + 2 * part - 1) / (2 * part)) >= 1024)
+    part *= 2;
+  return int32_t(part);
 }
 
 size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,

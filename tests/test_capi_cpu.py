@@ -206,7 +206,9 @@ def test_partition_resolution_and_workspace_size(L):
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 512, d) == 512
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 0, d) == 0
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 40, d) == -1      # not a multiple of B
-    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 512     # few units: split
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 2048    # few units: split
+    assert pk.pk_paged_attention_resolve_partition(2, 16, 32768, -1, d) == 512     # fewer units: finer
+    assert pk.pk_paged_attention_resolve_partition(64, 64, 2048, -1, d) == 0       # many units: whole
     assert pk.pk_paged_attention_resolve_partition(8, 64, 300, -1, d) == 0         # short: no split
     assert pk.pk_paged_attention_resolve_partition(8, 60, 300, -1, d) == -1        # Hq % Hk != 0
     assert pk.pk_paged_attention_resolve_partition(8, 128, 300, -1, d) == -1       # group of 16
