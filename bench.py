@@ -63,6 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="launch the timed steps eagerly, not as CUDA graphs")
+    p.add_argument("--no-order", action="store_true", help="launch sequences in index order, not longest first")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -352,12 +353,13 @@ def run_ours(args):
         pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
 
     def attend(d):
-        st.attention(d, out, ws, args.partition, args.attn_impl)
+        st.attention(d, out, ws, args.partition, args.attn_impl, ordered=not args.no_order)
 
     # warm-up (eager; also performs the library's one-time set-up)
     for i in range(args.warmup):
         flush.zero_()
-        st.run_step(dsteps[i % R], out, ws, args.partition, args.attn_impl)
+        cache_writes(dsteps[i % R])
+        attend(dsteps[i % R])
     torch.cuda.synchronize()
     kind, _ = pk.pk_get_device_error()
     if kind:
@@ -458,7 +460,8 @@ def run_ours(args):
                 "l2": "flushed between steps: 2x L2 written then 2x L2 read (cold, clean L2), outside the step events",
                 "kv_bytes_per_step_mean": total_bytes / args.steps,
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
-                "launch": "CUDA graphs per step" if graphs else "eager"}),
+                "launch": "CUDA graphs per step" if graphs else "eager",
+                "seq_order": "index" if args.no_order else "longest first (host)"}),
             "roofline": {"bound": "hbm", "kernel": "paged attention (attn_*_kernel + merge when split)",
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
@@ -498,6 +501,7 @@ def run_e2e(st, wl, E, Ew, args, dev):
     h_lens = torch.empty(S, dtype=torch.int32).pin_memory()
     h_slots = torch.empty(S, dtype=torch.int64).pin_memory()
     h_pairs = torch.empty((S, 2), dtype=torch.int64).pin_memory()
+    h_order = torch.empty(S, dtype=torch.int32).pin_memory()
     h_out = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt).pin_memory()
     d_q = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt, device=dev)
     d_k = torch.empty((S, wl.num_kv_heads, wl.head_dim), dtype=tdt, device=dev)
@@ -506,6 +510,7 @@ def run_e2e(st, wl, E, Ew, args, dev):
     d_lens = torch.empty(S, dtype=torch.int32, device=dev)
     d_slots = torch.empty(S, dtype=torch.int64, device=dev)
     d_pairs = torch.empty((S, 2), dtype=torch.int64, device=dev)
+    d_order = torch.empty(S, dtype=torch.int32, device=dev)
     d_out = torch.empty_like(h_out, device=dev)
     tables_np, lens_np = h_tables.numpy(), h_lens.numpy()
     seq_ids = np.arange(S, dtype=np.int64)
@@ -521,6 +526,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
         st.bm.export_tables(seq_ids, st.max_blocks, tables_out=tables_np, lens_out=lens_np)
         npair = len(pairs)
         h_slots.numpy()[:] = slots
+        if not args.no_order:
+            h_order.numpy()[:] = pk.pk_longest_first_order(lens_np)
         if npair:
             h_pairs.numpy()[:npair] = pairs
         d_q.copy_(hq[i], non_blocking=True)
@@ -529,13 +536,16 @@ def run_e2e(st, wl, E, Ew, args, dev):
         d_slots.copy_(h_slots, non_blocking=True)
         d_tables.copy_(h_tables, non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
+        if not args.no_order:
+            d_order.copy_(h_order, non_blocking=True)
         if npair:
             d_pairs[:npair].copy_(h_pairs[:npair], non_blocking=True)
             pk.pk_copy_blocks(st.k_cache, st.v_cache, d_pairs[:npair])
         pk.pk_reshape_and_cache(d_k, d_v, d_slots, st.k_cache, st.v_cache)
         mc = int(lens_np.max())
         pk.pk_paged_attention_decode(d_out, d_q, st.k_cache, st.v_cache, d_tables, d_lens, wl.scale, mc,
-                                     args.partition, ws, args.attn_impl)
+                                     args.partition, ws, args.attn_impl,
+                                     seq_order=None if args.no_order else d_order)
         h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
         dt = time.perf_counter() - t0
@@ -544,13 +554,15 @@ def run_e2e(st, wl, E, Ew, args, dev):
             tot_t += dt
             tot_b += wl.kv_bytes(lens_np)
             bytes_h2d = (hq[i].numel() * hq[i].element_size() + hk[i].numel() * hk[i].element_size()
-                         + hv[i].numel() * hv[i].element_size() + S * 8 + npair * 16 + h_tables.numel() * 4 + S * 4)
+                         + hv[i].numel() * hv[i].element_size() + S * 8 + npair * 16 + h_tables.numel() * 4 + S * 4
+                         + (0 if args.no_order else S * 4))
     kind, idx = pk.pk_get_device_error()
     if kind:
         raise RuntimeError(f"device error in the e2e steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
     return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(bytes_h2d),
             "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "steps": E,
-            "ms_per_step": 1e3 * tot_t / E, "includes": "host block-manager append + table export, H2D, kernels, D2H",
+            "ms_per_step": 1e3 * tot_t / E,
+            "includes": "host block-manager append, table export, launch order, H2D, kernels, D2H",
             "_seconds": tot_t, "_bytes": tot_b}
 
 

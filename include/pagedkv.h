@@ -69,7 +69,8 @@ enum {
     PK_DEVERR_BLOCK_ID = 2,    /* block table entry outside [0, num_blocks)            */
     PK_DEVERR_PAIR = 3,        /* copy_blocks pair outside [0, num_blocks)             */
     PK_DEVERR_CONTEXT = 4,     /* context_lens entry < 1 or beyond the table / bound   */
-    PK_DEVERR_TIMEOUT = 5      /* a pipeline wait gave up (never expected)             */
+    PK_DEVERR_TIMEOUT = 5,     /* a pipeline wait gave up (never expected)             */
+    PK_DEVERR_ORDER = 6        /* seq_order entry outside [0, num_seqs)                */
 };
 
 /* Geometry of one layer's KV pool. */
@@ -140,8 +141,13 @@ pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cach
                                     void *workspace, size_t workspace_bytes,
                                     const pk_cache_desc *desc, void *stream);
 
-/* As pk_paged_attention_decode, with the kernel chosen explicitly
- * (PK_ERR_UNSUPPORTED if that kernel is not compiled for the shape). */
+/* As pk_paged_attention_decode, plus two scheduling controls:
+ *   seq_order  optional device int32 [S], a permutation of 0..S-1: the order in
+ *              which sequences' work is launched (NULL = index order). Results
+ *              do not depend on it; launching the longest sequences first
+ *              (pk_longest_first_order) keeps the longest work from trailing.
+ *              An entry outside [0, S) is recorded (PK_DEVERR_ORDER).
+ *   impl       the kernel (PK_ERR_UNSUPPORTED if not compiled for the shape). */
 pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
                                          const void *v_cache, const int32_t *block_tables,
                                          const int32_t *context_lens, float scale,
@@ -149,7 +155,13 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
                                          int32_t max_blocks_per_seq, int32_t max_context_len,
                                          int32_t partition_size, void *workspace,
                                          size_t workspace_bytes, const pk_cache_desc *desc,
-                                         pk_attn_impl impl, void *stream);
+                                         const int32_t *seq_order, pk_attn_impl impl,
+                                         void *stream);
+
+/* Host helper for seq_order: order_out[0..n-1] = sequence indices sorted by
+ * descending context_lens (host int32 [n]), ties by index. */
+pk_status pk_longest_first_order(const int32_t *context_lens, int32_t num_seqs,
+                                 int32_t *order_out);
 
 /* Allocation-free decode attention. The pages have no counterpart: this is a
  * library convenience for callers that cannot allocate device memory -- a

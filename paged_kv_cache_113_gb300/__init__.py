@@ -39,14 +39,14 @@ PK_ERR_INVARIANT, PK_ERR_NOMEM = 8, 9
 PK_F32, PK_BF16 = 0, 1
 IMPLS = {"auto": 0, "simt": 1, "mma": 2}
 PK_STATIC_WORKSPACE_BYTES = 64 << 20  # the static split-K scratch of pk_paged_attention_decode_static
-DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5: "timeout"}
+DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5: "timeout", 6: "order"}
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = (
     "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
     "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static",
     "pk_paged_attention_resolve_partition",
-    "pk_paged_attention_workspace_size", "pk_get_device_error", "pk_status_string",
+    "pk_paged_attention_workspace_size", "pk_longest_first_order", "pk_get_device_error", "pk_status_string",
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
@@ -84,7 +84,8 @@ def lib() -> ctypes.CDLL:
         "pk_copy_blocks": (i32, [P, P, P, i32, D, P]),
         "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D, P]),
         "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
-                                                 i32, P]),
+                                                 P, i32, P]),
+        "pk_longest_first_order": (i32, [P, i32, P]),
         "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),
         "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
         "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
@@ -205,16 +206,25 @@ def pk_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len, pa
                                                        int(partition_size), ctypes.byref(desc)))
 
 
+def pk_longest_first_order(context_lens) -> np.ndarray:
+    """Host helper: sequence indices by descending context length (ties by index)."""
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.empty(max(len(lens), 1), np.int32)
+    _check(lib().pk_longest_first_order(_np_ptr(lens), len(lens), _np_ptr(out)), "pk_longest_first_order")
+    return out[: len(lens)]
+
+
 def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                               max_context_len: int, partition_size: int = -1, workspace=None,
-                              impl: str = "auto", stream=None):
+                              impl: str = "auto", stream=None, seq_order=None):
     """Decode attention through the block tables; writes ``out`` ``[S, Hq, d]``.
 
     ``block_tables`` int32 ``[S, max_blocks]``, ``context_lens`` int32 ``[S]``
     (lengths after the step token). ``partition_size``: 0 = no split, -1 =
     automatic, >0 = split-K partition in tokens. ``workspace``: a CUDA tensor
     of at least :func:`pk_paged_attention_workspace_size` bytes when the
-    partitioning splits.
+    partitioning splits. ``seq_order``: optional int32 CUDA tensor ``[S]``, the
+    launch order of the sequences (see :func:`pk_longest_first_order`).
     """
     torch = _torch()
     desc = cache_desc(k_cache)
@@ -234,7 +244,9 @@ def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_le
         _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
         float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
-        ws_ptr, ws_bytes, ctypes.byref(desc), IMPLS[impl], _stream(stream)), "pk_paged_attention_decode")
+        ws_ptr, ws_bytes, ctypes.byref(desc),
+        None if seq_order is None else _dev(seq_order, "seq_order", torch.int32),
+        IMPLS[impl], _stream(stream)), "pk_paged_attention_decode")
 
 
 def pk_paged_attention_decode_static(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -31,6 +31,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pagedkv.h"
@@ -52,6 +53,7 @@ struct AttnParams {
   float *ws_acc;             // [S, Hq, P, D] unnormalised partial outputs
   float *ws_m;               // [S, Hq, P] running maxima (log2 domain)
   float *ws_l;               // [S, Hq, P] softmax denominators
+  const int32_t *order;      // [S] launch order of the sequences, or null
   float scale_log2;          // scale * log2(e)
   int32_t num_seqs, num_q_heads, num_kv_heads, group;
   int32_t block_size, max_blocks, num_blocks;
@@ -71,6 +73,20 @@ __device__ __forceinline__ int context_len(const AttnParams &p, int s, bool reco
   return c;
 }
 
+// The sequence this CTA serves: order[blockIdx.y] when a launch order is
+// given (an out-of-range entry is recorded and falls back to blockIdx.y).
+__device__ __forceinline__ int launch_seq(const AttnParams &p) {
+  const int y = int(blockIdx.y);
+  if (!p.order) return y;
+  const int s = __ldg(p.order + y);
+  if (s < 0 || s >= p.num_seqs) {
+    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+      pk::record_error(&g_attn_error, PK_DEVERR_ORDER, y);
+    return y;
+  }
+  return s;
+}
+
 // ---------------------------------------------------------------------------
 // CUDA-core kernel (fp32 and bf16): one warp per token, lanes split the head
 // dimension, dot products reduced with shuffles, online softmax per head.
@@ -79,7 +95,12 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
   constexpr int NW = 4;
   constexpr int EPL = D / 32;  // elements per lane
-  const int kvh = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+  // Partitions launch last-first: the higher ones exist only for the longest
+  // sequences, so the heaviest work starts early and short work fills the end.
+  const int kvh = blockIdx.x, part = p.num_partitions - 1 - int(blockIdx.z);
+  // Sequences launch in the caller's order when one is given (longest first
+  // keeps the longest work from trailing the launch).
+  const int s = launch_seq(p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -224,7 +245,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   auto full_bar = [&](int i) { return bars + 8u * i; };
   auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
 
-  const int kvh = blockIdx.x, s = blockIdx.y, part = blockIdx.z;
+  // Partitions launch last-first: the higher ones exist only for the longest
+  // sequences, so the heaviest work starts early and short work fills the end.
+  const int kvh = blockIdx.x, part = p.num_partitions - 1 - int(blockIdx.z);
+  // Sequences launch in the caller's order when one is given (longest first
+  // keeps the longest work from trailing the launch).
+  const int s = launch_seq(p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -533,7 +559,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
 #define PK_MMA_WARPS 4
 #endif
 #ifndef PK_MMA_STAGES
-#define PK_MMA_STAGES 3
+#define PK_MMA_STAGES 2
 #endif
 constexpr int kMmaWarps = PK_MMA_WARPS;
 constexpr int kMmaStages = PK_MMA_STAGES;
@@ -606,9 +632,29 @@ pk_status launch_merge(const AttnParams &p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
+// SMs of the current device (152 on GB300 when no device can be queried).
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();  // clear a failed query on a machine without a GPU
+  return 152;
+}
+
 bool mma_supported(const pk_cache_desc &d, int group) {
   return d.dtype == PK_BF16 && (d.head_dim == 64 || d.head_dim == 128) &&
          (d.block_size == 8 || d.block_size == 16 || d.block_size == 32) && group <= kMaxGroup;
+}
+
+// Split-K partials (when the partitioning splits).
+size_t partial_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len, int32_t part,
+                     int32_t head_dim) {
+  if (part <= 0) return 0;
+  const int64_t P = (int64_t(max_context_len) + part - 1) / part;
+  if (P <= 1) return 0;
+  const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
+  return size_t(rows) * (size_t(head_dim) + 2) * sizeof(float);
 }
 
 pk_status check_common(const pk_cache_desc *desc, int32_t num_seqs, int32_t num_q_heads,
@@ -651,16 +697,20 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
   if (partition_size != -1) return -1;
   // Automatic: every partition costs a CTA prologue/epilogue and merge
   // traffic, so split only when the (sequence, KV head) units cannot fill the
-  // GPU several times over (measured on GB300: 64 sequences x 32 heads and
-  // 256 x 8 run fastest unsplit; 8 x 8 heads of 32K tokens fastest with
-  // 2048-token partitions). Aim for ~1024 work items, partitions a power of two
-  // of at least 512 tokens (multiples of every block size and stage).
+  // resident CTA slots twice over. Then cut each context into P equal
+  // partitions (multiples of 64 tokens, at least 512) with P chosen so that the
+  // work items fill the slots in four whole waves.
   const int64_t units = int64_t(num_seqs) * desc->num_kv_heads;
-  if (units >= 512 || max_context_len <= 512) return 0;
-  int64_t part = 512;
-  while (part * 2 < max_context_len && units * ((max_context_len + 2 * part - 1) / (2 * part)) >= 1024)
-    part *= 2;
-  return int32_t(part);
+  // Waves are counted in units of two CTAs per SM: on GB300 32K-token
+  // contexts over 64 units ran fastest with 19 partitions (1728 tokens).
+  const int64_t slots = int64_t(sm_count()) * 2;
+  if (units >= 2 * slots || max_context_len <= 512) return 0;
+  const int64_t P = (4 * slots + units - 1) / units;
+  int64_t part = (max_context_len + P - 1) / P;
+  part = (part + 63) / 64 * 64;
+  if (part < 512) part = 512;
+  part = (part + B - 1) / B * B;
+  return part >= max_context_len ? 0 : int32_t(part);
 }
 
 size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
@@ -668,11 +718,8 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          const pk_cache_desc *desc) {
   const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads,
                                                             max_context_len, partition_size, desc);
-  if (part <= 0) return 0;
-  const int64_t P = (int64_t(max_context_len) + part - 1) / part;
-  if (P <= 1) return 0;
-  const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
-  return size_t(rows) * (size_t(desc->head_dim) + 2) * sizeof(float);
+  if (part < 0) return 0;
+  return partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
 }
 
 pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
@@ -682,7 +729,8 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
                                          int32_t max_blocks_per_seq, int32_t max_context_len,
                                          int32_t partition_size, void *workspace,
                                          size_t workspace_bytes, const pk_cache_desc *desc,
-                                         pk_attn_impl impl, void *stream) {
+                                         const int32_t *seq_order, pk_attn_impl impl,
+                                         void *stream) {
   pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
   if (st != PK_OK) return st;
   if (num_seqs == 0) return PK_OK;
@@ -721,15 +769,16 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   }
   p.num_partitions = int32_t(P);
   if (num_seqs > 65535 || P > 65535) return PK_ERR_UNSUPPORTED;
+  const size_t pbytes = partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
+  if (workspace && !aligned16(workspace)) return PK_ERR_WORKSPACE;
   if (P > 1) {
-    const size_t need = pk_paged_attention_workspace_size(num_seqs, num_q_heads, max_context_len,
-                                                          partition_size, desc);
-    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PK_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < pbytes) return PK_ERR_WORKSPACE;
     const size_t rows = size_t(num_seqs) * num_q_heads * size_t(P);
     p.ws_acc = static_cast<float *>(workspace);
     p.ws_m = p.ws_acc + rows * desc->head_dim;
     p.ws_l = p.ws_m + rows;
   }
+  p.order = seq_order;
 
   const bool mma_ok = mma_supported(*desc, p.group);
   if (impl == PK_ATTN_MMA && !mma_ok) return PK_ERR_UNSUPPORTED;
@@ -767,10 +816,19 @@ pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cach
   return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
                                         scale, num_seqs, num_q_heads, max_blocks_per_seq,
                                         max_context_len, partition_size, workspace,
-                                        workspace_bytes, desc, PK_ATTN_AUTO, stream);
+                                        workspace_bytes, desc, nullptr, PK_ATTN_AUTO, stream);
 }
 
 }  // extern "C"
+
+extern "C" pk_status pk_longest_first_order(const int32_t *context_lens, int32_t num_seqs,
+                                            int32_t *order_out) {
+  if (num_seqs < 0 || (num_seqs > 0 && (!context_lens || !order_out))) return PK_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < num_seqs; ++i) order_out[i] = i;
+  std::stable_sort(order_out, order_out + num_seqs,
+                   [&](int32_t a, int32_t b) { return context_lens[a] > context_lens[b]; });
+  return PK_OK;
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the decode attention
@@ -834,5 +892,5 @@ extern "C" pk_status pk_paged_attention_decode_static(
                                         scale, num_seqs, num_q_heads, max_blocks_per_seq,
                                         max_context_len, partition_size, ws,
                                         need > 0 ? size_t(PK_STATIC_WORKSPACE_BYTES) : 0, desc,
-                                        PK_ATTN_AUTO, stream);
+                                        nullptr, PK_ATTN_AUTO, stream);
 }

@@ -18,7 +18,7 @@ from typing import List, Optional
 
 import numpy as np
 
-from . import (BlockManager, pk_copy_blocks, pk_paged_attention_decode,
+from . import (BlockManager, pk_copy_blocks, pk_longest_first_order, pk_paged_attention_decode,
                pk_paged_attention_resolve_partition, pk_paged_attention_workspace_size,
                pk_reshape_and_cache, cache_desc)
 
@@ -53,6 +53,7 @@ class StepInputs:
     pairs: np.ndarray       # int64 [n, 2]
     tables: np.ndarray      # int32 [S, max_blocks]
     ctx_lens: np.ndarray    # int32 [S]
+    order: np.ndarray       # int32 [S], launch order (longest first)
 
     @property
     def max_context_len(self) -> int:
@@ -113,7 +114,7 @@ class DecodeState:
         slots, pairs = self.bm.append_batch(range(wl.num_seqs))
         tables, lens = self.bm.export_tables(range(wl.num_seqs), self.max_blocks)
         self.steps_done += 1
-        return StepInputs(step, q, k, v, slots, pairs, tables, lens)
+        return StepInputs(step, q, k, v, slots, pairs, tables, lens, pk_longest_first_order(lens))
 
     def upload(self, si: StepInputs) -> dict:
         """The step's inputs as device tensors."""
@@ -127,6 +128,7 @@ class DecodeState:
             "pairs": torch.from_numpy(np.ascontiguousarray(si.pairs, dtype=np.int64).reshape(-1, 2)).to(dev),
             "tables": torch.from_numpy(si.tables).to(dev),
             "ctx_lens": torch.from_numpy(si.ctx_lens).to(dev),
+            "order": torch.from_numpy(si.order).to(dev),
             "max_context_len": si.max_context_len,
         }
 
@@ -161,7 +163,8 @@ class DecodeState:
         self.attention(d, out, workspace, partition_size, impl, stream)
 
     def attention(self, d: dict, out, workspace=None, partition_size: int = -1, impl: str = "auto",
-                  stream=None):
+                  stream=None, ordered: bool = True):
+        """The attention call; ``ordered`` launches the longest sequences first."""
         pk_paged_attention_decode(out, d["q"], self.k_cache, self.v_cache, d["tables"], d["ctx_lens"],
                                   self.wl.scale, d["max_context_len"], partition_size, workspace, impl,
-                                  stream)
+                                  stream, seq_order=d.get("order") if ordered else None)

@@ -206,14 +206,17 @@ def test_partition_resolution_and_workspace_size(L):
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 512, d) == 512
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 0, d) == 0
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 40, d) == -1      # not a multiple of B
-    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 2048    # few units: split
-    assert pk.pk_paged_attention_resolve_partition(2, 16, 32768, -1, d) == 512     # fewer units: finer
-    assert pk.pk_paged_attention_resolve_partition(64, 64, 2048, -1, d) == 0       # many units: whole
+    # Automatic (152 SMs when no GPU is visible): 64 units of 32K tokens split
+    # into 19 partitions of 1728 tokens (4 waves of 2 CTAs per SM).
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 1728
+    assert pk.pk_paged_attention_resolve_partition(2, 16, 32768, -1, d) == 512     # at least 512 tokens
+    assert pk.pk_paged_attention_resolve_partition(64, 64, 2048, -1, d) == 704     # 512 units: 3 partitions
+    assert pk.pk_paged_attention_resolve_partition(256, 64, 2048, -1, d) == 0      # 2048 units: whole
     assert pk.pk_paged_attention_resolve_partition(8, 64, 300, -1, d) == 0         # short: no split
     assert pk.pk_paged_attention_resolve_partition(8, 60, 300, -1, d) == -1        # Hq % Hk != 0
     assert pk.pk_paged_attention_resolve_partition(8, 128, 300, -1, d) == -1       # group of 16
     ws = pk.pk_paged_attention_workspace_size(8, 64, 32768, 512, d)
-    assert ws == 8 * 64 * 64 * (128 + 2) * 4
+    assert ws == 8 * 64 * 64 * (128 + 2) * 4                                        # [S, Hq, P, d+2] fp32
     assert pk.pk_paged_attention_workspace_size(8, 64, 512, 512, d) == 0           # one partition
     assert pk.pk_paged_attention_workspace_size(8, 64, 32768, 0, d) == 0
 
@@ -239,3 +242,11 @@ def test_host_checks_reject_before_launch(L):
     a4 = list(args)
     a4[14] = ctypes.byref(odd)
     assert L.pk_paged_attention_decode(*a4) == 2            # head_dim 96 not compiled
+
+
+def test_longest_first_order(L):
+    rng = np.random.default_rng(5)
+    for n in (0, 1, 7, 300):
+        lens = rng.integers(1, 50, size=n).astype(np.int32)   # many ties
+        got = pk.pk_longest_first_order(lens)
+        assert got.tolist() == np.lexsort((np.arange(n), -lens)).tolist()

@@ -211,6 +211,36 @@ def test_split_matches_unsplit():
         assert mx <= 8e-3 and rl <= 2e-3, (part, mx, rl)
 
 
+@pytest.mark.parametrize("impl", ["simt", "mma"])
+def test_launch_order_does_not_change_bits(impl):
+    """Longest-first, index order and a random order give identical outputs."""
+    wl = make_workload("gqa8b", num_seqs=40)
+    wl.enable_memo()
+    st = DecodeState(wl, "cuda")
+    d = st.upload(st.prepare_step(0))
+    rnd = torch.from_numpy(np.random.default_rng(3).permutation(wl.num_seqs).astype(np.int32)).cuda()
+    for part in (0, 256):
+        outs = []
+        for order in (d["order"], None, rnd):
+            out = st.new_out()
+            pk.pk_paged_attention_decode(out, d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"],
+                                         wl.scale, d["max_context_len"], part,
+                                         st.alloc_workspace(d["max_context_len"], part), impl, seq_order=order)
+            outs.append(from_device(out))
+        _no_device_error()
+        assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_bad_launch_order_is_recorded():
+    wl, st, d = _small_state()
+    order = torch.tensor([0, 7, 2], dtype=torch.int32, device="cuda")
+    out = st.new_out()
+    pk.pk_paged_attention_decode(out, d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"], wl.scale,
+                                 d["max_context_len"], 0, None, "mma", seq_order=order)
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "order" and idx == 1
+
+
 def test_standalone_copy_blocks_each_block_size():
     """96 copies (each group's last prefix block to three fresh blocks), bit-exact."""
     for B in (8, 16, 32):
