@@ -342,10 +342,15 @@ def run_ours(args):
 
     flush = _Flush()
 
+    # Kernels one step launches: copy_blocks (if pairs), the scatter, the
+    # attention kernel, and -- for the CUDA-core kernel only -- a separate
+    # split-K merge (the tensor-core kernel merges inside its last partition).
+    simt = args.attn_impl == "simt" or wl.dtype == "f32"
+
     def launches(si):
         part = st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
-        return (1 if len(si.pairs) else 0) + 2 + (1 if split else 0)
+        return (1 if len(si.pairs) else 0) + 2 + (1 if split and simt else 0)
 
     def cache_writes(d):
         if d["pairs"].shape[0]:
@@ -462,7 +467,7 @@ def run_ours(args):
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
                 "launch": "CUDA graphs per step" if graphs else "eager",
                 "seq_order": "index" if args.no_order else "longest first (host)"}),
-            "roofline": {"bound": "hbm", "kernel": "paged attention (attn_*_kernel + merge when split)",
+            "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel",
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": ncu_traffic(wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"),

@@ -200,7 +200,10 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
 /* Bytes of split-K workspace pk_paged_attention_decode needs for these
  * arguments (0 when the resolved partitioning does not split). Layout inside:
  * fp32 partial outputs [S, Hq, P, d], then running maxima and sums [S, Hq, P]
- * each, P = ceil(max_context_len / partition). Host only. */
+ * each, P = ceil(max_context_len / partition), then one 8-byte merge ticket
+ * per (sequence, KV head). Tickets are tagged per call, so the workspace
+ * needs no clearing; calls whose work overlaps on the GPU must not share a
+ * workspace. Host only. */
 size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, int32_t partition_size,
                                          const pk_cache_desc *desc);

@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pagedkv.h"
@@ -54,6 +55,8 @@ struct AttnParams {
   float *ws_m;               // [S, Hq, P] running maxima (log2 domain)
   float *ws_l;               // [S, Hq, P] softmax denominators
   const int32_t *order;      // [S] launch order of the sequences, or null
+  unsigned long long *merge_tickets;  // [S, Hk] arrival tickets of the fused merge, or null
+  uint32_t epoch;            // this call's tag on the tickets
   float scale_log2;          // scale * log2(e)
   int32_t num_seqs, num_q_heads, num_kv_heads, group;
   int32_t block_size, max_blocks, num_blocks;
@@ -85,6 +88,78 @@ __device__ __forceinline__ int launch_seq(const AttnParams &p) {
     return y;
   }
   return s;
+}
+
+// Fused-merge ticket of one (sequence, KV head): returns how many of this
+// call's partitions have arrived, counting the caller. A ticket holds
+// (epoch << 32 | arrivals); a ticket from another call (stale memory, or 0
+// after the previous merge reset it) starts over, so the workspace needs no
+// clearing and a replayed graph finds its tickets reset.
+__device__ __forceinline__ int take_merge_ticket(unsigned long long *t, uint32_t epoch) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(t);
+  for (;;) {
+    const unsigned long long mine = static_cast<unsigned long long>(epoch) << 32;
+    const unsigned long long next = (old >> 32) == epoch ? old + 1 : (mine | 1ull);
+    const unsigned long long seen = atomicCAS(t, old, next);
+    if (seen == old) return int(next & 0xFFFFFFFFull);
+    old = seen;
+  }
+}
+
+// Log-sum-exp merge of the np partials of query heads h0 .. h0+nh-1 of
+// sequence s, spread over `nthreads` threads (thread `tid`), four elements
+// per step. M = max_p m_p, L = sum_p l_p 2^(m_p - M),
+// out = sum_p acc_p 2^(m_p - M) / L. Partials are read from L2 (written by
+// other CTAs of the same launch).
+template <typename T, int D>
+__device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h0, int nh, int np,
+                                               int tid, int nthreads) {
+  for (int idx = tid; idx < nh * (D / 4); idx += nthreads) {
+    const int h = h0 + idx / (D / 4), i = (idx % (D / 4)) * 4;
+    const size_t row = size_t(s) * p.num_q_heads + h;
+    const float *mrow = p.ws_m + row * p.num_partitions;
+    const float *lrow = p.ws_l + row * p.num_partitions;
+    const float *arow = p.ws_acc + row * p.num_partitions * D + i;
+    float M = -INFINITY;
+    for (int q = 0; q < np; ++q) M = fmaxf(M, __ldcg(mrow + q));
+    float L = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int q = 0;
+    for (; q + 4 <= np; q += 4) {
+      float4 x[4];
+      float f[4], l[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        x[u] = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(q + u) * D));
+        f[u] = __ldcg(mrow + q + u);
+        l[u] = __ldcg(lrow + q + u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = exp2f(f[u] - M);
+        L = fmaf(l[u], w, L);
+        acc.x = fmaf(x[u].x, w, acc.x);
+        acc.y = fmaf(x[u].y, w, acc.y);
+        acc.z = fmaf(x[u].z, w, acc.z);
+        acc.w = fmaf(x[u].w, w, acc.w);
+      }
+    }
+    for (; q < np; ++q) {
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(q) * D));
+      const float w = exp2f(__ldcg(mrow + q) - M);
+      L = fmaf(__ldcg(lrow + q), w, L);
+      acc.x = fmaf(x.x, w, acc.x);
+      acc.y = fmaf(x.y, w, acc.y);
+      acc.z = fmaf(x.z, w, acc.z);
+      acc.w = fmaf(x.w, w, acc.w);
+    }
+    const float inv = 1.0f / L;
+    T *o = static_cast<T *>(p.out) + row * D + i;
+    pk::store_elem(o + 0, acc.x * inv);
+    pk::store_elem(o + 1, acc.y * inv);
+    pk::store_elem(o + 2, acc.z * inv);
+    pk::store_elem(o + 3, acc.w * inv);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -224,7 +299,7 @@ struct MmaShape {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;  // K then V
   static constexpr int KSTEPS = D / 16;
   static constexpr int OUT_STRIDE = D + 4;          // padded row of the merge buffer
-  static constexpr int MERGE_BYTES = NW * kMaxGroup * (OUT_STRIDE + 2) * 4;
+  static constexpr int MERGE_BYTES = NW * kMaxGroup * (OUT_STRIDE + 2) * 4 + 16;
   static constexpr int BAR_BYTES = 2 * STAGES * 8;
   static constexpr int SMEM_BYTES = 1024 + BAR_BYTES +
                                     (STAGES * STAGE_BYTES > MERGE_BYTES ? STAGES * STAGE_BYTES
@@ -507,47 +582,42 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       }
     }
   }
+  if (ctx > p.partition && p.merge_tickets) {
+    // Fused merge: the last partition to finish for (s, kvh) merges them all.
+    __threadfence();  // this thread's partials are visible device-wide
+    pk::named_barrier(1, NW * 32);
+    const int np = (ctx + p.partition - 1) / p.partition;
+    volatile int *flag = reinterpret_cast<volatile int *>(sm_l + NW * kMaxGroup);
+    if (threadIdx.x == 0)
+      *flag = take_merge_ticket(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, p.epoch) == np;
+    pk::named_barrier(1, NW * 32);
+    if (*flag) {
+      __threadfence();
+      merge_partials<__nv_bfloat16, D>(p, s, kvh * G, G, np, threadIdx.x, NW * 32);
+      pk::named_barrier(1, NW * 32);
+      if (threadIdx.x == 0) atomicExch(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, 0ull);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of split-K partials: one warp per (sequence, query head).
-//   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p acc_p 2^(m_p - M) / L
+// Log-sum-exp merge of split-K partials for the CUDA-core kernel (the
+// tensor-core kernel fuses the same merge into its last partition).
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
-  constexpr int EPL = D / 32;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= p.num_seqs * p.num_q_heads) return;
-  const int s = row / p.num_q_heads;
+  // One CTA per (sequence, query head) row.
+  const int row = blockIdx.x;
+  const int s = row / p.num_q_heads, h = row % p.num_q_heads;
   const int ctx = context_len(p, s, false);
   const int np = (ctx + p.partition - 1) / p.partition;
-  T *out = static_cast<T *>(p.out) + size_t(row) * D + lane * EPL;
   if (np == 0) {
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) pk::store_elem(out + e, 0.0f);
+    T *out = static_cast<T *>(p.out) + size_t(row) * D;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) pk::store_elem(out + i, 0.0f);
     return;
   }
   if (np == 1) return;  // written directly by the attention kernel
-  const float *mrow = p.ws_m + size_t(row) * p.num_partitions;
-  const float *lrow = p.ws_l + size_t(row) * p.num_partitions;
-  float M = -INFINITY;
-  for (int q = lane; q < np; q += 32) M = fmaxf(M, mrow[q]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.0f, acc[EPL];
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.0f;
-  const float *arow = p.ws_acc + size_t(row) * p.num_partitions * D + lane * EPL;
-  for (int q = 0; q < np; ++q) {
-    const float f = exp2f(mrow[q] - M);
-    L = fmaf(lrow[q], f, L);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(arow[size_t(q) * D + e], f, acc[e]);
-  }
-  const float inv = 1.0f / L;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) pk::store_elem(out + e, acc[e] * inv);
+  merge_partials<T, D>(p, s, h, 1, np, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -628,7 +698,7 @@ pk_status launch_simt(const AttnParams &p, cudaStream_t stream) {
 template <typename T, int D>
 pk_status launch_merge(const AttnParams &p, cudaStream_t stream) {
   const int rows = p.num_seqs * p.num_q_heads;
-  attn_merge_kernel<T, D><<<(rows + 3) / 4, 128, 0, stream>>>(p);
+  attn_merge_kernel<T, D><<<rows, D / 4, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
@@ -655,6 +725,20 @@ size_t partial_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_
   if (P <= 1) return 0;
   const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
   return size_t(rows) * (size_t(head_dim) + 2) * sizeof(float);
+}
+
+// Fused-merge tickets, one 8-byte word per (sequence, KV head), after the
+// partials (only when splitting).
+size_t ticket_bytes(int32_t num_seqs, int32_t num_kv_heads, size_t partials) {
+  return partials ? size_t(num_seqs) * size_t(num_kv_heads) * 8 : 0;
+}
+
+// A distinct non-zero tag per call for the merge tickets.
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e = ++counter;
+  while (e == 0) e = ++counter;
+  return e;
 }
 
 pk_status check_common(const pk_cache_desc *desc, int32_t num_seqs, int32_t num_q_heads,
@@ -719,7 +803,8 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
   const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads,
                                                             max_context_len, partition_size, desc);
   if (part < 0) return 0;
-  return partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
+  const size_t pb = partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
+  return pb + ticket_bytes(num_seqs, desc->num_kv_heads, pb);
 }
 
 pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
@@ -770,9 +855,10 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   p.num_partitions = int32_t(P);
   if (num_seqs > 65535 || P > 65535) return PK_ERR_UNSUPPORTED;
   const size_t pbytes = partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
+  const size_t tbytes = ticket_bytes(num_seqs, desc->num_kv_heads, pbytes);
   if (workspace && !aligned16(workspace)) return PK_ERR_WORKSPACE;
   if (P > 1) {
-    if (!workspace || workspace_bytes < pbytes) return PK_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < pbytes + tbytes) return PK_ERR_WORKSPACE;
     const size_t rows = size_t(num_seqs) * num_q_heads * size_t(P);
     p.ws_acc = static_cast<float *>(workspace);
     p.ws_m = p.ws_acc + rows * desc->head_dim;
@@ -788,6 +874,10 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, B = desc->block_size;
   if (use_mma) {
+    if (P > 1) {
+      p.merge_tickets = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + pbytes);
+      p.epoch = next_epoch();
+    }
     if (D == 128) {
       st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
                   : (B == 16 ? launch_mma<128, 16>(p, *desc, s) : launch_mma<128, 32>(p, *desc, s));
@@ -800,7 +890,7 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   } else {
     st = D == 128 ? launch_simt<__nv_bfloat16, 128>(p, s) : launch_simt<__nv_bfloat16, 64>(p, s);
   }
-  if (st != PK_OK || P == 1) return st;
+  if (st != PK_OK || P == 1 || use_mma) return st;  // the tensor-core kernel merges itself
   if (desc->dtype == PK_F32)
     return D == 128 ? launch_merge<float, 128>(p, s) : launch_merge<float, 64>(p, s);
   return D == 128 ? launch_merge<__nv_bfloat16, 128>(p, s) : launch_merge<__nv_bfloat16, 64>(p, s);

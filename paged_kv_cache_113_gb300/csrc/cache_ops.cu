@@ -15,30 +15,28 @@ namespace {
 
 __device__ int g_cache_ops_error;
 
-// One CTA per new token: token i's K row and V row go to slot slot_mapping[i]
-// ("Paged KV Cache Allocation and the Block Table", append_token: the token
-// is written at physical * block_size + slot).
+// grid.x = new token, grid.y = chunk of its row: token i's K row and V row
+// go to slot slot_mapping[i] ("Paged KV Cache Allocation and the Block
+// Table", append_token: the token is written at physical * block_size +
+// slot). Each thread moves one 16-byte vector of K and one of V, so a whole
+// step's scatter is a single round trip to memory.
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
     int32_t row_vecs) {
   const int64_t i = blockIdx.x;
+  const int32_t j = int32_t(blockIdx.y) * blockDim.x + threadIdx.x;
   const int64_t s = slots[i];
   if (s < 0) return;
   if (s >= num_slots) {
-    if (threadIdx.x == 0) pk::record_error(&g_cache_ops_error, PK_DEVERR_SLOT, i);
+    if (threadIdx.x == 0 && blockIdx.y == 0) pk::record_error(&g_cache_ops_error, PK_DEVERR_SLOT, i);
     return;
   }
-  const uint4 *ksrc = k + i * row_vecs;
-  const uint4 *vsrc = v + i * row_vecs;
-  uint4 *kdst = k_cache + s * row_vecs;
-  uint4 *vdst = v_cache + s * row_vecs;
-  for (int32_t j = threadIdx.x; j < row_vecs; j += blockDim.x) {
-    const uint4 a = __ldg(ksrc + j);
-    const uint4 b = __ldg(vsrc + j);
-    kdst[j] = a;
-    vdst[j] = b;
-  }
+  if (j >= row_vecs) return;
+  const uint4 a = __ldg(k + i * row_vecs + j);
+  const uint4 b = __ldg(v + i * row_vecs + j);
+  k_cache[s * row_vecs + j] = a;
+  v_cache[s * row_vecs + j] = b;
 }
 
 // grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block.
@@ -121,10 +119,14 @@ pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot
     return PK_ERR_INVALID_ARG;
   const int64_t row_bytes = int64_t(desc->num_kv_heads) * desc->head_dim * elem_size(desc->dtype);
   const int64_t num_slots = int64_t(desc->num_blocks) * desc->block_size;
-  reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+  const int64_t row_vecs = row_bytes / 16;
+  const int64_t chunks = (row_vecs + 127) / 128;
+  if (chunks > 65535) return PK_ERR_UNSUPPORTED;
+  reshape_and_cache_kernel<<<dim3(num_tokens, unsigned(chunks)), 128, 0,
+                             static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
-      int32_t(row_bytes / 16));
+      int32_t(row_vecs));
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
