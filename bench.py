@@ -487,88 +487,49 @@ def run_ours(args):
 
 
 def run_e2e(st, wl, E, Ew, args, dev):
-    """The same decode steps through the public API from pinned host memory."""
+    """The same decode steps through the public API from pinned host memory:
+    one pk_decode_step call per step (host block-manager append, table
+    export and launch order, one metadata transfer plus the q/k/v copies, the
+    kernels, the output copy back), then a stream synchronise."""
     import torch
     import paged_kv_cache_113_gb300 as pk
-    S = wl.num_seqs
-    tdt = st.torch_dtype
 
-    def pinned_from(a):
+    def pinned(a):
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16" \
             else torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
         return t.pin_memory()
 
-    steps = [wl.step_inputs(10_000 + i) for i in range(E + Ew)]
-    hq = [pinned_from(q) for q, _, _ in steps]
-    hk = [pinned_from(k) for _, k, _ in steps]
-    hv = [pinned_from(v) for _, _, v in steps]
-    h_tables = torch.empty((S, st.max_blocks), dtype=torch.int32).pin_memory()
-    h_lens = torch.empty(S, dtype=torch.int32).pin_memory()
-    h_slots = torch.empty(S, dtype=torch.int64).pin_memory()
-    h_pairs = torch.empty((S, 2), dtype=torch.int64).pin_memory()
-    h_order = torch.empty(S, dtype=torch.int32).pin_memory()
-    h_out = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt).pin_memory()
-    d_q = torch.empty((S, wl.num_q_heads, wl.head_dim), dtype=tdt, device=dev)
-    d_k = torch.empty((S, wl.num_kv_heads, wl.head_dim), dtype=tdt, device=dev)
-    d_v = torch.empty_like(d_k)
-    d_tables = torch.empty((S, st.max_blocks), dtype=torch.int32, device=dev)
-    d_lens = torch.empty(S, dtype=torch.int32, device=dev)
-    d_slots = torch.empty(S, dtype=torch.int64, device=dev)
-    d_pairs = torch.empty((S, 2), dtype=torch.int64, device=dev)
-    d_order = torch.empty(S, dtype=torch.int32, device=dev)
-    d_out = torch.empty_like(h_out, device=dev)
-    tables_np, lens_np = h_tables.numpy(), h_lens.numpy()
-    seq_ids = np.arange(S, dtype=np.int64)
+    inputs = [tuple(pinned(x) for x in wl.step_inputs(10_000 + i)) for i in range(E + Ew)]
+    max_ctx = int(wl.ctx_lens.max()) + st.steps_done + E + Ew + 1
+    stepper = pk.DecodeStepper(st.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, st.max_blocks,
+                               st.k_cache, st.v_cache, args.partition, max_context_len=max_ctx)
     stream = torch.cuda.current_stream()
-    bytes_h2d = 0
     tot_t, tot_b = 0.0, 0
-    max_ctx_bound = int(wl.ctx_lens.max()) + st.steps_done + E + Ew + 1
-    ws = st.alloc_workspace(max_ctx_bound, args.partition)
     for i in range(E + Ew):
-        torch.cuda.synchronize()
+        q, k, v = inputs[i]
+        stream.synchronize()
         t0 = time.perf_counter()
-        slots, pairs = st.bm.append_batch(seq_ids)
-        st.bm.export_tables(seq_ids, st.max_blocks, tables_out=tables_np, lens_out=lens_np)
-        npair = len(pairs)
-        h_slots.numpy()[:] = slots
-        if not args.no_order:
-            h_order.numpy()[:] = pk.pk_longest_first_order(lens_np)
-        if npair:
-            h_pairs.numpy()[:npair] = pairs
-        d_q.copy_(hq[i], non_blocking=True)
-        d_k.copy_(hk[i], non_blocking=True)
-        d_v.copy_(hv[i], non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        d_tables.copy_(h_tables, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
-        if not args.no_order:
-            d_order.copy_(h_order, non_blocking=True)
-        if npair:
-            d_pairs[:npair].copy_(h_pairs[:npair], non_blocking=True)
-            pk.pk_copy_blocks(st.k_cache, st.v_cache, d_pairs[:npair])
-        pk.pk_reshape_and_cache(d_k, d_v, d_slots, st.k_cache, st.v_cache)
-        mc = int(lens_np.max())
-        pk.pk_paged_attention_decode(d_out, d_q, st.k_cache, st.v_cache, d_tables, d_lens, wl.scale, mc,
-                                     args.partition, ws, args.attn_impl,
-                                     seq_order=None if args.no_order else d_order)
-        h_out.copy_(d_out, non_blocking=True)
+        stepper.launch(q_host=q, k_host=k, v_host=v)
         stream.synchronize()
         dt = time.perf_counter() - t0
         st.steps_done += 1
         if i >= Ew:
             tot_t += dt
-            tot_b += wl.kv_bytes(lens_np)
-            bytes_h2d = (hq[i].numel() * hq[i].element_size() + hk[i].numel() * hk[i].element_size()
-                         + hv[i].numel() * hv[i].element_size() + S * 8 + npair * 16 + h_tables.numel() * 4 + S * 4
-                         + (0 if args.no_order else S * 4))
+            tot_b += step_kv_bytes(st, wl)
     kind, idx = pk.pk_get_device_error()
     if kind:
         raise RuntimeError(f"device error in the e2e steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
-    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(bytes_h2d),
-            "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()), "steps": E,
-            "ms_per_step": 1e3 * tot_t / E,
-            "includes": "host block-manager append, table export, launch order, H2D, kernels, D2H",
+    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(stepper.h2d_bytes),
+            "d2h_bytes_per_step": int(stepper.d2h_bytes), "steps": E, "ms_per_step": 1e3 * tot_t / E,
+            "includes": "pk_decode_step: host block-manager append, table export, launch order, "
+                        "H2D (q, k, v, one metadata buffer), kernels, D2H of the output; stream sync",
             "_seconds": tot_t, "_bytes": tot_b}
+
+
+def step_kv_bytes(st, wl) -> int:
+    """K/V bytes the step just run read: the sequences' current lengths."""
+    lens = np.array([st.bm.seq_len(s) for s in range(wl.num_seqs)], dtype=np.int64)
+    return wl.kv_bytes(lens)
 
 
 def main(argv=None):

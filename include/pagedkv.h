@@ -283,6 +283,52 @@ pk_status pk_bm_check_invariants(const pk_bm *bm);
 pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_slots,
                       int64_t *tail_waste, int32_t *shared_blocks, int64_t *cow_copies);
 
+/* ------------------------------------------------------------------------ */
+/* One decode step from host buffers                                        */
+/* ------------------------------------------------------------------------ */
+/* Buffers of pk_decode_step. Host pointers should be pinned (page-locked) so
+ * the copies are asynchronous; device pointers are caller-owned, 16-byte
+ * aligned. */
+typedef struct {
+    const void *q_host;  /* [S, Hq, d] queries of the step                     */
+    const void *k_host;  /* [S, Hk, d] the step's new keys                      */
+    const void *v_host;  /* [S, Hk, d] the step's new values                    */
+    void *q_dev;         /* device copies of the three above                   */
+    void *k_dev;
+    void *v_dev;
+    void *meta_host;     /* pinned staging of pk_decode_step_meta_bytes bytes  */
+    void *meta_dev;      /* device staging of the same size                    */
+    size_t meta_bytes;
+    void *out_dev;       /* [S, Hq, d] attention output on the device           */
+    void *out_host;      /* [S, Hq, d] its host copy                            */
+    void *workspace;     /* split-K workspace (see pk_paged_attention_decode)   */
+    size_t workspace_bytes;
+} pk_step_buffers;
+
+/* Bytes of pk_step_buffers.meta_host / meta_dev for S sequences and tables of
+ * max_blocks_per_seq entries (0 for non-positive arguments). */
+size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
+
+/* One decode step of the whole path for the sequences seq_ids[0..S-1] (host):
+ *   1. host: append one token to each sequence (pk_bm_append_batch), export
+ *      the padded tables and lengths, order the sequences longest first --
+ *      all into meta_host;
+ *   2. copies host -> device: q, k, v from the caller's host buffers and the
+ *      metadata in one transfer;
+ *   3. device: pk_copy_blocks for the step's copy-on-write pairs, the slot
+ *      scatter of k/v, the attention (automatic kernel, the given
+ *      partition_size, the launch order);
+ *   4. copy device -> host of the output into out_host.
+ * All work is enqueued on `stream`; out_host holds the result once the stream
+ * is synchronised, and meta_host must not be reused before then. The paper has
+ * no counterpart for this packaging; each step it performs is the pages'
+ * (see the entry points above). On an error after step 1 the block manager
+ * keeps the appended tokens. */
+pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
+                         float scale, int32_t max_blocks_per_seq, int32_t partition_size,
+                         void *k_cache, void *v_cache, const pk_cache_desc *desc,
+                         const pk_step_buffers *buffers, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

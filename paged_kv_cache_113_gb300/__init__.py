@@ -50,6 +50,7 @@ EXPORTED = (
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
+    "pk_decode_step_meta_bytes", "pk_decode_step",
 )
 
 
@@ -57,6 +58,14 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32)]
+
+
+class StepBuffers(ctypes.Structure):
+    _fields_ = [("q_host", ctypes.c_void_p), ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
+                ("q_dev", ctypes.c_void_p), ("k_dev", ctypes.c_void_p), ("v_dev", ctypes.c_void_p),
+                ("meta_host", ctypes.c_void_p), ("meta_dev", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
+                ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class PagedKVError(RuntimeError):
@@ -105,6 +114,8 @@ def lib() -> ctypes.CDLL:
         "pk_bm_refcount": (i32, [P, i32]),
         "pk_bm_check_invariants": (i32, [P]),
         "pk_bm_stats": (i32, [P, P, P, P, P, P]),
+        "pk_decode_step_meta_bytes": (sz, [i32, i32]),
+        "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -378,3 +389,64 @@ class BlockManager:
                                    ctypes.byref(shared), ctypes.byref(cow)), "pk_bm_stats")
         return {"live_tokens": live.value, "reserved_slots": res.value, "tail_waste": waste.value,
                 "shared_blocks": shared.value, "cow_copies": cow.value}
+
+
+class DecodeStepper:
+    """Runs whole decode steps from pinned host buffers through pk_decode_step.
+
+    Owns the pinned host staging (queries, new K/V, metadata, output) and the
+    device buffers of one batch shape. ``step(q, k, v)`` copies the step's
+    host arrays into the pinned staging, calls pk_decode_step (host append,
+    one metadata transfer, the kernels, the output copy) and synchronises;
+    the output is then in ``out_host``.
+    """
+
+    def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
+                 k_cache, v_cache, partition_size: int = -1, max_context_len: Optional[int] = None):
+        torch = _torch()
+        self.bm, self.k_cache, self.v_cache = bm, k_cache, v_cache
+        self.desc = cache_desc(k_cache)
+        self.ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        S, Hk, d = len(self.ids), self.desc.num_kv_heads, self.desc.head_dim
+        self.S, self.Hq, self.scale, self.maxb, self.partition = S, int(num_q_heads), float(scale), \
+            int(max_blocks_per_seq), int(partition_size)
+        dt, dev = k_cache.dtype, k_cache.device
+        self.q_host = torch.empty((S, self.Hq, d), dtype=dt).pin_memory()
+        self.k_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
+        self.v_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
+        self.out_host = torch.empty((S, self.Hq, d), dtype=dt).pin_memory()
+        self.q_dev = torch.empty_like(self.q_host, device=dev)
+        self.k_dev = torch.empty_like(self.k_host, device=dev)
+        self.v_dev = torch.empty_like(self.v_host, device=dev)
+        self.out_dev = torch.empty_like(self.out_host, device=dev)
+        mb = int(lib().pk_decode_step_meta_bytes(S, self.maxb))
+        self.meta_host = torch.empty(mb, dtype=torch.uint8).pin_memory()
+        self.meta_dev = torch.empty(mb, dtype=torch.uint8, device=dev)
+        mc = self.maxb * self.desc.block_size if max_context_len is None else int(max_context_len)
+        wsb = pk_paged_attention_workspace_size(S, self.Hq, mc, self.partition, self.desc)
+        self.workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
+        self.buffers = StepBuffers(
+            self.q_host.data_ptr(), self.k_host.data_ptr(), self.v_host.data_ptr(),
+            self.q_dev.data_ptr(), self.k_dev.data_ptr(), self.v_dev.data_ptr(),
+            self.meta_host.data_ptr(), self.meta_dev.data_ptr(), mb,
+            self.out_dev.data_ptr(), self.out_host.data_ptr(),
+            None if self.workspace is None else self.workspace.data_ptr(), wsb)
+        self.h2d_bytes = (self.q_host.numel() + self.k_host.numel() + self.v_host.numel()) * \
+            self.q_host.element_size() + mb
+        self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
+
+    def launch(self, stream=None, q_host=None, k_host=None, v_host=None):
+        """Enqueues one step from q_host/k_host/v_host (the stepper's own pinned
+        buffers unless other pinned tensors are given)."""
+        for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
+            setattr(self.buffers, name, (getattr(self, name) if t is None else t).data_ptr())
+        _check(lib().pk_decode_step(self.bm._h, _np_ptr(self.ids), self.S, self.Hq, self.scale, self.maxb,
+                                    self.partition, ctypes.c_void_p(self.k_cache.data_ptr()),
+                                    ctypes.c_void_p(self.v_cache.data_ptr()), ctypes.byref(self.desc),
+                                    ctypes.byref(self.buffers), _stream(stream)), "pk_decode_step")
+
+    def step(self, stream=None):
+        """One step and a stream synchronise; returns the host output tensor."""
+        self.launch(stream)
+        (_torch().cuda.current_stream() if stream is None else stream).synchronize()
+        return self.out_host

@@ -1,0 +1,118 @@
+// One decode step from host buffers, in native code: the host block manager
+// appends a token to every sequence, the step's metadata (slots, copy-on-write
+// pairs, padded block tables, context lengths, launch order) is packed into
+// one pinned staging buffer and copied to the device with a single transfer,
+// the new tokens' K/V and the queries are copied from the caller's host
+// buffers, then copy_blocks (when pairs exist), the slot scatter and the
+// attention run, and the output is copied back to host memory. Everything is
+// enqueued on one stream; the call returns once the work is enqueued.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct MetaLayout {
+  size_t slots, pairs, tables, lens, order, total;
+};
+
+MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
+  MetaLayout m{};
+  size_t off = 0;
+  m.slots = off;
+  off = align_up(off + size_t(num_seqs) * sizeof(int64_t));
+  m.pairs = off;
+  off = align_up(off + size_t(num_seqs) * 2 * sizeof(int64_t));
+  m.tables = off;
+  off = align_up(off + size_t(num_seqs) * size_t(max_blocks) * sizeof(int32_t));
+  m.lens = off;
+  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
+  m.order = off;
+  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
+  m.total = off;
+  return m;
+}
+
+int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
+
+}  // namespace
+
+extern "C" {
+
+size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq) {
+  if (num_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
+  return layout(num_seqs, max_blocks_per_seq).total;
+}
+
+pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
+                         float scale, int32_t max_blocks_per_seq, int32_t partition_size,
+                         void *k_cache, void *v_cache, const pk_cache_desc *desc,
+                         const pk_step_buffers *b, void *stream) {
+  if (!bm || !desc || !b || num_seqs <= 0 || !seq_ids || max_blocks_per_seq <= 0)
+    return PK_ERR_INVALID_ARG;
+  const int64_t esz = elem_size(desc->dtype);
+  if (esz == 0) return PK_ERR_UNSUPPORTED;
+  if (!b->q_host || !b->k_host || !b->v_host || !b->q_dev || !b->k_dev || !b->v_dev ||
+      !b->meta_host || !b->meta_dev || !b->out_dev || !b->out_host)
+    return PK_ERR_INVALID_ARG;
+  const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
+  if (b->meta_bytes < m.total) return PK_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *mh = static_cast<uint8_t *>(b->meta_host);
+  uint8_t *md = static_cast<uint8_t *>(b->meta_dev);
+  int64_t *slots = reinterpret_cast<int64_t *>(mh + m.slots);
+  int64_t *pairs = reinterpret_cast<int64_t *>(mh + m.pairs);
+  int32_t *tables = reinterpret_cast<int32_t *>(mh + m.tables);
+  int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
+  int32_t *order = reinterpret_cast<int32_t *>(mh + m.order);
+
+  // Host side of the step.
+  int32_t npairs = 0;
+  pk_status st = pk_bm_append_batch(bm, seq_ids, num_seqs, slots, pairs, &npairs);
+  if (st != PK_OK) return st;
+  st = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
+  if (st != PK_OK) return st;
+  st = pk_longest_first_order(lens, num_seqs, order);
+  if (st != PK_OK) return st;
+  const int32_t max_ctx = *std::max_element(lens, lens + num_seqs);
+
+  // Transfers: the step's tensors from the caller's host buffers, the
+  // metadata in one copy.
+  const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
+  const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
+  if (cudaMemcpyAsync(b->q_dev, b->q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(b->k_dev, b->k_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(b->v_dev, b->v_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(md, mh, m.total, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PK_ERR_CUDA;
+
+  // Device side of the step.
+  if (npairs > 0) {
+    st = pk_copy_blocks(k_cache, v_cache, reinterpret_cast<const int64_t *>(md + m.pairs), npairs,
+                        desc, stream);
+    if (st != PK_OK) return st;
+  }
+  st = pk_reshape_and_cache(b->k_dev, b->v_dev, reinterpret_cast<const int64_t *>(md + m.slots),
+                            num_seqs, k_cache, v_cache, desc, stream);
+  if (st != PK_OK) return st;
+  st = pk_paged_attention_decode_impl(
+      b->out_dev, b->q_dev, k_cache, v_cache, reinterpret_cast<const int32_t *>(md + m.tables),
+      reinterpret_cast<const int32_t *>(md + m.lens), scale, num_seqs, num_q_heads,
+      max_blocks_per_seq, max_ctx, partition_size, b->workspace, b->workspace_bytes, desc,
+      reinterpret_cast<const int32_t *>(md + m.order), PK_ATTN_AUTO, stream);
+  if (st != PK_OK) return st;
+  if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PK_ERR_CUDA;
+  return PK_OK;
+}
+
+}  // extern "C"
