@@ -64,6 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="launch the timed steps eagerly, not as CUDA graphs")
     p.add_argument("--no-order", action="store_true", help="launch sequences in index order, not longest first")
+    p.add_argument("--cascade", action="store_true",
+                   help="cascade attention: each shared prefix read once per group (prefix workload)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -348,6 +350,8 @@ def run_ours(args):
     simt = args.attn_impl == "simt" or wl.dtype == "f32"
 
     def launches(si):
+        if groups is not None and groups["num_groups"]:
+            return (1 if len(si.pairs) else 0) + 3  # scatter, prefix kernel, suffix kernel
         part = st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
         return (1 if len(si.pairs) else 0) + 2 + (1 if split and simt else 0)
@@ -357,8 +361,15 @@ def run_ours(args):
             pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
         pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
 
+    groups = st.cascade_groups() if args.cascade else None
+    if groups is not None:
+        ws = st.alloc_cascade_workspace(max_ctx, groups, args.partition)
+
     def attend(d):
-        st.attention(d, out, ws, args.partition, args.attn_impl, ordered=not args.no_order)
+        if groups is not None:
+            st.attention_cascade(d, out, groups, ws, args.partition, ordered=not args.no_order)
+        else:
+            st.attention(d, out, ws, args.partition, args.attn_impl, ordered=not args.no_order)
 
     # warm-up (eager; also performs the library's one-time set-up)
     for i in range(args.warmup):
@@ -452,6 +463,8 @@ def run_ours(args):
         cpu = cpu_baseline(wl, ref, args.cpu_seconds)
 
     part = st.resolve_partition(max(si.max_context_len for si in host_steps), args.partition)
+    if groups is not None:
+        part = args.partition if args.partition >= 0 else "auto (cascade)"
     mean_ms = 1e3 * t_step / args.steps
     if rank == 0:
         line = {
@@ -466,8 +479,12 @@ def run_ours(args):
                 "kv_bytes_per_step_mean": total_bytes / args.steps,
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
                 "launch": "CUDA graphs per step" if graphs else "eager",
-                "seq_order": "index" if args.no_order else "longest first (host)"}),
-            "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel",
+                "seq_order": "index" if args.no_order else "longest first (host)",
+                "attention": (f"cascade: {groups['num_groups']} shared-prefix groups, prefix read once per group"
+                              if groups is not None else "per sequence")}),
+            "roofline": {"bound": "hbm",
+                         "kernel": ("attn_prefix_kernel + attn_mma_kernel" if groups is not None else
+                                    "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel"),
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "traffic": ncu_traffic(wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"),
@@ -522,7 +539,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
     return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(stepper.h2d_bytes),
             "d2h_bytes_per_step": int(stepper.d2h_bytes), "steps": E, "ms_per_step": 1e3 * tot_t / E,
             "includes": "pk_decode_step: host block-manager append, table export, launch order, "
-                        "H2D (q, k, v, one metadata buffer), kernels, D2H of the output; stream sync",
+                        "H2D (q, k, v, one metadata buffer), kernels (per-sequence attention), "
+                        "D2H of the output; stream sync",
             "_seconds": tot_t, "_bytes": tot_b}
 
 

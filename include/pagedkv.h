@@ -191,6 +191,47 @@ pk_status pk_paged_attention_decode_static(void *out, const void *q, const void 
                                            int32_t partition_size, const pk_cache_desc *desc,
                                            void *stream);
 
+/* Cascade (shared-prefix) decode attention ("PagedAttention" S06, "In
+ * production": the shared prefix batched separately from the divergent
+ * suffixes; "Copy-on-write, for free": forked samples share the prefix
+ * blocks). Same result as pk_paged_attention_decode, but for each group of
+ * sequences that share their first prefix tokens (pk_bm_prefix_groups) the
+ * prefix K/V is read once per KV head and scored against every member's
+ * queries; each member's remaining tokens are attended on their own, and
+ * the parts are merged by log-sum-exp.
+ *   group_offsets    device int32 [num_groups + 1] into group_members;
+ *   group_members    device int32, batch positions of the members (the first
+ *                    member's table supplies the prefix blocks);
+ *   group_prefix_len device int32 [num_groups], shared tokens (multiple of B);
+ *   seq_prefix_len   device int32 [S], shared tokens of each batch position
+ *                    (0 outside groups);
+ *   max_group_size   members per group; G * max_group_size <= 16;
+ *   max_prefix_len   host bound on group_prefix_len;
+ *   partition_size   0: one partition for the prefix and one for the rest;
+ *                    > 0: partitions of this many tokens (a multiple of B);
+ *                    -1: automatic (one partition when num_groups x Hk covers
+ *                    the SMs, else prefix partitions that do, >= 512 tokens);
+ *   seq_order        optional launch order of the suffix work (see _impl);
+ *   workspace        pk_cascade_workspace_size(...) bytes (required).
+ * bf16 only (PK_ERR_UNSUPPORTED otherwise). With num_groups == 0 this is
+ * pk_paged_attention_decode_impl with the automatic kernel. */
+pk_status pk_cascade_attention_decode(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, float scale, int32_t num_seqs,
+    int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_context_len,
+    int32_t partition_size, const int32_t *group_offsets, const int32_t *group_members,
+    const int32_t *group_prefix_len, const int32_t *seq_prefix_len, int32_t num_groups,
+    int32_t max_group_size, int32_t max_prefix_len, const int32_t *seq_order, void *workspace,
+    size_t workspace_bytes, const pk_cache_desc *desc, void *stream);
+
+/* Workspace bytes of pk_cascade_attention_decode: fp32 partials
+ * [S, Hq, Ppre + Psuf, d + 2] (Ppre = ceil(max_prefix_len / partition),
+ * Psuf = ceil(max_context_len / partition)) and one 8-byte merge ticket per
+ * (sequence, KV head); 0 on invalid arguments. Host only. */
+size_t pk_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                 int32_t num_groups, int32_t max_prefix_len,
+                                 int32_t partition_size, const pk_cache_desc *desc);
+
 /* The partition size (in tokens) that a partition_size argument resolves to
  * for this shape: 0 means no split. Host only, no GPU needed. */
 int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_heads,
@@ -275,6 +316,26 @@ int32_t pk_bm_refcount(const pk_bm *bm, int32_t block); /* -1 if out of range */
  * match, no named block is free, no block is lost or listed twice, and each
  * table holds ceil(len / B) blocks. PK_ERR_INVARIANT on the first violation. */
 pk_status pk_bm_check_invariants(const pk_bm *bm);
+
+/* Shared-prefix groups for cascade attention. Sequences of seq_ids[0..n-1]
+ * whose tables begin with the same physical block (forks of one parent) are
+ * grouped in batch order, in chunks of at most max_group_size; a chunk of two
+ * or more becomes a group when its members' tables agree on at least
+ * min_prefix_blocks leading blocks that every member has filled. Outputs (host
+ * arrays, capacity n each, n + 1 for group_offsets):
+ *   group_offsets[g] .. group_offsets[g+1]-1 index group_members, which holds
+ *     batch positions (indices into seq_ids); the first member's table
+ *     supplies the group's prefix blocks;
+ *   group_prefix_len[g]: shared tokens (a multiple of B);
+ *   seq_prefix_len[i]: shared tokens of batch position i (0 outside groups);
+ *   *num_groups_out: number of groups.
+ * ("paged attention deep", "Copy-on-write for shared prefixes": forked
+ * sequences name the same prefix blocks.) */
+pk_status pk_bm_prefix_groups(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
+                              int32_t max_group_size, int32_t min_prefix_blocks,
+                              int32_t *group_offsets, int32_t *group_members,
+                              int32_t *group_prefix_len, int32_t *seq_prefix_len,
+                              int32_t *num_groups_out);
 
 /* live_tokens: sum of sequence lengths; reserved_slots: B * (blocks in use);
  * tail_waste: sum over sequences of B*ceil(len/B) - len; shared_blocks:

@@ -51,6 +51,7 @@ EXPORTED = (
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
     "pk_decode_step_meta_bytes", "pk_decode_step",
+    "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
 )
 
 
@@ -115,6 +116,10 @@ def lib() -> ctypes.CDLL:
         "pk_bm_check_invariants": (i32, [P]),
         "pk_bm_stats": (i32, [P, P, P, P, P, P]),
         "pk_decode_step_meta_bytes": (sz, [i32, i32]),
+        "pk_bm_prefix_groups": (i32, [P, P, i32, i32, i32, P, P, P, P, P]),
+        "pk_cascade_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, P, P, P,
+                                              i32, i32, i32, P, P, sz, D, P]),
+        "pk_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, D]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
     }
     for name, (res, args) in sigs.items():
@@ -280,6 +285,41 @@ def pk_paged_attention_decode_static(out, q, k_cache, v_cache, block_tables, con
         ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_static")
 
 
+def pk_cascade_workspace_size(num_seqs, num_q_heads, max_context_len, num_groups, max_prefix_len,
+                              partition_size, desc) -> int:
+    return int(lib().pk_cascade_workspace_size(int(num_seqs), int(num_q_heads), int(max_context_len),
+                                               int(num_groups), int(max_prefix_len), int(partition_size),
+                                               ctypes.byref(desc)))
+
+
+def pk_cascade_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                max_context_len: int, groups: dict, partition_size: int = -1, workspace=None,
+                                seq_order=None, stream=None):
+    """Cascade (shared-prefix) decode attention; same result as
+    :func:`pk_paged_attention_decode`. ``groups`` holds CUDA int32 tensors
+    ``offsets``, ``members``, ``prefix_len``, ``seq_prefix_len`` and the ints
+    ``num_groups``, ``max_group_size``, ``max_prefix_len`` (see
+    :meth:`BlockManager.prefix_groups`)."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    S, Hq, d = (int(x) for x in q.shape)
+    if out.shape != q.shape or out.dtype != q.dtype or q.dtype != k_cache.dtype:
+        raise ValueError("out and q must be [num_seqs, num_q_heads, head_dim] of the cache dtype")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    i32 = torch.int32
+    _check(lib().pk_cascade_attention_decode(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", i32), _dev(context_lens, "context_lens", i32), float(scale), S, Hq,
+        int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+        _dev(groups["offsets"], "offsets", i32), _dev(groups["members"], "members", i32),
+        _dev(groups["prefix_len"], "prefix_len", i32), _dev(groups["seq_prefix_len"], "seq_prefix_len", i32),
+        int(groups["num_groups"]), int(groups["max_group_size"]), int(groups["max_prefix_len"]),
+        None if seq_order is None else _dev(seq_order, "seq_order", i32), ws_ptr, ws_bytes, ctypes.byref(desc),
+        _stream(stream)), "pk_cascade_attention_decode")
+
+
 def pk_get_device_error(stream=None) -> Tuple[int, int]:
     """Synchronises the stream, reads and clears the device error word.
 
@@ -372,6 +412,24 @@ class BlockManager:
         _check(self._L.pk_bm_export_tables(self._h, _np_ptr(ids), n, int(max_blocks), _np_ptr(tables),
                                            _np_ptr(lens)), "pk_bm_export_tables")
         return tables, lens
+
+    def prefix_groups(self, seqs: Sequence[int], max_group_size: int, min_prefix_blocks: int = 1) -> dict:
+        """Shared-prefix groups of the batch ``seqs`` (host numpy arrays)."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int64)
+        n = len(ids)
+        offsets = np.zeros(n + 1, np.int32)
+        members = np.zeros(max(n, 1), np.int32)
+        prefix = np.zeros(max(n, 1), np.int32)
+        seq_prefix = np.zeros(max(n, 1), np.int32)
+        ng = ctypes.c_int32(0)
+        _check(self._L.pk_bm_prefix_groups(self._h, _np_ptr(ids), n, int(max_group_size), int(min_prefix_blocks),
+                                           _np_ptr(offsets), _np_ptr(members), _np_ptr(prefix), _np_ptr(seq_prefix),
+                                           ctypes.byref(ng)), "pk_bm_prefix_groups")
+        g = ng.value
+        return {"num_groups": g, "offsets": offsets[: g + 1].copy(), "members": members[: offsets[g]].copy(),
+                "prefix_len": prefix[:g].copy(), "seq_prefix_len": seq_prefix[:n].copy(),
+                "max_group_size": int(max_group_size),
+                "max_prefix_len": int(prefix[:g].max()) if g else 0}
 
     def num_free(self) -> int:
         return int(self._L.pk_bm_num_free(self._h))

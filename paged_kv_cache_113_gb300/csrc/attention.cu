@@ -57,6 +57,14 @@ struct AttnParams {
   const int32_t *order;      // [S] launch order of the sequences, or null
   unsigned long long *merge_tickets;  // [S, Hk] arrival tickets of the fused merge, or null
   uint32_t epoch;            // this call's tag on the tickets
+  // Cascade (shared-prefix) attention: the first seq_prefix[s] tokens of
+  // sequence s are attended by its group's prefix work; partials of prefix
+  // partitions use workspace slots [0, prefix_slots), the rest follow.
+  const int32_t *seq_prefix;     // [S] or null
+  const int32_t *group_offsets;  // [num_groups + 1]
+  const int32_t *group_members;  // batch positions of the groups' members
+  const int32_t *group_prefix;   // [num_groups] shared tokens per group
+  int32_t prefix_slots;
   float scale_log2;          // scale * log2(e)
   int32_t num_seqs, num_q_heads, num_kv_heads, group;
   int32_t block_size, max_blocks, num_blocks;
@@ -106,14 +114,16 @@ __device__ __forceinline__ int take_merge_ticket(unsigned long long *t, uint32_t
   }
 }
 
-// Log-sum-exp merge of the np partials of query heads h0 .. h0+nh-1 of
-// sequence s, spread over `nthreads` threads (thread `tid`), four elements
-// per step. M = max_p m_p, L = sum_p l_p 2^(m_p - M),
-// out = sum_p acc_p 2^(m_p - M) / L. Partials are read from L2 (written by
-// other CTAs of the same launch).
+// Log-sum-exp merge of the partials of query heads h0 .. h0+nh-1 of
+// sequence s held in workspace slots [0, na) and [b0, b0 + nb), spread over
+// `nthreads` threads (thread `tid`), four elements per step.
+// M = max_p m_p, L = sum_p l_p 2^(m_p - M), out = sum_p acc_p 2^(m_p - M) / L.
+// Partials are read from L2 (written by other CTAs of the same call).
 template <typename T, int D>
-__device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h0, int nh, int np,
-                                               int tid, int nthreads) {
+__device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h0, int nh, int na,
+                                               int b0, int nb, int tid, int nthreads) {
+  const int np = na + nb;
+  auto slot = [&](int q) { return q < na ? q : b0 + (q - na); };
   for (int idx = tid; idx < nh * (D / 4); idx += nthreads) {
     const int h = h0 + idx / (D / 4), i = (idx % (D / 4)) * 4;
     const size_t row = size_t(s) * p.num_q_heads + h;
@@ -121,7 +131,7 @@ __device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h
     const float *lrow = p.ws_l + row * p.num_partitions;
     const float *arow = p.ws_acc + row * p.num_partitions * D + i;
     float M = -INFINITY;
-    for (int q = 0; q < np; ++q) M = fmaxf(M, __ldcg(mrow + q));
+    for (int q = 0; q < np; ++q) M = fmaxf(M, __ldcg(mrow + slot(q)));
     float L = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int q = 0;
@@ -130,9 +140,10 @@ __device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h
       float f[4], l[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        x[u] = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(q + u) * D));
-        f[u] = __ldcg(mrow + q + u);
-        l[u] = __ldcg(lrow + q + u);
+        const int sl = slot(q + u);
+        x[u] = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(sl) * D));
+        f[u] = __ldcg(mrow + sl);
+        l[u] = __ldcg(lrow + sl);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -145,9 +156,10 @@ __device__ __forceinline__ void merge_partials(const AttnParams &p, int s, int h
       }
     }
     for (; q < np; ++q) {
-      const float4 x = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(q) * D));
-      const float w = exp2f(__ldcg(mrow + q) - M);
-      L = fmaf(__ldcg(lrow + q), w, L);
+      const int sl = slot(q);
+      const float4 x = __ldcg(reinterpret_cast<const float4 *>(arow + size_t(sl) * D));
+      const float w = exp2f(__ldcg(mrow + sl) - M);
+      L = fmaf(__ldcg(lrow + sl), w, L);
       acc.x = fmaf(x.x, w, acc.x);
       acc.y = fmaf(x.y, w, acc.y);
       acc.z = fmaf(x.z, w, acc.z);
@@ -172,7 +184,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
   constexpr int EPL = D / 32;  // elements per lane
   // Partitions launch last-first: the higher ones exist only for the longest
   // sequences, so the heaviest work starts early and short work fills the end.
-  const int kvh = blockIdx.x, part = p.num_partitions - 1 - int(blockIdx.z);
+  const int kvh = blockIdx.x, part = int(gridDim.z) - 1 - int(blockIdx.z);
   // Sequences launch in the caller's order when one is given (longest first
   // keeps the longest work from trailing the launch).
   const int s = launch_seq(p);
@@ -322,24 +334,29 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   // Partitions launch last-first: the higher ones exist only for the longest
   // sequences, so the heaviest work starts early and short work fills the end.
-  const int kvh = blockIdx.x, part = p.num_partitions - 1 - int(blockIdx.z);
+  const int kvh = blockIdx.x, part = int(gridDim.z) - 1 - int(blockIdx.z);
   // Sequences launch in the caller's order when one is given (longest first
   // keeps the longest work from trailing the launch).
   const int s = launch_seq(p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
-  if (ctx == 0) {
-    if (p.num_partitions == 1 && part == 0)
+  if (ctx == 0) {  // invalid length (recorded): a zero row, nothing to merge
+    if (blockIdx.z == 0)
       for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
         static_cast<__nv_bfloat16 *>(p.out)[(size_t(s) * p.num_q_heads + kvh * G + idx / D) * D +
                                             idx % D] = __float2bfloat16_rn(0.0f);
     return;
   }
-  const int start = part * p.partition;
+  // Tokens [0, pre) belong to the sequence's shared prefix (cascade mode);
+  // this CTA covers partition `part` of the rest.
+  const int pre = p.seq_prefix ? min(max(__ldg(p.seq_prefix + s), 0), ctx) : 0;
+  const int start = pre + part * p.partition;
   if (start >= ctx) return;
   const int end = min(ctx, start + p.partition);
   const int nst = (end - start + S::TPS - 1) / S::TPS;
+  const int npre = (pre + p.partition - 1) / p.partition;
+  const int nsuf = (ctx - pre + p.partition - 1) / p.partition;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -568,13 +585,13 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       O1 = fmaf(row[1], f, O1);
     }
     const int h = kvh * G + g;
-    if (ctx <= p.partition) {  // a single partition: final output, no merge
+    if (npre + nsuf == 1) {  // a single part: final output, no merge
       const float inv = 1.0f / L;
       *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                           (size_t(s) * p.num_q_heads + h) * D + i) =
           __floats2bfloat162_rn(O0 * inv, O1 * inv);
     } else {
-      const size_t r = (size_t(s) * p.num_q_heads + h) * p.num_partitions + part;
+      const size_t r = (size_t(s) * p.num_q_heads + h) * p.num_partitions + p.prefix_slots + part;
       *reinterpret_cast<float2 *>(p.ws_acc + r * D + i) = make_float2(O0, O1);
       if (i == 0) {
         p.ws_m[r] = M;
@@ -582,21 +599,337 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       }
     }
   }
-  if (ctx > p.partition && p.merge_tickets) {
-    // Fused merge: the last partition to finish for (s, kvh) merges them all.
+  if (npre + nsuf > 1 && p.merge_tickets) {
+    // Fused merge: the last part to finish for (s, kvh) merges them all.
     __threadfence();  // this thread's partials are visible device-wide
     pk::named_barrier(1, NW * 32);
-    const int np = (ctx + p.partition - 1) / p.partition;
     volatile int *flag = reinterpret_cast<volatile int *>(sm_l + NW * kMaxGroup);
     if (threadIdx.x == 0)
-      *flag = take_merge_ticket(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, p.epoch) == np;
+      *flag = take_merge_ticket(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, p.epoch) ==
+              npre + nsuf;
     pk::named_barrier(1, NW * 32);
     if (*flag) {
       __threadfence();
-      merge_partials<__nv_bfloat16, D>(p, s, kvh * G, G, np, threadIdx.x, NW * 32);
+      merge_partials<__nv_bfloat16, D>(p, s, kvh * G, G, npre, p.prefix_slots, nsuf, threadIdx.x,
+                                       NW * 32);
       pk::named_barrier(1, NW * 32);
       if (threadIdx.x == 0) atomicExch(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, 0ull);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Cascade attention, shared-prefix part (bf16, tensor cores).
+//
+// One CTA per (KV head, group, partition of the group's shared prefix): the
+// prefix blocks are streamed once (from the first member's table -- every
+// member names the same blocks) and scored against the queries of every
+// member of the group: up to 16 query columns (members x G heads), two MMA
+// n-tiles. Each column's partial goes to its sequence's prefix slot; the
+// members' suffix work (attn_mma_kernel in cascade mode) fills the other
+// slots, and the last part to finish merges ("PagedAttention" S06, "In
+// production": the shared prefix batched separately from the divergent
+// suffixes).
+// ---------------------------------------------------------------------------
+template <int D, int BS, int NW, int STAGES>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    attn_prefix_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap vmap) {
+  using S = MmaShape<D, BS, NW, STAGES>;
+  constexpr int NT = 2;            // n-tiles of 8 query columns
+  constexpr int NC = 8 * NT;       // query columns per CTA
+  constexpr int MSTRIDE = S::OUT_STRIDE;
+  static_assert(NW * NC * (MSTRIDE + 2) * 4 + 64 <= STAGES * S::STAGE_BYTES,
+                "merge buffer must fit the stage ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = pk::smem_addr(smem_raw);
+  const uint32_t bars = (raw + 7u) & ~7u;
+  const uint32_t stages = (bars + S::BAR_BYTES + 1023u) & ~1023u;
+  auto full_bar = [&](int i) { return bars + 8u * i; };
+  auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
+
+  const int kvh = blockIdx.x, grp = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int g0 = __ldg(p.group_offsets + grp);
+  const int nm = __ldg(p.group_offsets + grp + 1) - g0;
+  const int lead = __ldg(p.group_members + g0);
+  const int pre = __ldg(p.group_prefix + grp);
+  const int npre_g = (pre + p.partition - 1) / p.partition;
+  const int part = int(blockIdx.z);
+  if (part >= npre_g || nm <= 0 || nm * G > NC) return;
+  const int start = part * p.partition;
+  const int end = min(pre, start + p.partition);
+  if (start >= end) return;
+  const int nst = (end - start + S::TPS - 1) / S::TPS;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      pk::mbar_init(full_bar(i), 1);
+      pk::mbar_init(empty_bar(i), NW);
+    }
+    pk::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ---------------- producer warp (as in attn_mma_kernel) ----------------
+    if (lane == 0) {
+      pk::prefetch_tensormap(&kmap);
+      pk::prefetch_tensormap(&vmap);
+    }
+    const int32_t *trow = p.tables + size_t(lead) * p.max_blocks + start / BS;
+    const int nb = (end - start + BS - 1) / BS;
+    int cur = lane < nb ? __ldg(trow + lane) : 0;
+    int nxt = 32 + lane < nb ? __ldg(trow + 32 + lane) : 0;
+    int chunk = 0;
+    int issued = 0;
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % STAGES;
+      const int b0 = st * S::BPS;
+      if (b0 >= 32 * (chunk + 1)) {
+        ++chunk;
+        cur = nxt;
+        const int j = 32 * (chunk + 1) + lane;
+        nxt = j < nb ? __ldg(trow + j) : 0;
+      }
+      const int mine = __shfl_sync(0xffffffffu, cur, (b0 & 31) + min(lane, S::BPS - 1));
+      if (st >= STAGES && !pk::mbar_wait(empty_bar(slot), ((st / STAGES) - 1) & 1)) {
+        if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, lead);
+        break;
+      }
+      const int tok0 = start + st * S::TPS;
+      const int nblk = min(S::BPS, (end - tok0 + BS - 1) / BS);
+      if (lane == 0)
+        pk::mbar_arrive_expect_tx(full_bar(slot), uint32_t(nblk * S::HALVES * 2 * BS * 128));
+      __syncwarp();
+      if (lane < nblk) {
+        int phys = mine;
+        if (phys < 0 || phys >= p.num_blocks) {
+          pk::record_error(&g_attn_error, PK_DEVERR_BLOCK_ID, lead);
+          phys = 0;
+        }
+        const uint32_t kdst = stages + slot * S::STAGE_BYTES + lane * BS * 128;
+#pragma unroll
+        for (int h = 0; h < S::HALVES; ++h) {
+          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, &kmap, full_bar(slot), h * 64, kvh, phys * BS);
+          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, &vmap, full_bar(slot), h * 64,
+                          kvh, phys * BS);
+        }
+      }
+      issued = st + 1;
+    }
+    if (lane == 0)
+      for (int st = max(0, issued - STAGES); st < issued; ++st)
+        pk::mbar_wait(full_bar(st % STAGES), (st / STAGES) & 1);
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int qd = lane & 3, rw = lane >> 2;
+  const int mi = lane >> 3, r8 = lane & 7;
+  const int ncol = nm * G;
+  // Q^T of the group's columns: column c = member c / G, head c % G.
+  uint32_t qb[NT][S::KSTEPS][2];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int c = t * 8 + rw;
+    const int cc = min(c, ncol - 1);
+    const int mem = __ldg(p.group_members + g0 + cc / G);
+    const __nv_bfloat16 *qrow = static_cast<const __nv_bfloat16 *>(p.q) +
+                                (size_t(mem) * p.num_q_heads + kvh * G + cc % G) * D;
+#pragma unroll
+    for (int ks = 0; ks < S::KSTEPS; ++ks) {
+      const uint32_t a = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * qd);
+      const uint32_t b = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * qd);
+      qb[t][ks][0] = c < ncol ? a : 0u;
+      qb[t][ks][1] = c < ncol ? b : 0u;
+    }
+  }
+  float o[S::KSTEPS][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < S::KSTEPS; ++mt)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) o[mt][t][0] = o[mt][t][1] = o[mt][t][2] = o[mt][t][3] = 0.0f;
+  float m[NT][2], l[NT][2];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) m[t][0] = m[t][1] = -INFINITY, l[t][0] = l[t][1] = 0.0f;
+  const float sl = p.scale_log2;
+  const int row0 = warp * 16;
+
+  for (int st = 0; st < nst; ++st) {
+    const int slot = st % STAGES;
+    if (!pk::mbar_wait(full_bar(slot), (st / STAGES) & 1)) {
+      if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, lead);
+      break;
+    }
+    const uint32_t kbase = stages + slot * S::STAGE_BYTES;
+    const uint32_t vbase = kbase + S::KV_BYTES;
+    const int nvalid = end - (start + st * S::TPS + row0);
+    if (nvalid > 0) {
+      if (nvalid < 16) {
+        const int nz = (16 - nvalid) * S::HALVES * 8;
+        for (int idx = lane; idx < nz; idx += 32) {
+          const int r = row0 + nvalid + idx / (S::HALVES * 8);
+          const int c = idx % (S::HALVES * 8);
+          const uint32_t a = vbase + (c >> 3) * S::SLAB_BYTES + r * 128 + (c & 7) * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+        }
+        __syncwarp();
+      }
+      // S^T for both n-tiles from one pass over the K tile.
+      float sacc[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < S::KSTEPS; ++ks) {
+        const int r = row0 + (mi & 1) * 8 + r8;
+        const int chunk = ks * 2 + (mi >> 1);
+        const uint32_t a = kbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
+                           (((chunk & 7) ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        pk::ldmatrix_x4(a, a0, a1, a2, a3);
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          pk::mma_bf16_16816(sacc[t], a0, a1, a2, a3, qb[t][ks][0], qb[t][ks][1]);
+      }
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float x0 = sacc[t][0] * sl, x1 = sacc[t][1] * sl, x2 = sacc[t][2] * sl, x3 = sacc[t][3] * sl;
+        if (rw >= nvalid) x0 = x1 = -INFINITY;
+        if (rw + 8 >= nvalid) x2 = x3 = -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[t][0], mx0), mn1 = fmaxf(m[t][1], mx1);
+        const float c0 = exp2f(m[t][0] - mn0), c1 = exp2f(m[t][1] - mn1);
+        const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+        const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+        const uint32_t w01 = pk::pack_bf16x2(p0, p1);
+        const uint32_t w23 = pk::pack_bf16x2(p2, p3);
+        const uint32_t r01 = pk::pack_bf16x2(p0 - pk::bf16_lo(w01), p1 - pk::bf16_hi(w01));
+        const uint32_t r23 = pk::pack_bf16x2(p2 - pk::bf16_lo(w23), p3 - pk::bf16_hi(w23));
+        l[t][0] = fmaf(l[t][0], c0, p0 + p2);
+        l[t][1] = fmaf(l[t][1], c1, p1 + p3);
+        m[t][0] = mn0;
+        m[t][1] = mn1;
+#pragma unroll
+        for (int mt = 0; mt < S::KSTEPS; ++mt) {
+          o[mt][t][0] *= c0;
+          o[mt][t][1] *= c1;
+          o[mt][t][2] *= c0;
+          o[mt][t][3] *= c1;
+        }
+        bh[t][0] = pk::movmatrix_trans(w01);
+        bh[t][1] = pk::movmatrix_trans(w23);
+        bl[t][0] = pk::movmatrix_trans(r01);
+        bl[t][1] = pk::movmatrix_trans(r23);
+      }
+#pragma unroll
+      for (int mt = 0; mt < S::KSTEPS; ++mt) {
+        const int r = row0 + (mi >> 1) * 8 + r8;
+        const int chunk = mt * 2 + (mi & 1);
+        const uint32_t a = vbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
+                           (((chunk & 7) ^ (r & 7)) << 4);
+        uint32_t a0, a1, a2, a3;
+        pk::ldmatrix_x4_trans(a, a0, a1, a2, a3);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          pk::mma_bf16_16816(o[mt][t], a0, a1, a2, a3, bh[t][0], bh[t][1]);
+          pk::mma_bf16_16816(o[mt][t], a0, a1, a2, a3, bl[t][0], bl[t][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) pk::mbar_arrive(empty_bar(slot));
+  }
+
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
+      l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
+    }
+
+  // Merge the consumer warps' states per column (the stage ring is free).
+  pk::named_barrier(1, NW * 32);
+  float *sm_o = reinterpret_cast<float *>(smem_raw + (stages - raw));
+  float *sm_m = sm_o + NW * NC * MSTRIDE;
+  float *sm_l = sm_m + NW * NC;
+  int *sm_last = reinterpret_cast<int *>(sm_l + NW * NC);
+#pragma unroll
+  for (int mt = 0; mt < S::KSTEPS; ++mt)
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float *base = sm_o + (warp * NC + t * 8 + 2 * qd) * MSTRIDE + mt * 16 + rw;
+      base[0] = o[mt][t][0];
+      base[MSTRIDE] = o[mt][t][1];
+      base[8] = o[mt][t][2];
+      base[MSTRIDE + 8] = o[mt][t][3];
+    }
+  if (rw == 0) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      sm_m[warp * NC + t * 8 + 2 * qd] = m[t][0];
+      sm_m[warp * NC + t * 8 + 2 * qd + 1] = m[t][1];
+      sm_l[warp * NC + t * 8 + 2 * qd] = l[t][0];
+      sm_l[warp * NC + t * 8 + 2 * qd + 1] = l[t][1];
+    }
+  }
+  pk::named_barrier(1, NW * 32);
+  for (int idx = threadIdx.x; idx < ncol * (D / 2); idx += NW * 32) {
+    const int c = idx / (D / 2), i = (idx % (D / 2)) * 2;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * NC + c]);
+    float L = 0.0f, O0 = 0.0f, O1 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = exp2f(sm_m[w * NC + c] - M);
+      const float *row = sm_o + (w * NC + c) * MSTRIDE + i;
+      L = fmaf(sm_l[w * NC + c], f, L);
+      O0 = fmaf(row[0], f, O0);
+      O1 = fmaf(row[1], f, O1);
+    }
+    const int mem = __ldg(p.group_members + g0 + c / G);
+    const size_t r = (size_t(mem) * p.num_q_heads + kvh * G + c % G) * p.num_partitions + part;
+    *reinterpret_cast<float2 *>(p.ws_acc + r * D + i) = make_float2(O0, O1);
+    if (i == 0) {
+      p.ws_m[r] = M;
+      p.ws_l[r] = L;
+    }
+  }
+  // Each member's part count: its prefix partitions plus its own suffix's.
+  __threadfence();
+  pk::named_barrier(1, NW * 32);
+  if (threadIdx.x < nm) {
+    const int mem = __ldg(p.group_members + g0 + threadIdx.x);
+    const int ctx = context_len(p, mem, false);
+    const int mpre = min(max(__ldg(p.seq_prefix + mem), 0), ctx);
+    const int nparts = (mpre + p.partition - 1) / p.partition +
+                       (ctx - mpre + p.partition - 1) / p.partition;
+    sm_last[threadIdx.x] =
+        take_merge_ticket(p.merge_tickets + size_t(mem) * p.num_kv_heads + kvh, p.epoch) == nparts;
+  }
+  pk::named_barrier(1, NW * 32);
+  for (int j = 0; j < nm; ++j) {
+    if (!sm_last[j]) continue;
+    __threadfence();
+    const int mem = __ldg(p.group_members + g0 + j);
+    const int ctx = context_len(p, mem, false);
+    const int mpre = min(max(__ldg(p.seq_prefix + mem), 0), ctx);
+    const int mnpre = (mpre + p.partition - 1) / p.partition;
+    const int mnsuf = (ctx - mpre + p.partition - 1) / p.partition;
+    merge_partials<__nv_bfloat16, D>(p, mem, kvh * G, G, mnpre, p.prefix_slots, mnsuf, threadIdx.x,
+                                     NW * 32);
+    pk::named_barrier(1, NW * 32);
+    if (threadIdx.x == 0) atomicExch(p.merge_tickets + size_t(mem) * p.num_kv_heads + kvh, 0ull);
   }
 }
 
@@ -617,7 +950,7 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
     return;
   }
   if (np == 1) return;  // written directly by the attention kernel
-  merge_partials<T, D>(p, s, h, 1, np, threadIdx.x, blockDim.x);
+  merge_partials<T, D>(p, s, h, 1, np, 0, 0, threadIdx.x, blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -683,7 +1016,34 @@ pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t s
                                     S::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return PK_ERR_CUDA;
-  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions);
+  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions - p.prefix_slots);
+  kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+// The prefix kernel holds 16 query columns (161 registers: 2 CTAs per SM),
+// so it affords a deeper ring than the suffix kernel.
+#ifndef PK_PREFIX_STAGES
+#define PK_PREFIX_STAGES 3
+#endif
+constexpr int kPrefixStages = PK_PREFIX_STAGES;
+
+template <int D, int BS>
+pk_status launch_prefix(const AttnParams &p, const pk_cache_desc &d, int num_groups,
+                        cudaStream_t stream) {
+  using S = MmaShape<D, BS, kMmaWarps, kPrefixStages>;
+  CUtensorMap kmap, vmap;
+  if (!encode_pool_map(&kmap, p.k_cache, d) || !encode_pool_map(&vmap, p.v_cache, d))
+    return PK_ERR_CUDA;
+  auto kern = attn_prefix_kernel<D, BS, kMmaWarps, kPrefixStages>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    S::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return PK_ERR_CUDA;
+  dim3 grid(p.num_kv_heads, num_groups, p.prefix_slots);
   kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
@@ -725,6 +1085,27 @@ size_t partial_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_
   if (P <= 1) return 0;
   const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
   return size_t(rows) * (size_t(head_dim) + 2) * sizeof(float);
+}
+
+// Partition of cascade attention. 0: one partition covering the longest
+// context; > 0: as given (a multiple of B); -1 (automatic): one partition
+// when the (group, KV head) prefix items already cover the SMs (on GB300 the
+// 32-group x 8-head prefix workload ran fastest unsplit), else prefix
+// partitions sized so the prefix items cover the SMs once, at least 512
+// tokens.
+int32_t cascade_partition(int32_t max_context_len, int32_t partition_size, int32_t B,
+                          int32_t num_groups, int32_t num_kv_heads, int32_t max_prefix_len) {
+  const int64_t whole = (int64_t(max_context_len) + B - 1) / B * B;
+  if (partition_size == 0) return int32_t(whole);
+  if (partition_size > 0) return partition_size % B == 0 ? partition_size : -1;
+  if (partition_size != -1) return -1;
+  const int64_t items = int64_t(num_groups) * num_kv_heads;
+  const int64_t sms = sm_count();
+  if (items >= sms || max_prefix_len <= 512) return int32_t(whole);
+  int64_t part = (int64_t(max_prefix_len) * items + sms - 1) / sms;
+  part = std::max<int64_t>(512, (part + 63) / 64 * 64);
+  part = (part + B - 1) / B * B;
+  return int32_t(std::min(part, whole));
 }
 
 // Fused-merge tickets, one 8-byte word per (sequence, KV head), after the
@@ -894,6 +1275,109 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   if (desc->dtype == PK_F32)
     return D == 128 ? launch_merge<float, 128>(p, s) : launch_merge<float, 64>(p, s);
   return D == 128 ? launch_merge<__nv_bfloat16, 128>(p, s) : launch_merge<__nv_bfloat16, 64>(p, s);
+}
+
+size_t pk_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
+                                 int32_t num_groups, int32_t max_prefix_len,
+                                 int32_t partition_size, const pk_cache_desc *desc) {
+  if (check_common(desc, num_seqs, num_q_heads, max_context_len) != PK_OK || max_prefix_len < 0 ||
+      num_groups < 0)
+    return 0;
+  const int32_t part = cascade_partition(max_context_len, partition_size, desc->block_size,
+                                         num_groups, desc->num_kv_heads, max_prefix_len);
+  if (part <= 0) return 0;
+  const int64_t P = (int64_t(max_prefix_len) + part - 1) / part +
+                    (int64_t(max_context_len) + part - 1) / part;
+  const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
+  return size_t(rows) * (size_t(desc->head_dim) + 2) * sizeof(float) +
+         size_t(num_seqs) * size_t(desc->num_kv_heads) * 8;
+}
+
+pk_status pk_cascade_attention_decode(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, float scale, int32_t num_seqs,
+    int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_context_len,
+    int32_t partition_size, const int32_t *group_offsets, const int32_t *group_members,
+    const int32_t *group_prefix_len, const int32_t *seq_prefix_len, int32_t num_groups,
+    int32_t max_group_size, int32_t max_prefix_len, const int32_t *seq_order, void *workspace,
+    size_t workspace_bytes, const pk_cache_desc *desc, void *stream) {
+  pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
+  if (st != PK_OK) return st;
+  if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PK_ERR_INVALID_ARG;
+  if (num_groups == 0)
+    return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
+                                          scale, num_seqs, num_q_heads, max_blocks_per_seq,
+                                          max_context_len, partition_size, workspace,
+                                          workspace_bytes, desc, seq_order, PK_ATTN_AUTO, stream);
+  const int32_t G = num_q_heads / desc->num_kv_heads;
+  if (!mma_supported(*desc, G)) return PK_ERR_UNSUPPORTED;
+  if (int64_t(max_group_size) * G > 16) return PK_ERR_UNSUPPORTED;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !group_offsets ||
+      !group_members || !group_prefix_len || !seq_prefix_len || max_blocks_per_seq <= 0)
+    return PK_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (workspace && !aligned16(workspace)))
+    return PK_ERR_INVALID_ARG;
+  const int32_t part = cascade_partition(max_context_len, partition_size, desc->block_size,
+                                         num_groups, desc->num_kv_heads, max_prefix_len);
+  if (part <= 0) return PK_ERR_INVALID_ARG;
+  const int64_t Ppre = (int64_t(max_prefix_len) + part - 1) / part;
+  const int64_t Psuf = (int64_t(max_context_len) + part - 1) / part;
+  if (num_seqs > 65535 || num_groups > 65535 || Ppre + Psuf > 65535) return PK_ERR_UNSUPPORTED;
+  const size_t need = pk_cascade_workspace_size(num_seqs, num_q_heads, max_context_len, num_groups,
+                                                max_prefix_len, partition_size, desc);
+  if (!workspace || workspace_bytes < need) return PK_ERR_WORKSPACE;
+  AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.tables = block_tables;
+  p.ctx_lens = context_lens;
+  p.scale_log2 = float(double(scale) * 1.4426950408889634);
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.group = G;
+  p.block_size = desc->block_size;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = desc->num_blocks;
+  p.partition = part;
+  p.num_partitions = int32_t(Ppre + Psuf);
+  p.prefix_slots = int32_t(Ppre);
+  const size_t rows = size_t(num_seqs) * num_q_heads * size_t(Ppre + Psuf);
+  p.ws_acc = static_cast<float *>(workspace);
+  p.ws_m = p.ws_acc + rows * desc->head_dim;
+  p.ws_l = p.ws_m + rows;
+  p.merge_tickets = reinterpret_cast<unsigned long long *>(p.ws_l + rows);
+  p.epoch = next_epoch();
+  p.order = seq_order;
+  p.seq_prefix = seq_prefix_len;
+  p.group_offsets = group_offsets;
+  p.group_members = group_members;
+  p.group_prefix = group_prefix_len;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = desc->head_dim, B = desc->block_size;
+  // The prefix grid first (its CTAs are the long ones), then the suffix grid;
+  // they meet only through the merge tickets.
+  if (Ppre > 0) {
+    if (D == 128)
+      st = B == 8 ? launch_prefix<128, 8>(p, *desc, num_groups, s)
+                  : (B == 16 ? launch_prefix<128, 16>(p, *desc, num_groups, s)
+                             : launch_prefix<128, 32>(p, *desc, num_groups, s));
+    else
+      st = B == 8 ? launch_prefix<64, 8>(p, *desc, num_groups, s)
+                  : (B == 16 ? launch_prefix<64, 16>(p, *desc, num_groups, s)
+                             : launch_prefix<64, 32>(p, *desc, num_groups, s));
+    if (st != PK_OK) return st;
+  }
+  if (D == 128)
+    st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
+                : (B == 16 ? launch_mma<128, 16>(p, *desc, s) : launch_mma<128, 32>(p, *desc, s));
+  else
+    st = B == 8 ? launch_mma<64, 8>(p, *desc, s)
+                : (B == 16 ? launch_mma<64, 16>(p, *desc, s) : launch_mma<64, 32>(p, *desc, s));
+  return st;
 }
 
 pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,

@@ -338,4 +338,67 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
   return PK_OK;
 }
 
+pk_status pk_bm_prefix_groups(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
+                              int32_t max_group_size, int32_t min_prefix_blocks,
+                              int32_t *group_offsets, int32_t *group_members,
+                              int32_t *group_prefix_len, int32_t *seq_prefix_len,
+                              int32_t *num_groups_out) {
+  if (!bm || n < 0 || max_group_size < 1 || min_prefix_blocks < 1 || !num_groups_out ||
+      (n > 0 && (!seq_ids || !group_offsets || !group_members || !group_prefix_len ||
+                 !seq_prefix_len)))
+    return PK_ERR_INVALID_ARG;
+  *num_groups_out = 0;
+  std::vector<const Sequence *> seq(n);
+  for (int32_t i = 0; i < n; ++i) {
+    auto it = bm->seqs.find(seq_ids[i]);
+    if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+    seq[i] = &it->second;
+    seq_prefix_len[i] = 0;
+  }
+  // Sequences whose tables start with the same physical block were forked
+  // from one parent; bucket them by that block, keeping batch order.
+  std::unordered_map<int32_t, std::vector<int32_t>> buckets;
+  std::vector<int32_t> first_seen;
+  for (int32_t i = 0; i < n; ++i) {
+    if (seq[i]->table.empty()) continue;
+    const int32_t b0 = seq[i]->table[0];
+    auto &v = buckets[b0];
+    if (v.empty()) first_seen.push_back(b0);
+    v.push_back(i);
+  }
+  const int64_t B = bm->block_size;
+  int32_t ng = 0, nm = 0;
+  group_offsets[0] = 0;
+  for (int32_t b0 : first_seen) {
+    const auto &members = buckets[b0];
+    for (size_t c0 = 0; c0 < members.size(); c0 += size_t(max_group_size)) {
+      const size_t c1 = std::min(members.size(), c0 + size_t(max_group_size));
+      if (c1 - c0 < 2) continue;
+      // Shared prefix: leading table entries equal across the chunk, limited
+      // to blocks every member has filled.
+      const Sequence &lead = *seq[members[c0]];
+      int64_t common = int64_t(lead.table.size());
+      int64_t min_len = lead.len;
+      for (size_t k = c0 + 1; k < c1; ++k) {
+        const Sequence &o = *seq[members[k]];
+        int64_t j = 0;
+        const int64_t lim = std::min<int64_t>(common, int64_t(o.table.size()));
+        while (j < lim && o.table[j] == lead.table[j]) ++j;
+        common = j;
+        min_len = std::min(min_len, o.len);
+      }
+      const int64_t blocks = std::min(common, min_len / B);
+      if (blocks < min_prefix_blocks) continue;
+      for (size_t k = c0; k < c1; ++k) {
+        group_members[nm++] = members[k];
+        seq_prefix_len[members[k]] = int32_t(blocks * B);
+      }
+      group_prefix_len[ng] = int32_t(blocks * B);
+      group_offsets[++ng] = nm;
+    }
+  }
+  *num_groups_out = ng;
+  return PK_OK;
+}
+
 }  // extern "C"

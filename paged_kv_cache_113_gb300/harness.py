@@ -18,9 +18,9 @@ from typing import List, Optional
 
 import numpy as np
 
-from . import (BlockManager, pk_copy_blocks, pk_longest_first_order, pk_paged_attention_decode,
-               pk_paged_attention_resolve_partition, pk_paged_attention_workspace_size,
-               pk_reshape_and_cache, cache_desc)
+from . import (BlockManager, pk_cascade_attention_decode, pk_cascade_workspace_size, pk_copy_blocks,
+               pk_longest_first_order, pk_paged_attention_decode, pk_paged_attention_resolve_partition,
+               pk_paged_attention_workspace_size, pk_reshape_and_cache, cache_desc)
 
 
 def to_device(a: np.ndarray, dtype: str, device):
@@ -168,3 +168,30 @@ class DecodeState:
         pk_paged_attention_decode(out, d["q"], self.k_cache, self.v_cache, d["tables"], d["ctx_lens"],
                                   self.wl.scale, d["max_context_len"], partition_size, workspace, impl,
                                   stream, seq_order=d.get("order") if ordered else None)
+
+    # -- cascade (shared-prefix) attention --------------------------------------
+    def cascade_groups(self, min_prefix_blocks: int = 1, max_group_size: Optional[int] = None) -> dict:
+        """The batch's shared-prefix groups as device tensors (host block manager)."""
+        import torch
+        wl = self.wl
+        mg = max(1, 16 // wl.group) if max_group_size is None else int(max_group_size)
+        g = self.bm.prefix_groups(range(wl.num_seqs), mg, min_prefix_blocks)
+        dev = self.device
+        out = dict(g)
+        for k in ("offsets", "members", "prefix_len", "seq_prefix_len"):
+            arr = g[k] if len(g[k]) else np.zeros(1, np.int32)
+            out[k] = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.int32)).to(dev)
+        return out
+
+    def alloc_cascade_workspace(self, max_context_len: int, groups: dict, partition_size: int = -1):
+        import torch
+        wl = self.wl
+        n = pk_cascade_workspace_size(wl.num_seqs, wl.num_q_heads, max_context_len, groups["num_groups"],
+                                      groups["max_prefix_len"], partition_size, self.desc)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+
+    def attention_cascade(self, d: dict, out, groups: dict, workspace, partition_size: int = -1, stream=None,
+                          ordered: bool = True):
+        pk_cascade_attention_decode(out, d["q"], self.k_cache, self.v_cache, d["tables"], d["ctx_lens"],
+                                    self.wl.scale, d["max_context_len"], groups, partition_size, workspace,
+                                    d.get("order") if ordered else None, stream)

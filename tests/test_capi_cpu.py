@@ -250,3 +250,51 @@ def test_longest_first_order(L):
         lens = rng.integers(1, 50, size=n).astype(np.int32)   # many ties
         got = pk.pk_longest_first_order(lens)
         assert got.tolist() == np.lexsort((np.arange(n), -lens)).tolist()
+
+
+def _brute_groups(ref_bm, n, B, max_group, min_blocks):
+    """Shared-prefix groups recomputed from the oracle's tables."""
+    tables = [ref_bm.table(s).tolist() for s in range(n)]
+    lens = [ref_bm.seq_len(s) for s in range(n)]
+    buckets, order = {}, []
+    for s in range(n):
+        if not tables[s]:
+            continue
+        b0 = tables[s][0]
+        if b0 not in buckets:
+            buckets[b0] = []
+            order.append(b0)
+        buckets[b0].append(s)
+    groups, seq_prefix = [], [0] * n
+    for b0 in order:
+        mem = buckets[b0]
+        for c in range(0, len(mem), max_group):
+            chunk = mem[c:c + max_group]
+            if len(chunk) < 2:
+                continue
+            common = min(len(tables[s]) for s in chunk)
+            for j in range(common):
+                if any(tables[s][j] != tables[chunk[0]][j] for s in chunk):
+                    common = j
+                    break
+            blocks = min(common, min(lens[s] for s in chunk) // B)
+            if blocks < min_blocks:
+                continue
+            groups.append((chunk, blocks * B))
+            for s in chunk:
+                seq_prefix[s] = blocks * B
+    return groups, seq_prefix
+
+
+@pytest.mark.parametrize("B,max_group,min_blocks", [(16, 4, 1), (32, 4, 1), (8, 3, 1), (16, 2, 1), (16, 4, 200)])
+def test_prefix_groups_match_brute_force(L, B, max_group, min_blocks):
+    wl = make_workload("prefix", block_size=B, num_seqs=24)
+    ours, ref = _replay_both(wl)
+    g = ours.prefix_groups(range(wl.num_seqs), max_group, min_blocks)
+    want, want_seq = _brute_groups(ref, wl.num_seqs, B, max_group, min_blocks)
+    got = [(g["members"][g["offsets"][i]:g["offsets"][i + 1]].tolist(), int(g["prefix_len"][i]))
+           for i in range(g["num_groups"])]
+    assert got == want
+    assert g["seq_prefix_len"].tolist() == want_seq
+    if min_blocks == 1:
+        assert g["num_groups"] > 0 and all(p >= (2000 // B - 1) * B for _, p in got)
