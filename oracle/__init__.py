@@ -79,6 +79,12 @@ def _load():
         "or_bm_num_free": (i32, [P]),
         "or_bm_cow_copies": (i64, [P]),
         "or_bm_free_list": (i32, [P, P, i32]),
+        "or_bm_set_swap_space": (i32, [P, i32, P]),
+        "or_bm_swap_out": (i32, [P, i64, P, P]),
+        "or_bm_swap_in": (i32, [P, i64, P, P]),
+        "or_bm_is_swapped": (i32, [P, i64]),
+        "or_bm_host_free": (i32, [P]),
+        "or_swap_copy": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32]),
         "or_reshape_and_cache": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32]),
         "or_copy_blocks": (i32, [P, P, P, i32, i32, i32, i32, i32, i32]),
         "or_paged_attention": (i32, [P, P, P, P, i32, P, i32, P, i32, i32, i32, i32, i32, i32, f64, P, i32]),
@@ -170,6 +176,33 @@ class BlockManager:
         self._lib.or_bm_free_list(self._h, _ptr(out), n)
         return out[:n]
 
+    def set_swap_space(self, num_host_blocks: int, host_order: Optional[np.ndarray] = None):
+        order = None if host_order is None else np.ascontiguousarray(host_order, dtype=np.int32)
+        self._keep_host = order
+        _check(self._lib.or_bm_set_swap_space(self._h, int(num_host_blocks), _ptr(order)), "set_swap_space")
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """(device block, host block) pairs, int64 [n, 2], in table order."""
+        n = len(self.table(seq))
+        pairs = np.zeros((max(n, 1), 2), np.int64)
+        cnt = ctypes.c_int(0)
+        _check(self._lib.or_bm_swap_out(self._h, int(seq), _ptr(pairs), ctypes.byref(cnt)), "swap_out")
+        return pairs[: cnt.value]
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """(host block, device block) pairs, int64 [n, 2], in table order."""
+        n = len(self.table(seq))
+        pairs = np.zeros((max(n, 1), 2), np.int64)
+        cnt = ctypes.c_int(0)
+        _check(self._lib.or_bm_swap_in(self._h, int(seq), _ptr(pairs), ctypes.byref(cnt)), "swap_in")
+        return pairs[: cnt.value]
+
+    def is_swapped(self, seq: int) -> bool:
+        return self._lib.or_bm_is_swapped(self._h, int(seq)) == 1
+
+    def host_free(self) -> int:
+        return int(self._lib.or_bm_host_free(self._h))
+
     def export_tables(self, seqs: Sequence[int], max_blocks: int) -> np.ndarray:
         """Padded ``int32 [len(seqs), max_blocks]`` tables, pad value -1."""
         out = np.full((len(seqs), max_blocks), -1, dtype=np.int32)
@@ -201,6 +234,16 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs: np.ndarray):
     N, B, Hk, d = k_cache.shape
     _check(lib.or_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), int(len(pairs)), int(N), int(B),
                               int(Hk), int(d), int(k_cache.itemsize)), "copy_blocks")
+
+
+def swap_copy(to_k: np.ndarray, to_v: np.ndarray, from_k: np.ndarray, from_v: np.ndarray, pairs: np.ndarray):
+    """Whole-block copies between two pools: block pairs[i, 0] of `from` to pairs[i, 1] of `to`."""
+    lib = _load()
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    _, B, Hk, d = to_k.shape
+    _check(lib.or_swap_copy(_ptr(to_k), _ptr(to_v), _ptr(from_k), _ptr(from_v), _ptr(pairs), int(len(pairs)),
+                            int(to_k.shape[0]), int(from_k.shape[0]), int(B), int(Hk), int(d), int(to_k.itemsize)),
+           "swap_copy")
 
 
 def paged_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray, tables: np.ndarray,

@@ -67,6 +67,7 @@ typedef struct {
     int nblk;           /* entries used in table                     */
     int cap;            /* entries allocated in table                */
     int live;
+    int swapped;        /* 1: table holds host swap-space block ids  */
 } or_seq;
 
 typedef struct {
@@ -79,6 +80,9 @@ typedef struct {
     int nseq;
     int seq_cap;
     long long cow_copies;
+    int num_host_blocks;  /* swap space in host memory (0: none)      */
+    int *host_stack;      /* host_stack[host_top - 1] is handed next  */
+    int host_top;
 } or_bm;
 
 static or_seq *find_seq(or_bm *bm, long long id) {
@@ -145,6 +149,7 @@ void or_bm_delete(or_bm *bm) {
     free(bm->seqs);
     free(bm->free_stack);
     free(bm->refcount);
+    free(bm->host_stack);
     free(bm);
 }
 
@@ -163,7 +168,7 @@ int or_bm_append(or_bm *bm, long long id, int n, long long *slots_out,
     or_seq *s = find_seq(bm, id);
     if (n_cow) *n_cow = 0;
     if (!s) return OR_ERR_UNKNOWN_SEQ;
-    if (n < 0) return OR_ERR_ARG;
+    if (n < 0 || s->swapped) return OR_ERR_ARG;
 
     /* Count the blocks the n tokens need before touching anything. */
     int need = 0;
@@ -213,6 +218,7 @@ int or_bm_append(or_bm *bm, long long id, int n, long long *slots_out,
 int or_bm_fork(or_bm *bm, long long parent, long long child) {
     if (find_seq(bm, child)) return OR_ERR_SEQ_EXISTS;
     if (!find_seq(bm, parent)) return OR_ERR_UNKNOWN_SEQ;
+    if (find_seq(bm, parent)->swapped) return OR_ERR_ARG;
     or_seq *c = new_seq(bm, child);
     if (!c) return OR_ERR_NOMEM;
     or_seq *p = find_seq(bm, parent); /* re-find: new_seq may move the array */
@@ -231,6 +237,10 @@ int or_bm_free_seq(or_bm *bm, long long id) {
     if (!s) return OR_ERR_UNKNOWN_SEQ;
     for (int j = 0; j < s->nblk; j++) {
         int b = s->table[j];
+        if (s->swapped) {            /* host blocks go back to the swap space */
+            bm->host_stack[bm->host_top++] = b;
+            continue;
+        }
         bm->refcount[b] -= 1;
         if (bm->refcount[b] == 0) bm->free_stack[bm->top++] = b;
     }
@@ -238,6 +248,93 @@ int or_bm_free_seq(or_bm *bm, long long id) {
     s->table = NULL;
     s->nblk = s->cap = 0;
     s->live = 0;
+    return OR_OK;
+}
+
+/* Swap space: num_host_blocks blocks in host memory, handed out first to
+ * last as host_order[0], host_order[1], ... (NULL: 0, 1, 2, ...). */
+int or_bm_set_swap_space(or_bm *bm, int num_host_blocks, const int *host_order) {
+    if (num_host_blocks < 0 || bm->num_host_blocks) return OR_ERR_ARG;
+    bm->host_stack = (int *)malloc(sizeof(int) * (size_t)(num_host_blocks > 0 ? num_host_blocks : 1));
+    if (!bm->host_stack) return OR_ERR_NOMEM;
+    for (int i = 0; i < num_host_blocks; i++)
+        bm->host_stack[i] = host_order ? host_order[num_host_blocks - 1 - i] : num_host_blocks - 1 - i;
+    bm->num_host_blocks = num_host_blocks;
+    bm->host_top = num_host_blocks;
+    return OR_OK;
+}
+
+/* Preemption by swapping ("Paged KV Cache Allocation and the Block Table",
+ * "What the design costs": the server may swap a sequence's blocks to host
+ * memory). Every block of the table, in table order, gets a host block:
+ * pairs_out[2j] = device block, pairs_out[2j+1] = host block. The device
+ * block loses the sequence's reference and returns to the free list when no
+ * table names it any more. All or nothing: OR_ERR_OUT_OF_BLOCKS if the swap
+ * space is short. The caller copies the pairs device -> host before the
+ * freed blocks are written again. */
+int or_bm_swap_out(or_bm *bm, long long id, long long *pairs_out, int *n_out) {
+    or_seq *s = find_seq(bm, id);
+    if (n_out) *n_out = 0;
+    if (!s) return OR_ERR_UNKNOWN_SEQ;
+    if (s->swapped) return OR_ERR_ARG;
+    if (s->nblk > bm->host_top) return OR_ERR_OUT_OF_BLOCKS;
+    for (int j = 0; j < s->nblk; j++) {
+        int d = s->table[j];
+        int h = bm->host_stack[--bm->host_top];
+        pairs_out[2 * j] = d;
+        pairs_out[2 * j + 1] = h;
+        bm->refcount[d] -= 1;
+        if (bm->refcount[d] == 0) bm->free_stack[bm->top++] = d;
+        s->table[j] = h;
+    }
+    s->swapped = 1;
+    if (n_out) *n_out = s->nblk;
+    return OR_OK;
+}
+
+/* Brings a swapped sequence back: every host block, in table order, gets a
+ * fresh private device block: pairs_out[2j] = host block, pairs_out[2j+1] =
+ * device block; the host block returns to the swap space. All or nothing:
+ * OR_ERR_OUT_OF_BLOCKS if the device pool is short. */
+int or_bm_swap_in(or_bm *bm, long long id, long long *pairs_out, int *n_out) {
+    or_seq *s = find_seq(bm, id);
+    if (n_out) *n_out = 0;
+    if (!s) return OR_ERR_UNKNOWN_SEQ;
+    if (!s->swapped) return OR_ERR_ARG;
+    if (s->nblk > bm->top) return OR_ERR_OUT_OF_BLOCKS;
+    for (int j = 0; j < s->nblk; j++) {
+        int h = s->table[j];
+        int d = bm->free_stack[--bm->top];
+        bm->refcount[d] = 1;
+        pairs_out[2 * j] = h;
+        pairs_out[2 * j + 1] = d;
+        bm->host_stack[bm->host_top++] = h;
+        s->table[j] = d;
+    }
+    s->swapped = 0;
+    if (n_out) *n_out = s->nblk;
+    return OR_OK;
+}
+
+int or_bm_is_swapped(or_bm *bm, long long id) {
+    or_seq *s = find_seq(bm, id);
+    return s ? s->swapped : -1;
+}
+
+int or_bm_host_free(or_bm *bm) { return bm->host_top; }
+
+/* Whole-block copies between two pools of the same block shape: block
+ * pairs[2p] of `from` goes to block pairs[2p+1] of `to` (K and V). */
+int or_swap_copy(void *to_k, void *to_v, const void *from_k, const void *from_v,
+                 const long long *pairs, int num_pairs, int to_blocks, int from_blocks,
+                 int B, int Hk, int d, int esz) {
+    const size_t blk_bytes = (size_t)B * (size_t)Hk * (size_t)d * (size_t)esz;
+    for (int p = 0; p < num_pairs; p++) {
+        long long src = pairs[2 * p], dst = pairs[2 * p + 1];
+        if (src < 0 || src >= from_blocks || dst < 0 || dst >= to_blocks) return OR_ERR_ARG;
+        memcpy((char *)to_k + (size_t)dst * blk_bytes, (const char *)from_k + (size_t)src * blk_bytes, blk_bytes);
+        memcpy((char *)to_v + (size_t)dst * blk_bytes, (const char *)from_v + (size_t)src * blk_bytes, blk_bytes);
+    }
     return OR_OK;
 }
 

@@ -24,7 +24,7 @@ import pytest
 
 import oracle
 from oracle.contiguous import ContiguousPool
-from workloads import make_workload, prefill_plan
+from workloads import f32_to_bf16_bits, make_workload, prefill_plan
 
 
 def _recount(bm, live):
@@ -300,3 +300,152 @@ def test_prefix_workload_sharing_before_divergence():
         elif op[3][0] == "prefix":
             bm.append(op[1], op[2])
     assert wl.num_blocks - bm.num_free() == 32 * 125
+
+
+# ---------------------------------------------------------------------------
+# Preemption by swapping ("Paged KV Cache Allocation and the Block Table",
+# "What the design costs": the server may swap a sequence's blocks to host
+# memory; "PagedAttention", "Exercises" item 3).
+# ---------------------------------------------------------------------------
+def _check_swap_invariants(bm, live, H):
+    device_live = [s for s in live if not bm.is_swapped(s)]
+    counts = _recount(bm, device_live)
+    for b in range(bm.num_blocks):
+        assert bm.refcount(b) == counts.get(b, 0)
+    assert len(counts) + bm.num_free() == bm.num_blocks
+    host_held = [b for s in live if bm.is_swapped(s) for b in bm.table(s).tolist()]
+    assert len(host_held) == len(set(host_held)), "a host block is held twice"
+    assert all(0 <= b < H for b in host_held)
+    assert len(host_held) + bm.host_free() == H
+
+
+def _pools(N, B, Hk, d):
+    return np.zeros((N, B, Hk, d), np.uint16), np.zeros((N, B, Hk, d), np.uint16)
+
+
+def test_swap_round_trip_keeps_attention_exact():
+    rng = np.random.default_rng(21)
+    N, H, B, Hk, d = 40, 24, 4, 2, 8
+    bm = oracle.BlockManager(N, B, rng.permutation(N).astype(np.int32))
+    bm.set_swap_space(H, rng.permutation(H).astype(np.int32))
+    kc, vc = _pools(N, B, Hk, d)
+    hk, hv = _pools(H, B, Hk, d)
+    lens = [7, 13, 30]
+    for s, n in enumerate(lens):
+        bm.add_seq(s)
+        slots, _ = bm.append(s, n)
+        k = f32_to_bf16_bits(rng.standard_normal((n, Hk, d)).astype(np.float32))
+        v = f32_to_bf16_bits(rng.standard_normal((n, Hk, d)).astype(np.float32))
+        oracle.reshape_and_cache(kc, vc, k, v, slots, N, B)
+    q = f32_to_bf16_bits(rng.standard_normal((3, 4, d)).astype(np.float32))
+    ctx = np.array(lens, np.int64)
+    before = oracle.paged_attention(q, kc, vc, bm.export_tables(range(3), 8), ctx, 0.3, "bf16")
+    pairs = bm.swap_out(1)
+    assert len(pairs) == 4 and bm.is_swapped(1)
+    oracle.swap_copy(hk, hv, kc, vc, pairs)          # device -> host
+    _check_swap_invariants(bm, [0, 1, 2], H)
+    kc[pairs[:, 0]] = 0                              # the freed blocks get reused / clobbered
+    vc[pairs[:, 0]] = 0
+    back = bm.swap_in(1)
+    assert not bm.is_swapped(1) and np.array_equal(back[:, 0], pairs[:, 1])
+    oracle.swap_copy(kc, vc, hk, hv, back)           # host -> device
+    _check_swap_invariants(bm, [0, 1, 2], H)
+    after = oracle.paged_attention(q, kc, vc, bm.export_tables(range(3), 8), ctx, 0.3, "bf16")
+    assert np.array_equal(before, after)
+
+
+def test_swap_out_of_a_fork_keeps_the_shared_blocks():
+    bm = oracle.BlockManager(32, 4, None)
+    bm.set_swap_space(16, None)
+    bm.add_seq(0)
+    bm.append(0, 10)
+    bm.fork(0, 1)
+    shared = bm.table(0).tolist()
+    pairs = bm.swap_out(1)
+    assert pairs[:, 0].tolist() == shared
+    assert all(bm.refcount(b) == 1 for b in shared)          # the parent still names them
+    assert bm.num_free() == 32 - len(shared)                 # nothing was freed
+    back = bm.swap_in(1)
+    assert not set(back[:, 1].tolist()) & set(shared)        # the child comes back private
+    assert all(bm.refcount(int(b)) == 1 for b in back[:, 1])
+    _check_swap_invariants(bm, [0, 1], 16)
+
+
+def test_swap_is_all_or_nothing_and_blocks_the_swapped_sequence():
+    bm = oracle.BlockManager(6, 4, None)
+    bm.set_swap_space(2, None)
+    bm.add_seq(0)
+    bm.append(0, 12)                                         # 3 blocks
+    with pytest.raises(oracle.OracleError) as ei:
+        bm.swap_out(0)                                       # swap space holds 2
+    assert ei.value.code == oracle.ERR_OUT_OF_BLOCKS
+    assert not bm.is_swapped(0) and bm.host_free() == 2 and bm.num_free() == 3
+    bm.add_seq(1)
+    bm.append(1, 5)                                          # 2 blocks
+    bm.swap_out(1)
+    with pytest.raises(oracle.OracleError):
+        bm.append(1, 1)                                      # a swapped sequence cannot grow
+    with pytest.raises(oracle.OracleError):
+        bm.fork(1, 9)
+    bm.add_seq(2)
+    bm.append(2, 12)                                         # takes the 3 free blocks
+    with pytest.raises(oracle.OracleError) as ei:
+        bm.swap_in(1)                                        # 2 device blocks needed, 1 free
+    assert ei.value.code == oracle.ERR_OUT_OF_BLOCKS and bm.is_swapped(1)
+    bm.free_seq(1)                                           # host blocks return
+    assert bm.host_free() == 2
+    _check_swap_invariants(bm, [0, 2], 2)
+
+
+def test_exhaustion_recovered_by_swapping():
+    # A sequence that keeps generating runs the pool dry; swapping another
+    # sequence out lets it continue, and the other comes back once space frees.
+    bm = oracle.BlockManager(8, 4, None)
+    bm.set_swap_space(8, None)
+    for s in (0, 1):
+        bm.add_seq(s)
+        bm.append(s, 16)                                     # 4 blocks each: pool full
+    with pytest.raises(oracle.OracleError):
+        bm.append(0, 1)
+    bm.swap_out(1)
+    bm.append(0, 1)                                          # now fits
+    assert bm.seq_len(0) == 17
+    bm.free_seq(0)
+    bm.swap_in(1)
+    assert bm.seq_len(1) == 16 and len(bm.table(1)) == 4
+    _check_swap_invariants(bm, [1], 8)
+
+
+def test_random_operations_with_swaps_keep_invariants():
+    rng = np.random.default_rng(77)
+    for trial in range(15):
+        B = int(rng.choice([1, 4, 8]))
+        N, H = int(rng.integers(10, 50)), int(rng.integers(4, 40))
+        bm = oracle.BlockManager(N, B, rng.permutation(N).astype(np.int32))
+        bm.set_swap_space(H, rng.permutation(H).astype(np.int32))
+        live, nid = [], 0
+        for _ in range(120):
+            r = rng.random()
+            try:
+                if r < 0.15 or not live:
+                    bm.add_seq(nid)
+                    live.append(nid)
+                    nid += 1
+                elif r < 0.45:
+                    bm.append(int(rng.choice(live)), int(rng.integers(0, 2 * B + 2)))
+                elif r < 0.55:
+                    p = int(rng.choice(live))
+                    bm.fork(p, nid)
+                    live.append(nid)
+                    nid += 1
+                elif r < 0.7:
+                    bm.swap_out(int(rng.choice(live)))
+                elif r < 0.85:
+                    bm.swap_in(int(rng.choice(live)))
+                else:
+                    s = int(rng.choice(live))
+                    bm.free_seq(s)
+                    live.remove(s)
+            except oracle.OracleError as e:
+                assert e.code in (oracle.ERR_OUT_OF_BLOCKS, oracle.ERR_ARG, oracle.ERR_SEQ_EXISTS)
+            _check_swap_invariants(bm, live, H)

@@ -34,6 +34,10 @@ MUTANTS = {
     "fork_without_increment": ("bm->refcount[p->table[j]] += 1;", ";"),
     "free_ignores_refcount": ("if (bm->refcount[b] == 0) bm->free_stack[bm->top++] = b;",
                               "bm->free_stack[bm->top++] = b;"),
+    "swap_out_keeps_reference": ("        bm->refcount[d] -= 1;\n        if (bm->refcount[d] == 0) bm->free_stack[bm->top++] = d;\n        s->table[j] = h;",
+                                 "        s->table[j] = h;"),
+    "swap_in_shares_host_block": ("        bm->host_stack[bm->host_top++] = h;\n        s->table[j] = d;",
+                                  "        s->table[j] = d;"),
     "copy_blocks_swapped": ("memcpy((char *)k_cache + (size_t)dst * blk_bytes, (char *)k_cache + (size_t)src * blk_bytes",
                             "memcpy((char *)k_cache + (size_t)src * blk_bytes, (char *)k_cache + (size_t)dst * blk_bytes"),
 }
