@@ -13,6 +13,9 @@ flushed (a write of twice its size) between steps, outside the events.
 ``e2e`` times the same steps through the public API from pinned host buffers:
 the host block-manager append, the host->device copies of the step's inputs,
 the kernels and the device->host copy of the output are all inside the timer.
+``swap`` (after the steps) times preemption by swapping: half the batch's
+blocks to a pinned host pool and back, one pk_swap_blocks launch per
+direction, beside a contiguous copy-engine copy of the same bytes.
 
 Metric: algorithmic K/V bytes read per step (sum over sequences of
 context_len * Hk * head_dim * 2 bytes * 2 for K and V) per second.
@@ -66,6 +69,7 @@ def parse_args(argv=None):
     p.add_argument("--no-order", action="store_true", help="launch sequences in index order, not longest first")
     p.add_argument("--cascade", action="store_true",
                    help="cascade attention: each shared prefix read once per group (prefix workload)")
+    p.add_argument("--no-swap", action="store_true", help="skip the swap-out / swap-in bandwidth measurement")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -457,6 +461,8 @@ def run_ours(args):
         e2e.pop("_seconds")
         e2e.pop("_bytes")
 
+    swap = None if args.no_swap or groups is not None else run_swap(st, wl, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref = oracle_state(wl)
@@ -495,6 +501,7 @@ def run_ours(args):
             "wall_s_timed_region": wall,
             "clocks": clocks,
             "e2e": e2e,
+            "swap": swap,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -542,6 +549,70 @@ def run_e2e(st, wl, E, Ew, args, dev):
                         "H2D (q, k, v, one metadata buffer), kernels (per-sequence attention), "
                         "D2H of the output; stream sync",
             "_seconds": tot_t, "_bytes": tot_b}
+
+
+def run_swap(st, wl, dev, reps: int = 5) -> dict:
+    """Preemption by swapping, measured after the decode steps: every other
+    sequence of the batch is swapped out to a pinned host pool and back in,
+    ``reps`` times. Each direction is one pk_swap_blocks launch timed with
+    CUDA events; the host-link peak beside it is a contiguous copy-engine
+    copy of the same bytes between pinned host memory and the device."""
+    import torch
+    import paged_kv_cache_113_gb300 as pk
+
+    victims = list(range(0, wl.num_seqs, 2))
+    nblk = sum(len(st.bm.table(s)) for s in victims)
+    st.bm.set_swap_space(nblk, np.arange(nblk, dtype=np.int32))
+    shape = (nblk,) + tuple(st.k_cache.shape[1:])
+    hk = torch.empty(shape, dtype=st.k_cache.dtype).pin_memory()
+    hv = torch.empty(shape, dtype=st.k_cache.dtype).pin_memory()
+    moved = 2 * hk.numel() * hk.element_size()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    t_out = t_in = 0.0
+    for r in range(reps + 1):
+        po = torch.from_numpy(np.concatenate([st.bm.swap_out(s) for s in victims])).to(dev)
+        torch.cuda.synchronize()
+        ev[0].record()
+        pk.pk_swap_blocks(st.k_cache, st.v_cache, hk, hv, po, pk.PK_SWAP_OUT)
+        ev[1].record()
+        pi = torch.from_numpy(np.concatenate([st.bm.swap_in(s) for s in victims])).to(dev)
+        torch.cuda.synchronize()
+        ev[2].record()
+        pk.pk_swap_blocks(st.k_cache, st.v_cache, hk, hv, pi, pk.PK_SWAP_IN)
+        ev[3].record()
+        torch.cuda.synchronize()
+        if r:
+            t_out += ev[0].elapsed_time(ev[1]) / 1e3
+            t_in += ev[2].elapsed_time(ev[3]) / 1e3
+    kind, idx = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error while swapping: {pk.DEVERR_NAMES.get(kind)} at {idx}")
+    st.bm.check_invariants()
+
+    # Copy-engine reference: the same bytes as two contiguous copies per direction.
+    scratch = torch.empty(2 * hk.numel(), dtype=hk.dtype, device=dev)
+    t_d2h = t_h2d = 0.0
+    for r in range(reps + 1):
+        torch.cuda.synchronize()
+        ev[0].record()
+        hk.view(-1).copy_(scratch[:hk.numel()], non_blocking=True)
+        hv.view(-1).copy_(scratch[hk.numel():], non_blocking=True)
+        ev[1].record()
+        scratch[:hk.numel()].copy_(hk.view(-1), non_blocking=True)
+        scratch[hk.numel():].copy_(hv.view(-1), non_blocking=True)
+        ev[2].record()
+        torch.cuda.synchronize()
+        if r:
+            t_d2h += ev[0].elapsed_time(ev[1]) / 1e3
+            t_h2d += ev[1].elapsed_time(ev[2]) / 1e3
+    out_gbs, in_gbs = reps * moved / t_out / 1e9, reps * moved / t_in / 1e9
+    d2h_gbs, h2d_gbs = reps * moved / t_d2h / 1e9, reps * moved / t_h2d / 1e9
+    return {"sequences": len(victims), "blocks": nblk, "bytes_per_direction": moved, "reps": reps,
+            "out_gbs": out_gbs, "in_gbs": in_gbs, "out_ms": 1e3 * t_out / reps, "in_ms": 1e3 * t_in / reps,
+            "link_copy_d2h_gbs": d2h_gbs, "link_copy_h2d_gbs": h2d_gbs,
+            "frac_out": out_gbs / d2h_gbs, "frac_in": in_gbs / h2d_gbs,
+            "kernel": "swap_blocks_kernel (one launch per direction, host pool mapped into the device)",
+            "peak_kind": "contiguous pinned copy of the same bytes, measured in this run"}
 
 
 def step_kv_bytes(st, wl) -> int:

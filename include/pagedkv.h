@@ -111,6 +111,25 @@ pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot
 pk_status pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pairs,
                          int32_t num_pairs, const pk_cache_desc *desc, void *stream);
 
+/* Swap copies for preemption ("Paged KV Cache Allocation and the Block
+ * Table", "What the design costs": a sequence's blocks swapped to host memory
+ * and restored). Copies whole blocks (K and V) between the device pool and a
+ * host pool of the same block shape, [num_host_blocks, B, Hk, d]:
+ *   direction PK_SWAP_OUT: pairs[p] = (device block, host block);
+ *   direction PK_SWAP_IN:  pairs[p] = (host block, device block)
+ * -- exactly the pairs pk_bm_swap_out / pk_bm_swap_in return.
+ *   k_host, v_host  pinned host memory the device can address (cudaHostAlloc
+ *                   or registered); PK_ERR_INVALID_ARG otherwise.
+ *   pairs           int64 [num_pairs][2], readable by the device (device
+ *                   memory or pinned host memory).
+ * A swap-out must be enqueued before anything writes the device blocks it
+ * freed; a swap-in before anything reads the sequence's new blocks.
+ * Out-of-range ids are skipped and recorded (PK_DEVERR_PAIR). */
+enum { PK_SWAP_OUT = 0, PK_SWAP_IN = 1 };
+pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_host,
+                         int32_t num_host_blocks, const int64_t *pairs, int32_t num_pairs,
+                         int32_t direction, const pk_cache_desc *desc, void *stream);
+
 /* Decode attention through the block table ("PagedAttention", S06, the
  * paged_attention listing and "Why this needed a custom CUDA kernel": the
  * table lookup happens inside the kernel, no pre-gather). For each sequence
@@ -316,6 +335,30 @@ int32_t pk_bm_refcount(const pk_bm *bm, int32_t block); /* -1 if out of range */
  * match, no named block is free, no block is lost or listed twice, and each
  * table holds ceil(len / B) blocks. PK_ERR_INVARIANT on the first violation. */
 pk_status pk_bm_check_invariants(const pk_bm *bm);
+
+/* Swap space for preemption: num_host_blocks host blocks, handed out first
+ * to last as host_order[0], host_order[1], ... (NULL: 0, 1, 2, ...). Once. */
+pk_status pk_bm_set_swap_space(pk_bm *bm, int32_t num_host_blocks, const int32_t *host_order);
+
+/* Swaps a sequence out: every block of its table, in table order, gets a
+ * host block; pairs_out[j] = (device block, host block) for pk_swap_blocks
+ * (PK_SWAP_OUT); the device block loses the sequence's reference and returns
+ * to the free list when no table names it (a block shared with a fork stays).
+ * cap >= table length. All or nothing (PK_ERR_OUT_OF_BLOCKS when the swap
+ * space is short). A swapped sequence cannot append, fork or be exported;
+ * pk_bm_free_seq returns its host blocks. */
+pk_status pk_bm_swap_out(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t cap,
+                         int32_t *n_out);
+
+/* Swaps a sequence back in: fresh private device blocks in table order;
+ * pairs_out[j] = (host block, device block) for pk_swap_blocks (PK_SWAP_IN);
+ * the host blocks return to the swap space. All or nothing
+ * (PK_ERR_OUT_OF_BLOCKS when the device pool is short). */
+pk_status pk_bm_swap_in(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t cap,
+                        int32_t *n_out);
+
+int32_t pk_bm_is_swapped(const pk_bm *bm, int64_t seq_id); /* 1, 0, or -1 if unknown */
+int32_t pk_bm_host_free(const pk_bm *bm);                 /* free swap-space blocks   */
 
 /* Shared-prefix groups for cascade attention. Sequences of seq_ids[0..n-1]
  * whose tables begin with the same physical block (forks of one parent) are

@@ -52,7 +52,10 @@ EXPORTED = (
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
     "pk_decode_step_meta_bytes", "pk_decode_step",
     "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
+    "pk_swap_blocks", "pk_bm_set_swap_space", "pk_bm_swap_out", "pk_bm_swap_in", "pk_bm_is_swapped",
+    "pk_bm_host_free",
 )
+PK_SWAP_OUT, PK_SWAP_IN = 0, 1
 
 
 class CacheDesc(ctypes.Structure):
@@ -120,6 +123,12 @@ def lib() -> ctypes.CDLL:
         "pk_cascade_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, P, P, P,
                                               i32, i32, i32, P, P, sz, D, P]),
         "pk_cascade_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, D]),
+        "pk_swap_blocks": (i32, [P, P, P, P, i32, P, i32, i32, D, P]),
+        "pk_bm_set_swap_space": (i32, [P, i32, P]),
+        "pk_bm_swap_out": (i32, [P, i64, P, i32, P]),
+        "pk_bm_swap_in": (i32, [P, i64, P, i32, P]),
+        "pk_bm_is_swapped": (i32, [P, i64]),
+        "pk_bm_host_free": (i32, [P]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
     }
     for name, (res, args) in sigs.items():
@@ -320,6 +329,28 @@ def pk_cascade_attention_decode(out, q, k_cache, v_cache, block_tables, context_
         _stream(stream)), "pk_cascade_attention_decode")
 
 
+def pk_swap_blocks(k_cache, v_cache, k_host, v_host, pairs, direction: int, stream=None):
+    """Whole-block copies between the device pool and a pinned host pool
+    ``[H, B, Hk, d]``: ``pairs`` int64 ``[n, 2]`` (CUDA or pinned CPU tensor)
+    from pk_bm_swap_out (``PK_SWAP_OUT``) or pk_bm_swap_in (``PK_SWAP_IN``)."""
+    desc = cache_desc(k_cache)
+    if k_host.is_cuda or not k_host.is_pinned() or not v_host.is_pinned():
+        raise ValueError("k_host and v_host must be pinned host tensors")
+    if tuple(k_host.shape[1:]) != tuple(k_cache.shape[1:]) or v_host.shape != k_host.shape:
+        raise ValueError("host pools must be [H, B, Hk, d] like the device pool")
+    n = int(pairs.shape[0]) if pairs.numel() else 0
+    if n == 0:
+        return
+    if pairs.dtype != _torch().int64 or not pairs.is_contiguous():
+        raise TypeError("pairs must be contiguous int64 [n, 2]")
+    if not (pairs.is_cuda or pairs.is_pinned()):
+        raise ValueError("pairs must be a CUDA tensor or pinned host memory")
+    _check(lib().pk_swap_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                                ctypes.c_void_p(k_host.data_ptr()), ctypes.c_void_p(v_host.data_ptr()),
+                                int(k_host.shape[0]), ctypes.c_void_p(pairs.data_ptr()), n, int(direction),
+                                ctypes.byref(desc), _stream(stream)), "pk_swap_blocks")
+
+
 def pk_get_device_error(stream=None) -> Tuple[int, int]:
     """Synchronises the stream, reads and clears the device error word.
 
@@ -412,6 +443,31 @@ class BlockManager:
         _check(self._L.pk_bm_export_tables(self._h, _np_ptr(ids), n, int(max_blocks), _np_ptr(tables),
                                            _np_ptr(lens)), "pk_bm_export_tables")
         return tables, lens
+
+    def set_swap_space(self, num_host_blocks: int, host_order: Optional[np.ndarray] = None):
+        order = None if host_order is None else np.ascontiguousarray(host_order, dtype=np.int32)
+        _check(self._L.pk_bm_set_swap_space(self._h, int(num_host_blocks), _np_ptr(order)), "pk_bm_set_swap_space")
+
+    def _swap(self, fn, name, seq):
+        n = len(self.table(seq))
+        pairs = np.zeros((max(n, 1), 2), np.int64)
+        cnt = ctypes.c_int32(0)
+        _check(fn(self._h, int(seq), _np_ptr(pairs), n, ctypes.byref(cnt)), name)
+        return pairs[: cnt.value]
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """(device block, host block) pairs, int64 [n, 2], in table order."""
+        return self._swap(self._L.pk_bm_swap_out, "pk_bm_swap_out", seq)
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """(host block, device block) pairs, int64 [n, 2], in table order."""
+        return self._swap(self._L.pk_bm_swap_in, "pk_bm_swap_in", seq)
+
+    def is_swapped(self, seq: int) -> bool:
+        return int(self._L.pk_bm_is_swapped(self._h, int(seq))) == 1
+
+    def host_free(self) -> int:
+        return int(self._L.pk_bm_host_free(self._h))
 
     def prefix_groups(self, seqs: Sequence[int], max_group_size: int, min_prefix_blocks: int = 1) -> dict:
         """Shared-prefix groups of the batch ``seqs`` (host numpy arrays)."""

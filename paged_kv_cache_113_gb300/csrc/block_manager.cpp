@@ -30,7 +30,8 @@ namespace {
 
 struct Sequence {
   int64_t len = 0;
-  std::vector<int32_t> table;
+  std::vector<int32_t> table;  // device block ids, or host block ids when swapped
+  bool swapped = false;
 };
 
 // What one token append changed, so a failed batch can be rolled back.
@@ -49,6 +50,8 @@ struct pk_bm {
   std::vector<int32_t> refs;
   std::unordered_map<int64_t, Sequence> seqs;
   int64_t cow_copies = 0;
+  int32_t num_host_blocks = 0;           // swap space in host memory
+  std::vector<int32_t> host_free;        // back() is handed out next
 
   int64_t blocks_for(int64_t len) const { return (len + block_size - 1) / block_size; }
 
@@ -158,6 +161,7 @@ pk_status pk_bm_append_slots(pk_bm *bm, int64_t seq_id, int32_t n, int64_t *slot
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
   Sequence &s = it->second;
+  if (s.swapped) return PK_ERR_INVALID_ARG;
   if (n == 0) return PK_OK;
   // Blocks needed: one per block boundary crossed, plus a CoW copy when the
   // first token lands in a shared, partly filled tail.
@@ -194,6 +198,7 @@ pk_status pk_bm_append_batch(pk_bm *bm, const int64_t *seq_ids, int32_t n, int64
     for (int32_t i = 0; i < n; ++i) {
       auto it = bm->seqs.find(seq_ids[i]);
       if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+      if (it->second.swapped) return PK_ERR_INVALID_ARG;
       it->second.table.reserve(size_t(bm->blocks_for(it->second.len + 1)));
       seqp.push_back(&it->second);
     }
@@ -229,6 +234,7 @@ pk_status pk_bm_fork(pk_bm *bm, int64_t parent, int64_t child) {
   if (bm->seqs.count(child)) return PK_ERR_SEQ_EXISTS;
   auto it = bm->seqs.find(parent);
   if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  if (it->second.swapped) return PK_ERR_INVALID_ARG;
   try {
     Sequence copy = it->second;
     for (int32_t b : copy.table) bm->refs[b] += 1;
@@ -244,7 +250,10 @@ pk_status pk_bm_free_seq(pk_bm *bm, int64_t seq_id) {
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
   for (int32_t b : it->second.table) {
-    if (--bm->refs[b] == 0) bm->free_stack.push_back(b);
+    if (it->second.swapped)
+      bm->host_free.push_back(b);  // a swapped sequence holds host blocks
+    else if (--bm->refs[b] == 0)
+      bm->free_stack.push_back(b);
   }
   bm->seqs.erase(it);
   return PK_OK;
@@ -278,7 +287,8 @@ pk_status pk_bm_export_tables(const pk_bm *bm, const int64_t *seq_ids, int32_t n
     auto it = bm->seqs.find(seq_ids[i]);
     if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
     const auto &s = it->second;
-    if (int64_t(s.table.size()) > max_blocks || s.len > INT32_MAX) return PK_ERR_INVALID_ARG;
+    if (s.swapped || int64_t(s.table.size()) > max_blocks || s.len > INT32_MAX)
+      return PK_ERR_INVALID_ARG;
     int32_t *row = tables_out + size_t(i) * size_t(max_blocks);
     std::copy(s.table.begin(), s.table.end(), row);
     std::fill(row + s.table.size(), row + max_blocks, -1);
@@ -297,14 +307,27 @@ int32_t pk_bm_refcount(const pk_bm *bm, int32_t block) {
 pk_status pk_bm_check_invariants(const pk_bm *bm) {
   if (!bm) return PK_ERR_INVALID_ARG;
   std::vector<int32_t> count(bm->num_blocks, 0);
+  std::vector<char> host_used(bm->num_host_blocks, 0);
+  int64_t host_held = 0;
   for (const auto &kv : bm->seqs) {
     const Sequence &s = kv.second;
     if (int64_t(s.table.size()) != bm->blocks_for(s.len)) return PK_ERR_INVARIANT;
     for (int32_t b : s.table) {
+      if (s.swapped) {
+        if (b < 0 || b >= bm->num_host_blocks || host_used[b]) return PK_ERR_INVARIANT;
+        host_used[b] = 1;
+        ++host_held;
+        continue;
+      }
       if (b < 0 || b >= bm->num_blocks) return PK_ERR_INVARIANT;
       ++count[b];
     }
   }
+  for (int32_t b : bm->host_free) {
+    if (b < 0 || b >= bm->num_host_blocks || host_used[b]) return PK_ERR_INVARIANT;
+    host_used[b] = 1;
+  }
+  if (host_held + int64_t(bm->host_free.size()) != bm->num_host_blocks) return PK_ERR_INVARIANT;
   std::vector<char> is_free(bm->num_blocks, 0);
   for (int32_t b : bm->free_stack) {
     if (b < 0 || b >= bm->num_blocks || is_free[b] || count[b] != 0) return PK_ERR_INVARIANT;
@@ -338,6 +361,82 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
   return PK_OK;
 }
 
+pk_status pk_bm_set_swap_space(pk_bm *bm, int32_t num_host_blocks, const int32_t *host_order) {
+  if (!bm || num_host_blocks < 0 || bm->num_host_blocks != 0) return PK_ERR_INVALID_ARG;
+  try {
+    std::vector<int32_t> stack(num_host_blocks);
+    std::vector<char> seen(num_host_blocks, 0);
+    for (int32_t i = 0; i < num_host_blocks; ++i) {
+      const int32_t b = host_order ? host_order[i] : i;
+      if (b < 0 || b >= num_host_blocks || seen[b]) return PK_ERR_INVALID_ARG;
+      seen[b] = 1;
+      stack[num_host_blocks - 1 - i] = b;  // host_order[0] ends on top
+    }
+    bm->host_free.swap(stack);
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  bm->num_host_blocks = num_host_blocks;
+  return PK_OK;
+}
+
+pk_status pk_bm_swap_out(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t cap,
+                         int32_t *n_out) {
+  if (!bm || !n_out) return PK_ERR_INVALID_ARG;
+  *n_out = 0;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  Sequence &s = it->second;
+  const int32_t n = int32_t(s.table.size());
+  if (s.swapped || cap < n || (n > 0 && !pairs_out)) return PK_ERR_INVALID_ARG;
+  if (n > int32_t(bm->host_free.size())) return PK_ERR_OUT_OF_BLOCKS;
+  for (int32_t j = 0; j < n; ++j) {
+    const int32_t d = s.table[j];
+    const int32_t h = bm->host_free.back();
+    bm->host_free.pop_back();
+    pairs_out[2 * j] = d;
+    pairs_out[2 * j + 1] = h;
+    if (--bm->refs[d] == 0) bm->free_stack.push_back(d);
+    s.table[j] = h;
+  }
+  s.swapped = true;
+  *n_out = n;
+  return PK_OK;
+}
+
+pk_status pk_bm_swap_in(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t cap,
+                        int32_t *n_out) {
+  if (!bm || !n_out) return PK_ERR_INVALID_ARG;
+  *n_out = 0;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  Sequence &s = it->second;
+  const int32_t n = int32_t(s.table.size());
+  if (!s.swapped || cap < n || (n > 0 && !pairs_out)) return PK_ERR_INVALID_ARG;
+  if (n > int32_t(bm->free_stack.size())) return PK_ERR_OUT_OF_BLOCKS;
+  for (int32_t j = 0; j < n; ++j) {
+    const int32_t h = s.table[j];
+    const int32_t d = bm->free_stack.back();
+    bm->free_stack.pop_back();
+    bm->refs[d] = 1;
+    pairs_out[2 * j] = h;
+    pairs_out[2 * j + 1] = d;
+    bm->host_free.push_back(h);
+    s.table[j] = d;
+  }
+  s.swapped = false;
+  *n_out = n;
+  return PK_OK;
+}
+
+int32_t pk_bm_is_swapped(const pk_bm *bm, int64_t seq_id) {
+  if (!bm) return -1;
+  auto it = bm->seqs.find(seq_id);
+  return it == bm->seqs.end() ? -1 : (it->second.swapped ? 1 : 0);
+}
+
+int32_t pk_bm_host_free(const pk_bm *bm) { return bm ? int32_t(bm->host_free.size()) : -1; }
+
 pk_status pk_bm_prefix_groups(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
                               int32_t max_group_size, int32_t min_prefix_blocks,
                               int32_t *group_offsets, int32_t *group_members,
@@ -360,7 +459,7 @@ pk_status pk_bm_prefix_groups(const pk_bm *bm, const int64_t *seq_ids, int32_t n
   std::unordered_map<int32_t, std::vector<int32_t>> buckets;
   std::vector<int32_t> first_seen;
   for (int32_t i = 0; i < n; ++i) {
-    if (seq[i]->table.empty()) continue;
+    if (seq[i]->table.empty() || seq[i]->swapped) continue;
     const int32_t b0 = seq[i]->table[0];
     auto &v = buckets[b0];
     if (v.empty()) first_seen.push_back(b0);

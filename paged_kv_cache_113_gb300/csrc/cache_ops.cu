@@ -74,6 +74,39 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
   for (; j < end; j += blockDim.x) to[j] = from[j];
 }
 
+// grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block:
+// whole block pairs[2p] of one pool goes to block pairs[2p+1] of the other
+// (swap out: device pool -> pinned host pool; swap in: the reverse). The host
+// pool is read or written through its device-visible address.
+__global__ void __launch_bounds__(256) swap_blocks_kernel(
+    const uint4 *__restrict__ from_k, const uint4 *__restrict__ from_v, uint4 *__restrict__ to_k,
+    uint4 *__restrict__ to_v, const int64_t *__restrict__ pairs, int32_t from_blocks,
+    int32_t to_blocks, int64_t block_vecs, int64_t chunk_vecs) {
+  const int64_t src = pairs[2 * blockIdx.x];
+  const int64_t dst = pairs[2 * blockIdx.x + 1];
+  if (src < 0 || src >= from_blocks || dst < 0 || dst >= to_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+      pk::record_error(&g_cache_ops_error, PK_DEVERR_PAIR, blockIdx.x);
+    return;
+  }
+  const uint4 *from = (blockIdx.y == 0 ? from_k : from_v) + src * block_vecs;
+  uint4 *to = (blockIdx.y == 0 ? to_k : to_v) + dst * block_vecs;
+  const int64_t beg = int64_t(blockIdx.z) * chunk_vecs;
+  const int64_t end = min(block_vecs, beg + chunk_vecs);
+  int64_t j = beg + threadIdx.x;
+  for (; j + 3 * int64_t(blockDim.x) < end; j += 4 * int64_t(blockDim.x)) {
+    const uint4 a = from[j];
+    const uint4 b = from[j + blockDim.x];
+    const uint4 c = from[j + 2 * blockDim.x];
+    const uint4 d = from[j + 3 * blockDim.x];
+    to[j] = a;
+    to[j + blockDim.x] = b;
+    to[j + 2 * blockDim.x] = c;
+    to[j + 3 * blockDim.x] = d;
+  }
+  for (; j < end; j += blockDim.x) to[j] = from[j];
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
@@ -148,6 +181,40 @@ pk_status pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pa
   copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs,
       desc->num_blocks, block_vecs, chunk_vecs);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_host,
+                         int32_t num_host_blocks, const int64_t *pairs, int32_t num_pairs,
+                         int32_t direction, const pk_cache_desc *desc, void *stream) {
+  pk_status st = check_desc(desc);
+  if (st != PK_OK) return st;
+  if (num_pairs < 0 || num_host_blocks < 0 || (direction != PK_SWAP_OUT && direction != PK_SWAP_IN))
+    return PK_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PK_OK;
+  if (!k_cache || !v_cache || !k_host || !v_host || !pairs) return PK_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_host) || !aligned16(v_host))
+    return PK_ERR_INVALID_ARG;
+  // The host pool must be reachable from the device (pinned, mapped memory).
+  void *dk = nullptr, *dv = nullptr;
+  if (cudaHostGetDevicePointer(&dk, k_host, 0) != cudaSuccess ||
+      cudaHostGetDevicePointer(&dv, v_host, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_INVALID_ARG;
+  }
+  const int64_t block_bytes = int64_t(desc->block_size) * desc->num_kv_heads * desc->head_dim *
+                              elem_size(desc->dtype);
+  const int64_t block_vecs = block_bytes / 16;
+  const int64_t chunk_vecs = 256 * 8;
+  const int64_t chunks = (block_vecs + chunk_vecs - 1) / chunk_vecs;
+  if (chunks > 65535) return PK_ERR_UNSUPPORTED;
+  dim3 grid(num_pairs, 2, unsigned(chunks));
+  const bool out = direction == PK_SWAP_OUT;
+  swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4 *>(out ? k_cache : dk), static_cast<const uint4 *>(out ? v_cache : dv),
+      static_cast<uint4 *>(out ? dk : k_cache), static_cast<uint4 *>(out ? dv : v_cache), pairs,
+      out ? desc->num_blocks : num_host_blocks, out ? num_host_blocks : desc->num_blocks, block_vecs,
+      chunk_vecs);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 

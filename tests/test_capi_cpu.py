@@ -298,3 +298,58 @@ def test_prefix_groups_match_brute_force(L, B, max_group, min_blocks):
     assert g["seq_prefix_len"].tolist() == want_seq
     if min_blocks == 1:
         assert g["num_groups"] > 0 and all(p >= (2000 // B - 1) * B for _, p in got)
+
+
+def test_swap_matches_oracle_on_random_operations(L):
+    rng = np.random.default_rng(314)
+    for trial in range(12):
+        B = int(rng.choice([1, 4, 16]))
+        N, H = int(rng.integers(10, 60)), int(rng.integers(4, 50))
+        order, horder = rng.permutation(N).astype(np.int32), rng.permutation(H).astype(np.int32)
+        ours, ref = pk.BlockManager(N, B, order), oracle.BlockManager(N, B, order)
+        ours.set_swap_space(H, horder)
+        ref.set_swap_space(H, horder)
+        live, nid = [], 0
+        for _ in range(150):
+            r = rng.random()
+            s = int(rng.choice(live)) if live else None
+            if r < 0.15 or not live:
+                ours.add_seq(nid)
+                ref.add_seq(nid)
+                live.append(nid)
+                nid += 1
+                continue
+            if r < 0.45:
+                n = int(rng.integers(0, 2 * B + 2))
+                args = ("append", s, n)
+            elif r < 0.55:
+                args = ("fork", s, nid)
+            elif r < 0.7:
+                args = ("swap_out", s)
+            elif r < 0.85:
+                args = ("swap_in", s)
+            else:
+                args = ("free_seq", s)
+            res = []
+            for bm, err in ((ours, pk.PagedKVError), (ref, oracle.OracleError)):
+                try:
+                    res.append(("ok", getattr(bm, args[0])(*args[1:])))
+                except err:
+                    res.append(("err", None))
+            assert res[0][0] == res[1][0], (args, res)
+            if res[0][0] == "ok":
+                a, b = res[0][1], res[1][1]
+                if args[0] == "append":
+                    assert np.array_equal(a[0], b[0]) and a[1] == b[1]
+                elif args[0] in ("swap_out", "swap_in"):
+                    assert np.array_equal(a, b)
+                elif args[0] == "fork":
+                    live.append(nid)
+                    nid += 1
+                elif args[0] == "free_seq":
+                    live.remove(s)
+            ours.check_invariants()
+            assert ours.num_free() == ref.num_free() and ours.host_free() == ref.host_free()
+            for q in live:
+                assert ours.is_swapped(q) == ref.is_swapped(q)
+                assert np.array_equal(ours.table(q), ref.table(q))
