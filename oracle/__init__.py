@@ -84,6 +84,10 @@ def _load():
         "or_bm_swap_in": (i32, [P, i64, P, P]),
         "or_bm_is_swapped": (i32, [P, i64]),
         "or_bm_host_free": (i32, [P]),
+        "or_bm_add_seq_cached": (i32, [P, i64, P, i32, P]),
+        "or_bm_commit": (i32, [P, i64, P, i32]),
+        "or_bm_cache_stats": (None, [P, P, P, P, P]),
+        "or_bm_is_cached": (i32, [P, i32]),
         "or_swap_copy": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32]),
         "or_reshape_and_cache": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32]),
         "or_copy_blocks": (i32, [P, P, P, i32, i32, i32, i32, i32, i32]),
@@ -171,7 +175,9 @@ class BlockManager:
         return int(self._lib.or_bm_cow_copies(self._h))
 
     def free_list(self) -> np.ndarray:
-        n = self.num_free()
+        """The free stack, next block to be handed out first (cached blocks
+        that no table names are not on it)."""
+        n = int(self._lib.or_bm_free_list(self._h, None, 0))
         out = np.empty(max(n, 1), dtype=np.int32)
         self._lib.or_bm_free_list(self._h, _ptr(out), n)
         return out[:n]
@@ -202,6 +208,29 @@ class BlockManager:
 
     def host_free(self) -> int:
         return int(self._lib.or_bm_host_free(self._h))
+
+    # -- prefix caching ("PagedAttention" S06, "What's next") ----------------
+    def add_seq_cached(self, seq: int, tokens) -> int:
+        """New sequence whose prompt is ``tokens``; starts with every leading
+        full block found in the cache. Returns the number of cached tokens."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int(0)
+        _check(self._lib.or_bm_add_seq_cached(self._h, int(seq), _ptr(t) if len(t) else None, len(t),
+                                              ctypes.byref(n)), "add_seq_cached")
+        return int(n.value)
+
+    def commit(self, seq: int, tokens):
+        """Registers the sequence's full blocks among ``tokens`` (its token ids)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(self._lib.or_bm_commit(self._h, int(seq), _ptr(t) if len(t) else None, len(t)), "commit")
+
+    def cache_stats(self) -> dict:
+        v = [ctypes.c_longlong(0) for _ in range(4)]
+        self._lib.or_bm_cache_stats(self._h, *[ctypes.byref(x) for x in v])
+        return dict(zip(("cached", "unreferenced", "hits", "evictions"), (int(x.value) for x in v)))
+
+    def is_cached(self, block: int) -> bool:
+        return self._lib.or_bm_is_cached(self._h, int(block)) == 1
 
     def export_tables(self, seqs: Sequence[int], max_blocks: int) -> np.ndarray:
         """Padded ``int32 [len(seqs), max_blocks]`` tables, pad value -1."""

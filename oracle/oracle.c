@@ -39,6 +39,15 @@
  *     filled tail block whose refcount is above one. [P4 "copies that single
  *     block".]
  *   - Query head h reads KV head h / (Hq / Hk).
+ *   - Prefix caching ("PagedAttention" S06, "What's next": block contents are
+ *     hashed so that requests with a common prefix share physical blocks).
+ *     Only full blocks are cached. A block's key is every token of the
+ *     prompt up to and including the block, so a hit at block j means the
+ *     whole prefix matches. A cached block whose last reference goes away
+ *     stays cached (unreferenced, evictable) rather than returning to the
+ *     free list; an allocation takes the free list first and, only when it
+ *     is empty, evicts the unreferenced cached block released longest ago
+ *     (among blocks released by one call, the deepest first).
  */
 #include <math.h>
 #include <stdint.h>
@@ -83,6 +92,14 @@ typedef struct {
     int num_host_blocks;  /* swap space in host memory (0: none)      */
     int *host_stack;      /* host_stack[host_top - 1] is handed next  */
     int host_top;
+    /* prefix cache, per block */
+    int *cached;          /* 1: the block holds a committed prefix          */
+    int **key;            /* key[b]: tokens 0 .. key_len[b]-1 of that prefix */
+    int *key_len;
+    long long *released;  /* clock of the call that left it unreferenced    */
+    long long clock;
+    long long cache_hits; /* blocks served from the cache                    */
+    long long evictions;
 } or_bm;
 
 static or_seq *find_seq(or_bm *bm, long long id) {
@@ -101,6 +118,60 @@ static int table_push(or_seq *s, int block) {
     }
     s->table[s->nblk++] = block;
     return OR_OK;
+}
+
+/* Blocks an allocation can take: the free list plus every cached block that
+ * no table names. */
+static int available(or_bm *bm) {
+    int n = bm->top;
+    for (int b = 0; b < bm->num_blocks; b++)
+        if (bm->cached[b] && bm->refcount[b] == 0) n++;
+    return n;
+}
+
+static void uncache(or_bm *bm, int b) {
+    free(bm->key[b]);
+    bm->key[b] = NULL;
+    bm->key_len[b] = 0;
+    bm->cached[b] = 0;
+}
+
+/* One block for a table: the top of the free list, else the unreferenced
+ * cached block released longest ago (deepest first on a tie), which leaves
+ * the cache. The caller has checked available(bm) > 0. */
+static int take_block(or_bm *bm) {
+    if (bm->top > 0) return bm->free_stack[--bm->top];
+    int best = -1;
+    for (int b = 0; b < bm->num_blocks; b++) {
+        if (!bm->cached[b] || bm->refcount[b] != 0) continue;
+        if (best < 0 || bm->released[b] < bm->released[best] ||
+            (bm->released[b] == bm->released[best] && bm->key_len[b] > bm->key_len[best]))
+            best = b;
+    }
+    uncache(bm, best);
+    bm->evictions += 1;
+    return best;
+}
+
+/* A table stops naming block b. At zero references an uncached block goes
+ * back on the free list; a cached one stays, stamped with this call's clock. */
+static void release(or_bm *bm, int b) {
+    bm->refcount[b] -= 1;
+    if (bm->refcount[b] == 0) {
+        if (bm->cached[b])
+            bm->released[b] = bm->clock;
+        else
+            bm->free_stack[bm->top++] = b;
+    }
+}
+
+/* The cached block whose key is exactly tokens[0 .. len-1], or -1. */
+static int find_cached(or_bm *bm, const int *tokens, int len) {
+    for (int b = 0; b < bm->num_blocks; b++)
+        if (bm->cached[b] && bm->key_len[b] == len &&
+            memcmp(bm->key[b], tokens, sizeof(int) * (size_t)len) == 0)
+            return b;
+    return -1;
 }
 
 static or_seq *new_seq(or_bm *bm, long long id) {
@@ -128,9 +199,18 @@ or_bm *or_bm_new(int num_blocks, int block_size, const int *alloc_order) {
     bm->block_size = block_size;
     bm->free_stack = (int *)malloc(sizeof(int) * (size_t)num_blocks);
     bm->refcount = (int *)calloc((size_t)num_blocks, sizeof(int));
-    if (!bm->free_stack || !bm->refcount) {
+    bm->cached = (int *)calloc((size_t)num_blocks, sizeof(int));
+    bm->key = (int **)calloc((size_t)num_blocks, sizeof(int *));
+    bm->key_len = (int *)calloc((size_t)num_blocks, sizeof(int));
+    bm->released = (long long *)calloc((size_t)num_blocks, sizeof(long long));
+    if (!bm->free_stack || !bm->refcount || !bm->cached || !bm->key || !bm->key_len ||
+        !bm->released) {
         free(bm->free_stack);
         free(bm->refcount);
+        free(bm->cached);
+        free(bm->key);
+        free(bm->key_len);
+        free(bm->released);
         free(bm);
         return NULL;
     }
@@ -147,8 +227,13 @@ void or_bm_delete(or_bm *bm) {
     if (!bm) return;
     for (int i = 0; i < bm->nseq; i++) free(bm->seqs[i].table);
     free(bm->seqs);
+    for (int b = 0; b < bm->num_blocks; b++) free(bm->key[b]);
     free(bm->free_stack);
     free(bm->refcount);
+    free(bm->cached);
+    free(bm->key);
+    free(bm->key_len);
+    free(bm->released);
     free(bm->host_stack);
     free(bm);
 }
@@ -179,20 +264,20 @@ int or_bm_append(or_bm *bm, long long id, int n, long long *slots_out,
         else if (i == 0 && bm->refcount[s->table[s->nblk - 1]] > 1)
             need++;                                  /* a CoW copy      */
     }
-    if (need > bm->top) return OR_ERR_OUT_OF_BLOCKS;
+    if (need > available(bm)) return OR_ERR_OUT_OF_BLOCKS;
 
     for (int i = 0; i < n; i++) {
         long long offset = s->len % B;
         if (offset == 0) {
             /* [P1] the sequence has outgrown its table: one more block. */
-            int blk = bm->free_stack[--bm->top];
+            int blk = take_block(bm);
             bm->refcount[blk] = 1;
             if (table_push(s, blk) != OR_OK) return OR_ERR_NOMEM;
         } else {
             int tail = s->table[s->nblk - 1];
             if (bm->refcount[tail] > 1) {
                 /* [P1]/[P4] writing into a shared block: take a private copy. */
-                int blk = bm->free_stack[--bm->top];
+                int blk = take_block(bm);
                 bm->refcount[blk] = 1;
                 bm->refcount[tail] -= 1;
                 s->table[s->nblk - 1] = blk;
@@ -235,14 +320,14 @@ int or_bm_fork(or_bm *bm, long long parent, long long child) {
 int or_bm_free_seq(or_bm *bm, long long id) {
     or_seq *s = find_seq(bm, id);
     if (!s) return OR_ERR_UNKNOWN_SEQ;
+    bm->clock += 1;
     for (int j = 0; j < s->nblk; j++) {
         int b = s->table[j];
         if (s->swapped) {            /* host blocks go back to the swap space */
             bm->host_stack[bm->host_top++] = b;
             continue;
         }
-        bm->refcount[b] -= 1;
-        if (bm->refcount[b] == 0) bm->free_stack[bm->top++] = b;
+        release(bm, b);
     }
     free(s->table);
     s->table = NULL;
@@ -278,13 +363,13 @@ int or_bm_swap_out(or_bm *bm, long long id, long long *pairs_out, int *n_out) {
     if (!s) return OR_ERR_UNKNOWN_SEQ;
     if (s->swapped) return OR_ERR_ARG;
     if (s->nblk > bm->host_top) return OR_ERR_OUT_OF_BLOCKS;
+    bm->clock += 1;
     for (int j = 0; j < s->nblk; j++) {
         int d = s->table[j];
         int h = bm->host_stack[--bm->host_top];
         pairs_out[2 * j] = d;
         pairs_out[2 * j + 1] = h;
-        bm->refcount[d] -= 1;
-        if (bm->refcount[d] == 0) bm->free_stack[bm->top++] = d;
+        release(bm, d);
         s->table[j] = h;
     }
     s->swapped = 1;
@@ -301,10 +386,10 @@ int or_bm_swap_in(or_bm *bm, long long id, long long *pairs_out, int *n_out) {
     if (n_out) *n_out = 0;
     if (!s) return OR_ERR_UNKNOWN_SEQ;
     if (!s->swapped) return OR_ERR_ARG;
-    if (s->nblk > bm->top) return OR_ERR_OUT_OF_BLOCKS;
+    if (s->nblk > available(bm)) return OR_ERR_OUT_OF_BLOCKS;
     for (int j = 0; j < s->nblk; j++) {
         int h = s->table[j];
-        int d = bm->free_stack[--bm->top];
+        int d = take_block(bm);
         bm->refcount[d] = 1;
         pairs_out[2 * j] = h;
         pairs_out[2 * j + 1] = d;
@@ -322,6 +407,72 @@ int or_bm_is_swapped(or_bm *bm, long long id) {
 }
 
 int or_bm_host_free(or_bm *bm) { return bm->host_top; }
+
+/* Prefix caching: a new sequence whose prompt is tokens[0 .. n-1] starts
+ * with every leading full block already in the cache. Block j is a hit when
+ * a cached block's key is exactly tokens[0 .. (j+1)B - 1]; the first miss
+ * ends the walk. Each hit is named by the new table (one more reference).
+ * The sequence's length becomes hits * B (*n_cached); the caller appends and
+ * writes the remaining n - *n_cached tokens as usual. */
+int or_bm_add_seq_cached(or_bm *bm, long long id, const int *tokens, int n, int *n_cached) {
+    const int B = bm->block_size;
+    if (n_cached) *n_cached = 0;
+    if (n < 0 || (n > 0 && !tokens)) return OR_ERR_ARG;
+    if (find_seq(bm, id)) return OR_ERR_SEQ_EXISTS;
+    or_seq *s = new_seq(bm, id);
+    if (!s) return OR_ERR_NOMEM;
+    for (int j = 0; (long long)(j + 1) * B <= n; j++) {
+        int b = find_cached(bm, tokens, (j + 1) * B);
+        if (b < 0) break;
+        if (table_push(s, b) != OR_OK) return OR_ERR_NOMEM;
+        bm->refcount[b] += 1;
+        bm->cache_hits += 1;
+    }
+    s->len = (long long)s->nblk * B;
+    if (n_cached) *n_cached = (int)s->len;
+    return OR_OK;
+}
+
+/* Registers the full blocks among the first n tokens of sequence id (its
+ * token ids are tokens[0 .. n-1], n <= its length, their K/V written): block
+ * j gets the key tokens[0 .. (j+1)B - 1] unless it is cached already or
+ * another block already holds that key (the first one stays). */
+int or_bm_commit(or_bm *bm, long long id, const int *tokens, int n) {
+    const int B = bm->block_size;
+    or_seq *s = find_seq(bm, id);
+    if (!s) return OR_ERR_UNKNOWN_SEQ;
+    if (s->swapped || n < 0 || n > s->len || (n > 0 && !tokens)) return OR_ERR_ARG;
+    for (int j = 0; (long long)(j + 1) * B <= n; j++) {
+        int b = s->table[j];
+        int len = (j + 1) * B;
+        if (bm->cached[b] || find_cached(bm, tokens, len) >= 0) continue;
+        bm->key[b] = (int *)malloc(sizeof(int) * (size_t)len);
+        if (!bm->key[b]) return OR_ERR_NOMEM;
+        memcpy(bm->key[b], tokens, sizeof(int) * (size_t)len);
+        bm->key_len[b] = len;
+        bm->cached[b] = 1;
+    }
+    return OR_OK;
+}
+
+/* Cached blocks, of which unreferenced; blocks served from the cache;
+ * cached blocks evicted by allocations. */
+void or_bm_cache_stats(or_bm *bm, long long *cached, long long *unreferenced,
+                       long long *hits, long long *evictions) {
+    long long c = 0, u = 0;
+    for (int b = 0; b < bm->num_blocks; b++) {
+        c += bm->cached[b];
+        u += bm->cached[b] && bm->refcount[b] == 0;
+    }
+    *cached = c;
+    *unreferenced = u;
+    *hits = bm->cache_hits;
+    *evictions = bm->evictions;
+}
+
+int or_bm_is_cached(or_bm *bm, int block) {
+    return (block >= 0 && block < bm->num_blocks) ? bm->cached[block] : -1;
+}
 
 /* Whole-block copies between two pools of the same block shape: block
  * pairs[2p] of `from` goes to block pairs[2p+1] of `to` (K and V). */
@@ -357,7 +508,7 @@ int or_bm_refcount(or_bm *bm, int block) {
     return bm->refcount[block];
 }
 
-int or_bm_num_free(or_bm *bm) { return bm->top; }
+int or_bm_num_free(or_bm *bm) { return available(bm); }
 
 long long or_bm_cow_copies(or_bm *bm) { return bm->cow_copies; }
 

@@ -15,7 +15,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
-PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_block_manager.py"]
+PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_block_manager.py", "tests/test_oracle_prefix_cache.py"]
 
 MUTANTS = {
     "gqa_head_mapping": ("const int kvh = h / G;", "const int kvh = h % Hk;"),
@@ -32,12 +32,24 @@ MUTANTS = {
     "cow_keeps_source_count": ("bm->refcount[tail] -= 1;", ";"),
     "cow_on_private_block": ("if (bm->refcount[tail] > 1) {", "if (bm->refcount[tail] >= 1) {"),
     "fork_without_increment": ("bm->refcount[p->table[j]] += 1;", ";"),
-    "free_ignores_refcount": ("if (bm->refcount[b] == 0) bm->free_stack[bm->top++] = b;",
-                              "bm->free_stack[bm->top++] = b;"),
-    "swap_out_keeps_reference": ("        bm->refcount[d] -= 1;\n        if (bm->refcount[d] == 0) bm->free_stack[bm->top++] = d;\n        s->table[j] = h;",
-                                 "        s->table[j] = h;"),
+    "free_ignores_refcount": ("    bm->refcount[b] -= 1;\n    if (bm->refcount[b] == 0) {",
+                              "    bm->refcount[b] = 0;\n    if (bm->refcount[b] == 0) {"),
+    "swap_out_keeps_reference": ("        release(bm, d);\n        s->table[j] = h;", "        s->table[j] = h;"),
     "swap_in_shares_host_block": ("        bm->host_stack[bm->host_top++] = h;\n        s->table[j] = d;",
                                   "        s->table[j] = d;"),
+    "cache_key_is_block_only": ("memcmp(bm->key[b], tokens, sizeof(int) * (size_t)len) == 0",
+                                "memcmp(bm->key[b] + len - bm->block_size, tokens + len - bm->block_size,"
+                                " sizeof(int) * (size_t)bm->block_size) == 0"),
+    "evict_most_recent": ("bm->released[b] < bm->released[best]", "bm->released[b] > bm->released[best]"),
+    "evict_shallowest_first": ("bm->key_len[b] > bm->key_len[best]", "bm->key_len[b] < bm->key_len[best]"),
+    "no_retention": ("        if (bm->cached[b])\n            bm->released[b] = bm->clock;",
+                     "        if (0)\n            bm->released[b] = bm->clock;"),
+    "hit_without_reference": ("        bm->refcount[b] += 1;\n        bm->cache_hits += 1;",
+                              "        bm->cache_hits += 1;"),
+    "commit_partial_block": ("(long long)(j + 1) * B <= n; j++) {\n        int b = s->table[j];",
+                             "(long long)j * B < n; j++) {\n        int b = s->table[j];"),
+    "evictable_not_available": ("        if (bm->cached[b] && bm->refcount[b] == 0) n++;", ""),
+    "evict_keeps_key": ("    uncache(bm, best);\n", ""),
     "copy_blocks_swapped": ("memcpy((char *)k_cache + (size_t)dst * blk_bytes, (char *)k_cache + (size_t)src * blk_bytes",
                             "memcpy((char *)k_cache + (size_t)src * blk_bytes, (char *)k_cache + (size_t)dst * blk_bytes"),
 }
