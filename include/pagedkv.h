@@ -332,8 +332,10 @@ int32_t pk_bm_num_free(const pk_bm *bm);
 int32_t pk_bm_refcount(const pk_bm *bm, int32_t block); /* -1 if out of range */
 
 /* Recounts every block's references from the tables and checks: counts
- * match, no named block is free, no block is lost or listed twice, and each
- * table holds ceil(len / B) blocks. PK_ERR_INVARIANT on the first violation. */
+ * match, no named block is free, no block is lost or listed twice, each
+ * table holds ceil(len / B) blocks, every cached block is found by its own
+ * key, and named + free + unreferenced cached blocks make up the pool.
+ * PK_ERR_INVARIANT on the first violation. */
 pk_status pk_bm_check_invariants(const pk_bm *bm);
 
 /* Swap space for preemption: num_host_blocks host blocks, handed out first
@@ -359,6 +361,44 @@ pk_status pk_bm_swap_in(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t c
 
 int32_t pk_bm_is_swapped(const pk_bm *bm, int64_t seq_id); /* 1, 0, or -1 if unknown */
 int32_t pk_bm_host_free(const pk_bm *bm);                 /* free swap-space blocks   */
+
+/* Prefix caching ("PagedAttention" S06, "What's next": block contents are
+ * hashed so that any two requests with a common prefix share the same
+ * physical blocks). Only full blocks are cached. A block's key is every token
+ * id of the prompt up to and including the block: a 64-bit hash chained over
+ * the blocks, verified on lookup against the block's depth, its parent's
+ * chain hash and its own B token ids (a false hit needs two different
+ * prefixes with equal 64-bit chain hashes and equal last blocks). A cached
+ * block that loses its last reference stays cached and unreferenced (it still
+ * counts in pk_bm_num_free); allocations take the free list first and then
+ * evict the unreferenced cached block released longest ago (deepest first
+ * among blocks released by one call). Host only: the K/V of a cached block
+ * stay where the first request wrote them. */
+
+/* New sequence whose prompt is tokens[0, n): its table starts with every
+ * leading full block found in the cache (a hit at block j needs all of
+ * tokens[0, (j+1)B) to match; the first miss ends the walk), each named once
+ * more. Its length becomes *n_cached_out = hits * B; the caller appends the
+ * remaining n - *n_cached_out tokens with pk_bm_append_slots and writes their
+ * K/V. A caller that must compute the last prompt token passes n - 1. */
+pk_status pk_bm_add_seq_cached(pk_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t n,
+                               int32_t *n_cached_out);
+
+/* Registers the full blocks among the first n tokens of a sequence (tokens =
+ * its token ids, n <= its length; their K/V written on the stream that later
+ * readers use): block j gets the key of tokens[0, (j+1)B) unless it is cached
+ * already or another block holds that key (the first stays). */
+pk_status pk_bm_commit(pk_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t n);
+
+/* Tokens of tokens[0, n) that pk_bm_add_seq_cached would find cached now. */
+pk_status pk_bm_cache_match(const pk_bm *bm, const int32_t *tokens, int32_t n,
+                            int32_t *n_cached_out);
+
+/* Cached blocks, of which unreferenced; blocks served from the cache since
+ * creation; cached blocks evicted by allocations. NULL outputs are skipped. */
+pk_status pk_bm_cache_stats(const pk_bm *bm, int64_t *cached, int64_t *unreferenced,
+                            int64_t *hits, int64_t *evictions);
+int32_t pk_bm_is_cached(const pk_bm *bm, int32_t block); /* 1, 0, or -1 if out of range */
 
 /* Shared-prefix groups for cascade attention. Sequences of seq_ids[0..n-1]
  * whose tables begin with the same physical block (forks of one parent) are

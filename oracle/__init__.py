@@ -324,6 +324,21 @@ def run_workload(wl, step: int = 0, attention: bool = True, select: Optional[np.
             bm.add_seq(op[1])
         elif op[0] == "fork":
             bm.fork(op[1], op[2])
+        elif op[0] == "free":
+            bm.free_seq(op[1])
+        elif op[0] == "admit":
+            # A request arrives: its prompt's leading full blocks come from the
+            # prefix cache, the rest is written, then its full blocks are registered.
+            r = op[1]
+            toks = wl.chat_tokens(r)
+            n_cached = bm.add_seq_cached(r, toks)
+            if len(toks) > n_cached:
+                slots, _ = bm.append(r, len(toks) - n_cached)
+                prefill_slots.append(slots)
+                if pool:
+                    k, v = wl.chat_kv(r, n_cached, len(toks))
+                    reshape_and_cache(kc, vc, k, v, slots, wl.num_blocks, wl.block_size)
+            bm.commit(r, toks)
         else:
             _, seq, n, src = op
             slots, cow = bm.append(seq, n)

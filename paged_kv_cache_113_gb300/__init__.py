@@ -53,7 +53,8 @@ EXPORTED = (
     "pk_decode_step_meta_bytes", "pk_decode_step",
     "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
     "pk_swap_blocks", "pk_bm_set_swap_space", "pk_bm_swap_out", "pk_bm_swap_in", "pk_bm_is_swapped",
-    "pk_bm_host_free",
+    "pk_bm_host_free", "pk_bm_add_seq_cached", "pk_bm_commit", "pk_bm_cache_match", "pk_bm_cache_stats",
+    "pk_bm_is_cached",
 )
 PK_SWAP_OUT, PK_SWAP_IN = 0, 1
 
@@ -129,6 +130,11 @@ def lib() -> ctypes.CDLL:
         "pk_bm_swap_in": (i32, [P, i64, P, i32, P]),
         "pk_bm_is_swapped": (i32, [P, i64]),
         "pk_bm_host_free": (i32, [P]),
+        "pk_bm_add_seq_cached": (i32, [P, i64, P, i32, P]),
+        "pk_bm_commit": (i32, [P, i64, P, i32]),
+        "pk_bm_cache_match": (i32, [P, P, i32, P]),
+        "pk_bm_cache_stats": (i32, [P, P, P, P, P]),
+        "pk_bm_is_cached": (i32, [P, i32]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
     }
     for name, (res, args) in sigs.items():
@@ -468,6 +474,36 @@ class BlockManager:
 
     def host_free(self) -> int:
         return int(self._L.pk_bm_host_free(self._h))
+
+    # -- prefix caching -------------------------------------------------------
+    def add_seq_cached(self, seq: int, tokens) -> int:
+        """New sequence whose prompt is ``tokens`` (int32 ids); starts with the
+        leading full blocks found in the cache. Returns the cached token count."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(self._L.pk_bm_add_seq_cached(self._h, int(seq), _np_ptr(t) if len(t) else None, len(t),
+                                            ctypes.byref(n)), "pk_bm_add_seq_cached")
+        return int(n.value)
+
+    def commit(self, seq: int, tokens):
+        """Registers the sequence's full blocks among ``tokens`` (its token ids)."""
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(self._L.pk_bm_commit(self._h, int(seq), _np_ptr(t) if len(t) else None, len(t)), "pk_bm_commit")
+
+    def cache_match(self, tokens) -> int:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(self._L.pk_bm_cache_match(self._h, _np_ptr(t) if len(t) else None, len(t), ctypes.byref(n)),
+               "pk_bm_cache_match")
+        return int(n.value)
+
+    def cache_stats(self) -> dict:
+        v = [ctypes.c_int64(0) for _ in range(4)]
+        _check(self._L.pk_bm_cache_stats(self._h, *[ctypes.byref(x) for x in v]), "pk_bm_cache_stats")
+        return dict(zip(("cached", "unreferenced", "hits", "evictions"), (int(x.value) for x in v)))
+
+    def is_cached(self, block: int) -> bool:
+        return int(self._L.pk_bm_is_cached(self._h, int(block))) == 1
 
     def prefix_groups(self, seqs: Sequence[int], max_group_size: int, min_prefix_blocks: int = 1) -> dict:
         """Shared-prefix groups of the batch ``seqs`` (host numpy arrays)."""

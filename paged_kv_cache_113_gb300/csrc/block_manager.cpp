@@ -16,11 +16,21 @@
 //   * Retire: each block of the table loses one reference; those reaching
 //     zero go back to the free list, in table order.
 //   * The free list is a stack whose first pop is alloc_order[0].
-// Appends are all or nothing; a batch append is undone on failure.
+//   * Prefix caching ("PagedAttention" S06, "What's next": block contents are
+//     hashed so that requests with a common prefix share physical blocks):
+//     a full block is registered under a 64-bit hash chained over every token
+//     up to and including it, and verified on lookup against its depth, its
+//     parent's chain hash and its own tokens. A cached block whose last
+//     reference goes away stays cached; allocations take the free list first
+//     and then evict the unreferenced cached block released longest ago,
+//     deepest first among blocks released by one call.
+// Appends are all or nothing (a batch counts the blocks it needs first).
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <set>
+#include <tuple>
 #include <unordered_map>
 #include <vector>
 
@@ -34,12 +44,36 @@ struct Sequence {
   bool swapped = false;
 };
 
-// What one token append changed, so a failed batch can be rolled back.
-struct AppendRecord {
-  int64_t seq;
-  int32_t popped;     // block taken from the free list, or -1
-  int32_t replaced;   // shared tail block given up by CoW, or -1
+// Prefix-cache entry of one block.
+struct CacheEntry {
+  bool cached = false;
+  int32_t depth = 0;             // block index in every table that names it
+  uint64_t chain = 0;            // hash of tokens [0, (depth + 1) * B)
+  uint64_t parent = 0;           // hash of tokens [0, depth * B)
+  std::vector<int32_t> tokens;   // the block's own B tokens
+  int64_t released = 0;          // clock of the call that left it unreferenced
 };
+
+// Chained block hash: the SplitMix64 output function (Steele, Lea and Flood,
+// "Fast splittable pseudorandom number generators", 2014) applied after each
+// token is added in.
+inline uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+inline uint64_t chain_hash(uint64_t parent, const int32_t *tok, int32_t n) {
+  uint64_t h = parent;
+  for (int32_t i = 0; i < n; ++i) h = mix64(h + 0x9e3779b97f4a7c15ull + uint32_t(tok[i]));
+  return h;
+}
+
+constexpr uint64_t kChainSeed = 0x243f6a8885a308d3ull;
+
+// Unreferenced cached blocks in eviction order: oldest release first, then
+// the deepest block, then the lowest id.
+using EvictKey = std::tuple<int64_t, int32_t, int32_t>;
 
 }  // namespace
 
@@ -52,38 +86,88 @@ struct pk_bm {
   int64_t cow_copies = 0;
   int32_t num_host_blocks = 0;           // swap space in host memory
   std::vector<int32_t> host_free;        // back() is handed out next
+  // prefix cache
+  std::vector<CacheEntry> entry;                    // per block
+  std::unordered_multimap<uint64_t, int32_t> index;  // chain hash -> cached block
+  std::set<EvictKey> idle;                          // unreferenced cached blocks
+  int64_t clock = 0;
+  int64_t cache_hits = 0;
+  int64_t evictions = 0;
 
   int64_t blocks_for(int64_t len) const { return (len + block_size - 1) / block_size; }
 
-  // Blocks a single-token append to `s` would take right now.
-  int32_t need_one(const Sequence &s) const {
-    if (s.len % block_size == 0) return 1;
-    return refs[s.table.back()] > 1 ? 1 : 0;
+  // Blocks an allocation can take: the free list plus the idle cached blocks.
+  int64_t available() const { return int64_t(free_stack.size()) + int64_t(idle.size()); }
+
+  EvictKey idle_key(int32_t b) const { return EvictKey(entry[b].released, -entry[b].depth, b); }
+
+  void uncache(int32_t b) {
+    CacheEntry &e = entry[b];
+    auto range = index.equal_range(e.chain);
+    for (auto it = range.first; it != range.second; ++it)
+      if (it->second == b) {
+        index.erase(it);
+        break;
+      }
+    e.cached = false;
+    e.tokens.clear();
+    e.tokens.shrink_to_fit();
   }
 
-  // Appends one token; assumes the free list can cover it.
-  int64_t append_one(int64_t id, Sequence &s, AppendRecord *rec, int64_t *cow_src,
-                     int64_t *cow_dst) {
-    rec->seq = id;
-    rec->popped = -1;
-    rec->replaced = -1;
-    const int64_t off = s.len % block_size;
-    if (off == 0) {
+  // One block for a table (available() > 0 checked by the caller): the top
+  // of the free list, else the first idle cached block, which leaves the cache.
+  int32_t take_block() {
+    if (!free_stack.empty()) {
       const int32_t b = free_stack.back();
       free_stack.pop_back();
+      return b;
+    }
+    const int32_t b = std::get<2>(*idle.begin());
+    idle.erase(idle.begin());
+    uncache(b);
+    ++evictions;
+    return b;
+  }
+
+  // A table stops naming block b.
+  void release(int32_t b) {
+    if (--refs[b] != 0) return;
+    if (entry[b].cached) {
+      entry[b].released = clock;
+      idle.insert(idle_key(b));
+    } else {
+      free_stack.push_back(b);
+    }
+  }
+
+  // The cached block holding the prefix whose last block is tok[0, B) at
+  // `depth`, after a prefix with chain hash `parent`; -1 if none.
+  int32_t find_cached(uint64_t chain, uint64_t parent, int32_t depth, const int32_t *tok) const {
+    auto range = index.equal_range(chain);
+    for (auto it = range.first; it != range.second; ++it) {
+      const CacheEntry &e = entry[it->second];
+      if (e.depth == depth && e.parent == parent &&
+          std::equal(e.tokens.begin(), e.tokens.end(), tok))
+        return it->second;
+    }
+    return -1;
+  }
+
+  // Appends one token (the caller has checked that a block is available if
+  // one is needed). A new block or a CoW copy comes from take_block.
+  int64_t append_one(Sequence &s, int64_t *cow_src, int64_t *cow_dst) {
+    const int64_t off = s.len % block_size;
+    if (off == 0) {
+      const int32_t b = take_block();
       refs[b] = 1;
       s.table.push_back(b);
-      rec->popped = b;
     } else {
       const int32_t tail = s.table.back();
       if (refs[tail] > 1) {
-        const int32_t b = free_stack.back();
-        free_stack.pop_back();
+        const int32_t b = take_block();
         refs[b] = 1;
         refs[tail] -= 1;
         s.table.back() = b;
-        rec->popped = b;
-        rec->replaced = tail;
         ++cow_copies;
         if (cow_src) *cow_src = tail;
         if (cow_dst) *cow_dst = b;
@@ -92,22 +176,6 @@ struct pk_bm {
     const int64_t slot = int64_t(s.table[s.len / block_size]) * block_size + off;
     s.len += 1;
     return slot;
-  }
-
-  // Undoes append_one in reverse order of application.
-  void undo(const AppendRecord &rec) {
-    Sequence &s = seqs[rec.seq];
-    s.len -= 1;
-    if (rec.popped < 0) return;
-    if (rec.replaced >= 0) {
-      s.table.back() = rec.replaced;
-      refs[rec.replaced] += 1;
-      --cow_copies;
-    } else {
-      s.table.pop_back();
-    }
-    refs[rec.popped] = 0;
-    free_stack.push_back(rec.popped);
   }
 };
 
@@ -123,6 +191,7 @@ pk_status pk_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *al
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->refs.assign(num_blocks, 0);
+    bm->entry.resize(num_blocks);
     bm->free_stack.resize(num_blocks);
     std::vector<char> seen(num_blocks, 0);
     for (int32_t i = 0; i < num_blocks; ++i) {
@@ -167,15 +236,14 @@ pk_status pk_bm_append_slots(pk_bm *bm, int64_t seq_id, int32_t n, int64_t *slot
   // first token lands in a shared, partly filled tail.
   const int64_t fresh = bm->blocks_for(s.len + n) - bm->blocks_for(s.len);
   const int64_t cow = (s.len % bm->block_size != 0 && bm->refs[s.table.back()] > 1) ? 1 : 0;
-  if (fresh + cow > int64_t(bm->free_stack.size())) return PK_ERR_OUT_OF_BLOCKS;
+  if (fresh + cow > bm->available()) return PK_ERR_OUT_OF_BLOCKS;
   try {
     s.table.reserve(size_t(bm->blocks_for(s.len + n)));
   } catch (const std::bad_alloc &) {
     return PK_ERR_NOMEM;
   }
   int64_t src = -1, dst = -1;
-  AppendRecord rec;
-  for (int32_t i = 0; i < n; ++i) slots_out[i] = bm->append_one(seq_id, s, &rec, &src, &dst);
+  for (int32_t i = 0; i < n; ++i) slots_out[i] = bm->append_one(s, &src, &dst);
   if (src >= 0) {
     if (cow_pairs_out) {
       cow_pairs_out[0] = src;
@@ -190,33 +258,48 @@ pk_status pk_bm_append_batch(pk_bm *bm, const int64_t *seq_ids, int32_t n, int64
                              int64_t *cow_pairs_out, int32_t *n_cow_out) {
   if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out))) return PK_ERR_INVALID_ARG;
   if (n_cow_out) *n_cow_out = 0;
-  std::vector<AppendRecord> log;
   std::vector<Sequence *> seqp;
+  int64_t need = 0;
   try {
-    log.reserve(n);
     seqp.reserve(n);
+    // Count the blocks the whole batch takes before changing anything: a
+    // token at a block boundary takes one; a token landing in a tail another
+    // table still names takes a CoW copy (siblings earlier in the batch may
+    // already have given that tail up). A sequence's tail is private after
+    // its first token of the batch.
+    std::unordered_map<const Sequence *, int64_t> grown;
+    std::unordered_map<int32_t, int32_t> given_up;
     for (int32_t i = 0; i < n; ++i) {
       auto it = bm->seqs.find(seq_ids[i]);
       if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
-      if (it->second.swapped) return PK_ERR_INVALID_ARG;
-      it->second.table.reserve(size_t(bm->blocks_for(it->second.len + 1)));
-      seqp.push_back(&it->second);
+      Sequence &s = it->second;
+      if (s.swapped) return PK_ERR_INVALID_ARG;
+      seqp.push_back(&s);
+      int64_t &g = grown[&s];
+      if ((s.len + g) % bm->block_size == 0) {
+        ++need;
+      } else if (g == 0) {
+        const int32_t tail = s.table.back();
+        int32_t &gu = given_up[tail];
+        if (bm->refs[tail] - gu > 1) {
+          ++need;
+          ++gu;
+        }
+      }
+      ++g;
+    }
+    for (auto &kv : grown) {
+      Sequence *s = const_cast<Sequence *>(kv.first);
+      s->table.reserve(size_t(bm->blocks_for(s->len + kv.second)));
     }
   } catch (const std::bad_alloc &) {
     return PK_ERR_NOMEM;
   }
+  if (need > bm->available()) return PK_ERR_OUT_OF_BLOCKS;
   int32_t ncow = 0;
   for (int32_t i = 0; i < n; ++i) {
-    Sequence &s = *seqp[i];
-    if (bm->need_one(s) > int32_t(bm->free_stack.size())) {
-      for (auto r = log.rbegin(); r != log.rend(); ++r) bm->undo(*r);
-      if (n_cow_out) *n_cow_out = 0;
-      return PK_ERR_OUT_OF_BLOCKS;
-    }
     int64_t src = -1, dst = -1;
-    AppendRecord rec;
-    slots_out[i] = bm->append_one(seq_ids[i], s, &rec, &src, &dst);
-    log.push_back(rec);
+    slots_out[i] = bm->append_one(*seqp[i], &src, &dst);
     if (src >= 0) {
       if (cow_pairs_out) {
         cow_pairs_out[2 * ncow] = src;
@@ -249,11 +332,12 @@ pk_status pk_bm_free_seq(pk_bm *bm, int64_t seq_id) {
   if (!bm) return PK_ERR_INVALID_ARG;
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  ++bm->clock;
   for (int32_t b : it->second.table) {
     if (it->second.swapped)
       bm->host_free.push_back(b);  // a swapped sequence holds host blocks
-    else if (--bm->refs[b] == 0)
-      bm->free_stack.push_back(b);
+    else
+      bm->release(b);
   }
   bm->seqs.erase(it);
   return PK_OK;
@@ -297,7 +381,7 @@ pk_status pk_bm_export_tables(const pk_bm *bm, const int64_t *seq_ids, int32_t n
   return PK_OK;
 }
 
-int32_t pk_bm_num_free(const pk_bm *bm) { return bm ? int32_t(bm->free_stack.size()) : -1; }
+int32_t pk_bm_num_free(const pk_bm *bm) { return bm ? int32_t(bm->available()) : -1; }
 
 int32_t pk_bm_refcount(const pk_bm *bm, int32_t block) {
   if (!bm || block < 0 || block >= bm->num_blocks) return -1;
@@ -330,15 +414,28 @@ pk_status pk_bm_check_invariants(const pk_bm *bm) {
   if (host_held + int64_t(bm->host_free.size()) != bm->num_host_blocks) return PK_ERR_INVARIANT;
   std::vector<char> is_free(bm->num_blocks, 0);
   for (int32_t b : bm->free_stack) {
-    if (b < 0 || b >= bm->num_blocks || is_free[b] || count[b] != 0) return PK_ERR_INVARIANT;
+    if (b < 0 || b >= bm->num_blocks || is_free[b] || count[b] != 0 || bm->entry[b].cached)
+      return PK_ERR_INVARIANT;
     is_free[b] = 1;
   }
-  int64_t named = 0;
+  int64_t named = 0, cached = 0, idle = 0;
   for (int32_t b = 0; b < bm->num_blocks; ++b) {
     if (count[b] != bm->refs[b]) return PK_ERR_INVARIANT;
     named += count[b] > 0;
+    const CacheEntry &e = bm->entry[b];
+    if (!e.cached) continue;
+    ++cached;
+    if (int32_t(e.tokens.size()) != bm->block_size ||
+        bm->find_cached(e.chain, e.parent, e.depth, e.tokens.data()) != b)
+      return PK_ERR_INVARIANT;
+    if (count[b] == 0) {
+      if (!bm->idle.count(bm->idle_key(b))) return PK_ERR_INVARIANT;
+      ++idle;
+    }
   }
-  if (named + int64_t(bm->free_stack.size()) != bm->num_blocks) return PK_ERR_INVARIANT;
+  if (cached != int64_t(bm->index.size()) || idle != int64_t(bm->idle.size()))
+    return PK_ERR_INVARIANT;
+  if (named + int64_t(bm->free_stack.size()) + idle != bm->num_blocks) return PK_ERR_INVARIANT;
   return PK_OK;
 }
 
@@ -353,8 +450,7 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
   int32_t shared = 0;
   for (int32_t r : bm->refs) shared += r > 1;
   if (live_tokens) *live_tokens = live;
-  if (reserved_slots)
-    *reserved_slots = int64_t(bm->num_blocks - int32_t(bm->free_stack.size())) * bm->block_size;
+  if (reserved_slots) *reserved_slots = (int64_t(bm->num_blocks) - bm->available()) * bm->block_size;
   if (tail_waste) *tail_waste = waste;
   if (shared_blocks) *shared_blocks = shared;
   if (cow_copies) *cow_copies = bm->cow_copies;
@@ -390,13 +486,14 @@ pk_status pk_bm_swap_out(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t 
   const int32_t n = int32_t(s.table.size());
   if (s.swapped || cap < n || (n > 0 && !pairs_out)) return PK_ERR_INVALID_ARG;
   if (n > int32_t(bm->host_free.size())) return PK_ERR_OUT_OF_BLOCKS;
+  ++bm->clock;
   for (int32_t j = 0; j < n; ++j) {
     const int32_t d = s.table[j];
     const int32_t h = bm->host_free.back();
     bm->host_free.pop_back();
     pairs_out[2 * j] = d;
     pairs_out[2 * j + 1] = h;
-    if (--bm->refs[d] == 0) bm->free_stack.push_back(d);
+    bm->release(d);
     s.table[j] = h;
   }
   s.swapped = true;
@@ -413,11 +510,10 @@ pk_status pk_bm_swap_in(pk_bm *bm, int64_t seq_id, int64_t *pairs_out, int32_t c
   Sequence &s = it->second;
   const int32_t n = int32_t(s.table.size());
   if (!s.swapped || cap < n || (n > 0 && !pairs_out)) return PK_ERR_INVALID_ARG;
-  if (n > int32_t(bm->free_stack.size())) return PK_ERR_OUT_OF_BLOCKS;
+  if (n > bm->available()) return PK_ERR_OUT_OF_BLOCKS;
   for (int32_t j = 0; j < n; ++j) {
     const int32_t h = s.table[j];
-    const int32_t d = bm->free_stack.back();
-    bm->free_stack.pop_back();
+    const int32_t d = bm->take_block();
     bm->refs[d] = 1;
     pairs_out[2 * j] = h;
     pairs_out[2 * j + 1] = d;
@@ -436,6 +532,98 @@ int32_t pk_bm_is_swapped(const pk_bm *bm, int64_t seq_id) {
 }
 
 int32_t pk_bm_host_free(const pk_bm *bm) { return bm ? int32_t(bm->host_free.size()) : -1; }
+
+pk_status pk_bm_cache_match(const pk_bm *bm, const int32_t *tokens, int32_t n,
+                            int32_t *n_cached_out) {
+  if (!bm || n < 0 || (n > 0 && !tokens) || !n_cached_out) return PK_ERR_INVALID_ARG;
+  const int32_t B = bm->block_size;
+  uint64_t parent = kChainSeed;
+  int32_t j = 0;
+  for (; int64_t(j + 1) * B <= n; ++j) {
+    const int32_t *tok = tokens + int64_t(j) * B;
+    const uint64_t chain = chain_hash(parent, tok, B);
+    if (bm->find_cached(chain, parent, j, tok) < 0) break;
+    parent = chain;
+  }
+  *n_cached_out = j * B;
+  return PK_OK;
+}
+
+pk_status pk_bm_add_seq_cached(pk_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t n,
+                               int32_t *n_cached_out) {
+  if (!bm || n < 0 || (n > 0 && !tokens)) return PK_ERR_INVALID_ARG;
+  if (n_cached_out) *n_cached_out = 0;
+  if (bm->seqs.count(seq_id)) return PK_ERR_SEQ_EXISTS;
+  const int32_t B = bm->block_size;
+  Sequence s;
+  try {
+    uint64_t parent = kChainSeed;
+    for (int32_t j = 0; int64_t(j + 1) * B <= n; ++j) {
+      const int32_t *tok = tokens + int64_t(j) * B;
+      const uint64_t chain = chain_hash(parent, tok, B);
+      const int32_t b = bm->find_cached(chain, parent, j, tok);
+      if (b < 0) break;
+      s.table.push_back(b);
+      parent = chain;
+    }
+    s.len = int64_t(s.table.size()) * B;
+    bm->seqs.emplace(seq_id, s);
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  for (int32_t b : s.table) {
+    if (bm->refs[b] == 0) bm->idle.erase(bm->idle_key(b));
+    bm->refs[b] += 1;
+  }
+  bm->cache_hits += int64_t(s.table.size());
+  if (n_cached_out) *n_cached_out = int32_t(s.len);
+  return PK_OK;
+}
+
+pk_status pk_bm_commit(pk_bm *bm, int64_t seq_id, const int32_t *tokens, int32_t n) {
+  if (!bm || n < 0 || (n > 0 && !tokens)) return PK_ERR_INVALID_ARG;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
+  const Sequence &s = it->second;
+  if (s.swapped || n > s.len) return PK_ERR_INVALID_ARG;
+  const int32_t B = bm->block_size;
+  uint64_t parent = kChainSeed;
+  try {
+    for (int32_t j = 0; int64_t(j + 1) * B <= n; ++j) {
+      const int32_t *tok = tokens + int64_t(j) * B;
+      const uint64_t chain = chain_hash(parent, tok, B);
+      const int32_t b = s.table[j];
+      if (!bm->entry[b].cached && bm->find_cached(chain, parent, j, tok) < 0) {
+        CacheEntry &e = bm->entry[b];
+        e.tokens.assign(tok, tok + B);
+        e.depth = j;
+        e.chain = chain;
+        e.parent = parent;
+        bm->index.emplace(chain, b);
+        e.cached = true;
+      }
+      parent = chain;
+    }
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  return PK_OK;
+}
+
+pk_status pk_bm_cache_stats(const pk_bm *bm, int64_t *cached, int64_t *unreferenced,
+                            int64_t *hits, int64_t *evictions) {
+  if (!bm) return PK_ERR_INVALID_ARG;
+  if (cached) *cached = int64_t(bm->index.size());
+  if (unreferenced) *unreferenced = int64_t(bm->idle.size());
+  if (hits) *hits = bm->cache_hits;
+  if (evictions) *evictions = bm->evictions;
+  return PK_OK;
+}
+
+int32_t pk_bm_is_cached(const pk_bm *bm, int32_t block) {
+  if (!bm || block < 0 || block >= bm->num_blocks) return -1;
+  return bm->entry[block].cached ? 1 : 0;
+}
 
 pk_status pk_bm_prefix_groups(const pk_bm *bm, const int64_t *seq_ids, int32_t n,
                               int32_t max_group_size, int32_t min_prefix_blocks,

@@ -82,6 +82,8 @@ class DecodeState:
         self.prefill_slots: List[np.ndarray] = []
         self.prefill_pairs: List[tuple] = []
         self.steps_done = 0
+        self.prompt_tokens = 0   # prompt tokens admitted through the prefix cache
+        self.cached_tokens = 0   # of which served by the cache
         self._prefill()
 
     def _prefill(self):
@@ -93,6 +95,21 @@ class DecodeState:
                 self.bm.add_seq(op[1])
             elif op[0] == "fork":
                 self.bm.fork(op[1], op[2])
+            elif op[0] == "free":
+                self.bm.free_seq(op[1])
+            elif op[0] == "admit":
+                r = op[1]
+                toks = wl.chat_tokens(r)
+                n_cached = self.bm.add_seq_cached(r, toks)
+                self.cached_tokens += n_cached
+                self.prompt_tokens += len(toks)
+                if len(toks) > n_cached:
+                    slots, _ = self.bm.append(r, len(toks) - n_cached)
+                    self.prefill_slots.append(slots)
+                    k, v = wl.chat_kv(r, n_cached, len(toks))
+                    pk_reshape_and_cache(to_device(k, wl.dtype, self.device), to_device(v, wl.dtype, self.device),
+                                         torch.from_numpy(slots).to(self.device), self.k_cache, self.v_cache)
+                self.bm.commit(r, toks)
             else:
                 _, seq, n, src = op
                 slots, cow = self.bm.append(seq, n)

@@ -52,6 +52,19 @@ def _replay_both(wl):
         elif op[0] == "fork":
             ours.fork(op[1], op[2])
             ref.fork(op[1], op[2])
+        elif op[0] == "free":
+            ours.free_seq(op[1])
+            ref.free_seq(op[1])
+        elif op[0] == "admit":
+            toks = wl.chat_tokens(op[1])
+            n = ours.add_seq_cached(op[1], toks)
+            assert n == ref.add_seq_cached(op[1], toks)
+            if len(toks) > n:
+                s1, _ = ours.append(op[1], len(toks) - n)
+                s2, _ = ref.append(op[1], len(toks) - n)
+                assert np.array_equal(s1, s2)
+            ours.commit(op[1], toks)
+            ref.commit(op[1], toks)
         else:
             s1, c1 = ours.append(op[1], op[2])
             s2, c2 = ref.append(op[1], op[2])
@@ -82,6 +95,7 @@ def test_block_manager_matches_oracle_on_workloads(L, name, B):
     for b in range(0, wl.num_blocks, max(1, wl.num_blocks // 500)):
         assert ours.refcount(b) == ref.refcount(b)
     ours.check_invariants()
+    assert ours.cache_stats() == ref.cache_stats()
     st = ours.stats()
     assert st["live_tokens"] == int(ctx.sum())
     assert st["cow_copies"] == ref.cow_copies()
@@ -353,3 +367,115 @@ def test_swap_matches_oracle_on_random_operations(L):
             for q in live:
                 assert ours.is_swapped(q) == ref.is_swapped(q)
                 assert np.array_equal(ours.table(q), ref.table(q))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefix_cache_matches_oracle_on_random_traces(L, seed):
+    assert _prefix_cache_trace(seed) > 0     # some batches ran out of blocks
+
+
+def _prefix_cache_trace(seed):
+    """Admissions through the cache, commits, decode appends (single and
+    batched), forks, swaps and retirements in a small pool (so cached blocks
+    are released, revived and evicted): tables, cached counts, free counts
+    and cache statistics equal the oracle's after every operation."""
+    rng = np.random.default_rng(900 + seed)
+    B = int(rng.choice([2, 4, 16]))
+    N = int(rng.integers(16, 64))
+    order = rng.permutation(N).astype(np.int32)
+    ours, ref = pk.BlockManager(N, B, order), oracle.BlockManager(N, B, order)
+    H = 32
+    ours.set_swap_space(H)
+    ref.set_swap_space(H)
+    bases = [list(rng.integers(0, 4, 5 * B)) for _ in range(3)]
+    toks, nid = {}, 0
+
+    log, failures = [], [0]
+
+    def both(name, *args):
+        out = []
+        for bm, err in ((ours, pk.PagedKVError), (ref, oracle.OracleError)):
+            try:
+                out.append(("ok", getattr(bm, name)(*args)))
+            except err:
+                out.append(("err", None))
+        assert out[0][0] == out[1][0], (name, args)
+        if out[1][0] == "ok":
+            log.append((name, args))
+        return out
+
+    for _ in range(250):
+        r = rng.random()
+        live = [s for s in toks if not ref.is_swapped(s)]
+        if r < 0.3 or not live:
+            base = bases[int(rng.integers(3))]
+            prompt = base[: int(rng.integers(0, len(base)))] + list(rng.integers(0, 4, int(rng.integers(1, 2 * B))))
+            assert ours.cache_match(prompt) == ref.add_seq_cached(nid, prompt)
+            log.append(("add_seq_cached", (nid, prompt)))
+            ours.add_seq_cached(nid, prompt)
+            toks[nid] = prompt
+            got = both("append", nid, len(prompt) - ref.seq_len(nid))
+            if got[0][0] == "ok":
+                assert np.array_equal(got[0][1][0], got[1][1][0]) and got[0][1][1] == got[1][1][1]
+                if rng.random() < 0.8:
+                    both("commit", nid, prompt)
+            else:
+                toks[nid] = toks[nid][: ref.seq_len(nid)]
+            nid += 1
+        elif r < 0.5:
+            batch = list(rng.choice(live, size=int(rng.integers(1, len(live) + 1))))
+            before_free = ref.num_free()
+            try:
+                slots, pairs = ours.append_batch(batch)
+            except pk.PagedKVError:
+                # Nothing changed, and one token at a time the oracle runs out too
+                # (on a replica rebuilt from the operation log).
+                assert ours.num_free() == before_free
+                replica = oracle.BlockManager(N, B, order)
+                replica.set_swap_space(H)
+                for name, args in log:
+                    getattr(replica, name)(*args)
+                with pytest.raises(oracle.OracleError):
+                    for s in batch:
+                        replica.append(s, 1)
+                failures[0] += 1
+                continue
+            want, wpairs = [], []
+            for s in batch:
+                sl, cow = ref.append(s, 1)
+                log.append(("append", (s, 1)))
+                want.append(sl[0])
+                if cow is not None:
+                    wpairs.append(cow)
+                toks[s] = toks[s] + [int(rng.integers(0, 4))]
+            assert np.array_equal(slots, want)
+            assert np.array_equal(pairs.reshape(-1, 2), np.array(wpairs, np.int64).reshape(-1, 2))
+        elif r < 0.6:
+            s = int(rng.choice(live))
+            got = both("fork", s, nid)
+            if got[0][0] == "ok":
+                toks[nid] = list(toks[s])
+                nid += 1
+        elif r < 0.7:
+            s = int(rng.choice(live))
+            both("commit", s, toks[s])
+        elif r < 0.8:
+            s = int(rng.choice(list(toks)))
+            name = "swap_in" if ref.is_swapped(s) else "swap_out"
+            got = both(name, s)
+            if got[0][0] == "ok":
+                assert np.array_equal(got[0][1], got[1][1])
+        else:
+            s = int(rng.choice(list(toks)))
+            both("free_seq", s)
+            del toks[s]
+        ours.check_invariants()
+        assert ours.num_free() == ref.num_free()
+        assert ours.cache_stats() == ref.cache_stats()
+        for s in toks:
+            assert ours.is_swapped(s) == ref.is_swapped(s)
+            assert np.array_equal(ours.table(s), ref.table(s))
+        for b in range(N):
+            assert ours.is_cached(b) == ref.is_cached(b)
+    assert ref.cache_stats()["evictions"] > 0 and ref.cache_stats()["hits"] > 0
+    return failures[0]

@@ -95,3 +95,11 @@ def test_cascade_without_groups_is_regular_attention():
     st.attention_cascade(d, out, groups, st.alloc_workspace(d["max_context_len"], -1))
     torch.cuda.synchronize()
     assert_close(from_device(out), ref["out"], "bf16", "no groups")
+
+
+@pytest.mark.parametrize("nseq", [16, 128])
+def test_cascade_chat_requests_sharing_cached_system_prompts(nseq):
+    """Requests that share a cached system prompt (not forks) form cascade groups."""
+    wl = make_workload("chat", num_seqs=nseq)
+    groups = _run(wl, parts=(-1,) if nseq > 16 else (-1, 0, 256))
+    assert groups["max_prefix_len"] >= 512

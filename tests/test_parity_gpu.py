@@ -90,6 +90,7 @@ REDUCED = [
     ("prefix", 8, 8),
     ("prefix", 8, 16),
     ("prefix", 8, 32),
+    ("chat", 12, None),
 ]
 
 
@@ -114,7 +115,8 @@ def _sample_rows(wl, ctx, n=48, seed=0):
     return np.array(sorted(rows), dtype=np.int32)
 
 
-FULL = [("mha7b", None), ("gqa8b", None), ("long", None), ("prefix", 8), ("prefix", 16), ("prefix", 32)]
+FULL = [("mha7b", None), ("gqa8b", None), ("long", None), ("prefix", 8), ("prefix", 16), ("prefix", 32),
+        ("chat", None)]
 
 
 @pytest.mark.slow
@@ -343,3 +345,21 @@ def test_host_side_rejections():
         pk.pk_paged_attention_decode(out.cpu(), d["q"], st.k_cache, st.v_cache, d["tables"], d["ctx_lens"],
                                      wl.scale, d["max_context_len"])
     _no_device_error()
+
+
+def test_chat_prefix_cache_bookkeeping():
+    """Requests admitted through the prefix cache: the cache served the same
+    blocks on both sides, the GPU pool holds the oracle's bits everywhere, and
+    sequences that share a system prompt name the same physical blocks."""
+    wl = make_workload("chat", num_seqs=24)
+    st, d, out, ref = _build_pair(wl)
+    assert st.bm.cache_stats() == ref["bm"].cache_stats()
+    assert st.cached_tokens == ref["bm"].cache_stats()["hits"] * wl.block_size
+    assert st.cached_tokens > 0
+    tables = ref["tables"]
+    for p in range(len(wl.chat_prompt_lens)):
+        members = [s for s in range(wl.num_seqs) if wl.chat_choice[s] == p]
+        full = int(wl.chat_prompt_lens[p]) // wl.block_size
+        if len(members) > 1 and full:
+            assert (tables[members, :full] == tables[members[0], :full]).all()
+    st.bm.check_invariants()

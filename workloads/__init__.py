@@ -21,6 +21,15 @@ Workloads (shapes follow the pages' examples; all data is synthetic):
 * ``prefix`` 32 groups of 4 parallel samples sharing a 2000-token prompt, then
              1..500 divergent tokens each, 32 / 8 heads, head_dim 128, bf16,
              block size 8, 16 or 32, a pool of 524288 slots.
+* ``chat``   a chat server's decode batch: 128 requests, each one of 4 system
+             prompts (1000, 1536, 2000, 600 tokens; popularity 1 : 1/2 : 1/3 :
+             1/4) followed by a lognormal user turn (mean 200, sigma 1, capped
+             at 2000), admitted through a prefix cache after 32 earlier
+             requests that have already finished; 32 / 8 heads, head_dim 128,
+             bf16, 16-token blocks, 32768 blocks. Token ids are drawn from a
+             32000-word vocabulary; the K/V of a system-prompt position depend
+             only on the prompt and the position, those of the user turn on the
+             request.
 
 Every context length is the length *after* the step's new token is appended.
 """
@@ -41,7 +50,7 @@ __all__ = [
     "normal_values",
 ]
 
-WORKLOAD_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix")
+WORKLOAD_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix", "chat")
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -104,6 +113,9 @@ class Workload:
     prefix_groups: int = 0
     prefix_n: int = 0
     prefix_len: int = 0
+    chat_prompt_lens: Optional[np.ndarray] = None  # system prompt lengths (chat)
+    chat_choice: Optional[np.ndarray] = None       # prompt of each request, batch then retired
+    chat_retired: int = 0                          # earlier requests, ids num_seqs ..
     memo: Optional[dict] = dataclasses.field(default=None, repr=False, compare=False)
 
     def enable_memo(self) -> "Workload":
@@ -164,6 +176,45 @@ class Workload:
         if self.memo is not None:
             self.memo[key] = (k, v)
         return k, v
+
+    # ---- chat requests (token ids and their K/V) ----------------------------
+    def chat_user_len(self, req: int) -> int:
+        """Length of request ``req``'s user turn (batch requests end one token
+        before the step token; retired requests have their own draw)."""
+        if req < self.num_seqs:
+            return int(self.ctx_lens[req]) - 1 - int(self.chat_prompt_lens[self.chat_choice[req]])
+        rng = np.random.default_rng([self.seed, 6, req])
+        return int(_lognormal_outputs(rng, 1, 200.0, 1.0, 2000)[0])
+
+    def chat_tokens(self, req: int) -> np.ndarray:
+        """Token ids of request ``req``'s prompt: system prompt, then user turn (int32)."""
+        p = int(self.chat_choice[req])
+        sys_ids = np.random.default_rng([self.seed, 4, p]).integers(0, 32000, int(self.chat_prompt_lens[p]))
+        user = np.random.default_rng([self.seed, 5, req]).integers(0, 32000, self.chat_user_len(req))
+        return np.concatenate([sys_ids, user]).astype(np.int32)
+
+    def chat_kv(self, req: int, start: int, end: int):
+        """K and V ``[end - start, Hk, d]`` of positions [start, end) of request ``req``."""
+        p = int(self.chat_choice[req])
+        S = int(self.chat_prompt_lens[p])
+        shape = (self.num_kv_heads, self.head_dim)
+        key_s, key_u = ("chat_sys", p), ("chat_user", req)
+        if self.memo is not None and key_s in self.memo:
+            ks, vs = self.memo[key_s]
+        else:
+            rng = np.random.default_rng([self.seed, 7, p])
+            ks, vs = normal_values(rng, (S,) + shape, self.dtype), normal_values(rng, (S,) + shape, self.dtype)
+            if self.memo is not None:
+                self.memo[key_s] = (ks, vs)
+        if self.memo is not None and key_u in self.memo:
+            ku, vu = self.memo[key_u]
+        else:
+            n = self.chat_user_len(req)
+            rng = np.random.default_rng([self.seed, 8, req])
+            ku, vu = normal_values(rng, (n,) + shape, self.dtype), normal_values(rng, (n,) + shape, self.dtype)
+            if self.memo is not None:
+                self.memo[key_u] = (ku, vu)
+        return np.concatenate([ks, ku])[start:end], np.concatenate([vs, vu])[start:end]
 
     def step_inputs(self, step: int):
         """Query ``[S, Hq, d]`` and the new token's K, V ``[S, Hk, d]`` of a step."""
@@ -233,6 +284,16 @@ def make_workload(name: str, block_size: Optional[int] = None, num_seqs: Optiona
         div = rng.integers(1, 501, size=groups * n).astype(np.int64)
         wl = Workload("prefix", groups * n, 32, 8, 128, B, "bf16", 524288 // B, plen + div,
                       seed=seed, prefix_groups=groups, prefix_n=n, prefix_len=plen)
+    elif name == "chat":
+        seed = 1136
+        rng = np.random.default_rng([seed, 0])
+        S, retired = 128, 32
+        lens = np.array([1000, 1536, 2000, 600], dtype=np.int64)
+        w = 1.0 / np.arange(1, 5)
+        choice = rng.choice(4, size=S + retired, p=w / w.sum())
+        user = _lognormal_outputs(rng, S, 200.0, 1.0, 2000)
+        wl = Workload("chat", S, 32, 8, 128, 16, "bf16", 32768, lens[choice[:S]] + user + 1, seed=seed,
+                      chat_prompt_lens=lens, chat_choice=choice, chat_retired=retired)
     else:
         raise ValueError(f"unknown workload {name!r}; choose from {WORKLOAD_NAMES}")
     if block_size is not None and name != "prefix":
@@ -242,6 +303,10 @@ def make_workload(name: str, block_size: Optional[int] = None, num_seqs: Optiona
             g = max(1, num_seqs // wl.prefix_n)
             wl.prefix_groups = g
             wl.num_seqs = g * wl.prefix_n
+        elif wl.chat_choice is not None:
+            # keep the retired requests (and their draws) after the shorter batch
+            wl.chat_choice = np.concatenate([wl.chat_choice[: int(num_seqs)], wl.chat_choice[wl.num_seqs:]])
+            wl.num_seqs = int(num_seqs)
         else:
             wl.num_seqs = int(num_seqs)
         wl.ctx_lens = wl.ctx_lens[: wl.num_seqs].copy()
@@ -251,14 +316,25 @@ def make_workload(name: str, block_size: Optional[int] = None, num_seqs: Optiona
 def prefill_plan(wl: Workload) -> List[tuple]:
     """The ordered list of host operations that builds a workload's state.
 
-    Each entry is one of ``("add", seq)``, ``("append", seq, n, source)`` or
-    ``("fork", parent, child)``; ``source`` says where the appended tokens'
-    K/V come from: ``("prefix", group)`` or ``("private", seq)``. After the
-    plan, every sequence holds ``ctx_lens[s] - 1`` tokens; the decode step
-    then appends one more token to each sequence in index order.
+    Each entry is one of ``("add", seq)``, ``("append", seq, n, source)``,
+    ``("fork", parent, child)``, ``("admit", seq)`` or ``("free", seq)``;
+    ``source`` says where the appended tokens' K/V come from: ``("prefix",
+    group)`` or ``("private", seq)``. ``admit`` (chat) is a request arriving
+    with the prompt ``wl.chat_tokens(seq)`` whose K/V are
+    ``wl.chat_kv(seq, ...)``: the consumer admits it through its prefix
+    cache, writes the positions the cache did not cover and registers the
+    prompt's full blocks. After the plan, every batch sequence holds
+    ``ctx_lens[s] - 1`` tokens; the decode step then appends one more token
+    to each sequence in index order.
     """
     ops: List[tuple] = []
-    if wl.prefix_groups:
+    if wl.chat_choice is not None:
+        for r in range(wl.num_seqs, wl.num_seqs + wl.chat_retired):
+            ops.append(("admit", r))
+            ops.append(("free", r))
+        for s in range(wl.num_seqs):
+            ops.append(("admit", s))
+    elif wl.prefix_groups:
         n = wl.prefix_n
         for g in range(wl.prefix_groups):
             parent = g * n
