@@ -10,7 +10,8 @@ contrast between contiguous placement and paged placement:
   "Three ways contiguous reservation loses memory": external fragmentation.
 
 Each request reserves one interval [start, start + n); placement is first fit
-(the lowest free start that fits). Freeing returns the interval.
+(the lowest free start that fits). An interval grows in place by one slot when
+the slot after it is free. Freeing returns the interval.
 """
 from __future__ import annotations
 
@@ -47,6 +48,19 @@ class ContiguousPool:
                 self.extents[rid] = (start, n)
                 return start
         return None
+
+    def grow(self, rid: int) -> bool:
+        """Extends the request's interval by one slot in place (no
+        relocation): succeeds only if the slot right after it is free."""
+        start, n = self.extents[rid]
+        end = start + n
+        if end >= self.num_slots:
+            return False
+        for other, (s2, n2) in self.extents.items():
+            if other != rid and s2 <= end < s2 + n2:
+                return False
+        self.extents[rid] = (start, n + 1)
+        return True
 
     def release(self, rid: int):
         del self.extents[rid]

@@ -15,7 +15,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
-PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_block_manager.py", "tests/test_oracle_prefix_cache.py"]
+PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_block_manager.py", "tests/test_oracle_prefix_cache.py",
+        "tests/test_oracle_allocator_sim.py"]
 
 MUTANTS = {
     "gqa_head_mapping": ("const int kvh = h / G;", "const int kvh = h % Hk;"),
@@ -53,6 +54,62 @@ MUTANTS = {
     "copy_blocks_swapped": ("memcpy((char *)k_cache + (size_t)dst * blk_bytes, (char *)k_cache + (size_t)src * blk_bytes",
                             "memcpy((char *)k_cache + (size_t)src * blk_bytes, (char *)k_cache + (size_t)dst * blk_bytes"),
 }
+
+
+# Mistakes planted in the Python parts of the oracle: (module, old, new).
+PY_MUTANTS = {
+    "last_fit_placement": ("contiguous", "for start, length in self.holes():",
+                           "for start, length in reversed(self.holes()):"),
+    "grow_into_neighbour": ("contiguous", "if other != rid and s2 <= end < s2 + n2:",
+                            "if other != rid and s2 < end < s2 + n2:"),
+    "reserve_prompt_only": ("allocator_sim", 'return req["prompt"] + (req["max_new"] if self.reserve_max else 0)',
+                            'return req["prompt"]'),
+    "failed_growth_not_dropped": ("allocator_sim", "            if drop:\n", "            if False:\n"),
+    "peaks_only_at_admission": ("allocator_sim", "                generated[i] += 1\n                note_peaks()\n",
+                                "                generated[i] += 1\n"),
+    "despite_free_misread": ("allocator_sim", "if alloc.capacity - alloc.reserved() >= 1:",
+                             "if alloc.reserved() >= 1:"),
+    "paged_need_rounds_down": ("allocator_sim", 'need = -(-req["prompt"] // self.B)', 'need = req["prompt"] // self.B'),
+    "free_run_ignores_gaps": ("allocator_sim", "run = run + 1 if prev is not None and b == prev + 1 else 1",
+                              "run = run + 1"),
+    "paged_capacity_in_slots": ("allocator_sim", "self.capacity = self.N * B", "self.capacity = capacity"),
+}
+
+PY_PINS = ["tests/test_oracle_allocator_sim.py", "tests/test_oracle_block_manager.py"]
+
+_BOOT = """
+import importlib.util, sys
+sys.path.insert(0, {root!r})
+import oracle
+spec = importlib.util.spec_from_file_location("oracle.{mod}", {path!r})
+mod = importlib.util.module_from_spec(spec)
+sys.modules["oracle.{mod}"] = mod
+setattr(oracle, "{mod}", mod)
+spec.loader.exec_module(mod)
+import pytest
+sys.exit(pytest.main(["-x", "-q", "-p", "no:cacheprovider", *{pins!r}]))
+"""
+
+
+def _run_py_mutant(name, tmpdir):
+    module, old, new = PY_MUTANTS[name]
+    text = open(os.path.join(ROOT, "oracle", module + ".py")).read()
+    assert text.count(old) == 1, f"{name}: pattern must occur exactly once"
+    path = os.path.join(tmpdir, f"{name}_{module}.py")
+    with open(path, "w") as f:
+        f.write(text.replace(old, new))
+    boot = _BOOT.format(root=ROOT, mod=module, path=path, pins=PY_PINS)
+    r = subprocess.run([sys.executable, "-c", boot], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    return name, r.returncode
+
+
+def test_every_python_mutant_is_caught(tmp_path):
+    names = sorted(PY_MUTANTS)
+    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 2)) as ex:
+        results = dict(ex.map(lambda n: _run_py_mutant(n, str(tmp_path)), names))
+    survivors = [n for n, rc in results.items() if rc == 0]
+    assert not survivors, f"pins did not catch: {survivors}"
+    assert all(rc == 1 for rc in results.values()), results
 
 
 def _run_mutant(name, tmpdir):
