@@ -16,6 +16,7 @@ the kernels and the device->host copy of the output are all inside the timer.
 ``swap`` (after the steps) times preemption by swapping: half the batch's
 blocks to a pinned host pool and back, one pk_swap_blocks launch per
 direction, beside a contiguous copy-engine copy of the same bytes.
+``allocator_sim`` (host) is the allocator policy table on the seeded traces.
 
 Metric: algorithmic K/V bytes read per step (sum over sequences of
 context_len * Hk * head_dim * 2 bytes * 2 for K and V) per second.
@@ -70,6 +71,7 @@ def parse_args(argv=None):
     p.add_argument("--cascade", action="store_true",
                    help="cascade attention: each shared prefix read once per group (prefix workload)")
     p.add_argument("--no-swap", action="store_true", help="skip the swap-out / swap-in bandwidth measurement")
+    p.add_argument("--no-allocator-sim", action="store_true", help="skip the allocator policy table")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -462,6 +464,7 @@ def run_ours(args):
         e2e.pop("_bytes")
 
     prefix_cache = run_prefix_cache(st, wl) if wl.chat_choice is not None else None
+    allocator_sim = None if args.no_allocator_sim else run_allocator_sim()
     swap = None if args.no_swap or groups is not None else run_swap(st, wl, dev)
 
     cpu = None
@@ -504,6 +507,7 @@ def run_ours(args):
             "e2e": e2e,
             "swap": swap,
             "prefix_cache": prefix_cache,
+            "allocator_sim": allocator_sim,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -653,6 +657,37 @@ def run_prefix_cache(st, wl, reps: int = 3) -> dict:
             "host_admission_us_per_request": 1e6 * best / len(toks),
             "host_admission_prompt_tokens_per_s": prompt / best,
             "host_admission": "add_seq_cached + append of the uncached rest + commit, Python binding, best of 3"}
+
+
+def run_allocator_sim(reps: int = 3) -> dict:
+    """The allocator policy table ("The KV Cache Is an Allocator Problem",
+    "What the trace shows") on the seeded traces, from the library's
+    simulator, with its host time per run (best of ``reps``)."""
+    import paged_kv_cache_113_gb300 as pk
+    from workloads import ALLOCATOR_TRACES, allocator_trace
+
+    out = {"rule": "a failed growth drops the request", "traces": {}}
+    for name in ALLOCATOR_TRACES:
+        C, trace = allocator_trace(name)
+        rows = {}
+        for policy, B in (("max_reservation", 0), ("exact_contiguous", 0), ("paged", 4), ("paged", 8),
+                          ("paged", 16)):
+            best = None
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                r = pk.pk_sim_run(trace, C, policy, B, "drop")
+                dt = time.perf_counter() - t0
+                best = dt if best is None else min(best, dt)
+            s = r["summary"]
+            rows[policy if not B else f"paged_b{B}"] = {
+                "rejected": s["rejected"], "rejected_despite_free": s["rejected_despite_free"],
+                "growth_failures": s["growth_failures"],
+                "growth_failures_despite_free": s["growth_failures_despite_free"],
+                "peak_reserved": s["peak_reserved"], "peak_waste": s["peak_waste"], "peak_live": s["peak_live"],
+                "host_ms": 1e3 * best, "host_us_per_step": 1e6 * best / s["num_steps"]}
+        out["traces"][name] = {"capacity_slots": C, "requests": len(trace), "steps": r["summary"]["num_steps"],
+                               "policies": rows}
+    return out
 
 
 def step_kv_bytes(st, wl) -> int:

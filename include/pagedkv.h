@@ -400,6 +400,70 @@ pk_status pk_bm_cache_stats(const pk_bm *bm, int64_t *cached, int64_t *unreferen
                             int64_t *hits, int64_t *evictions);
 int32_t pk_bm_is_cached(const pk_bm *bm, int32_t block); /* 1, 0, or -1 if out of range */
 
+/* The free list, next block to be handed out first: up to cap ids into out,
+ * the list's length into *n_out. Unreferenced cached blocks are not on it. */
+pk_status pk_bm_free_blocks(const pk_bm *bm, int32_t *out, int32_t cap, int32_t *n_out);
+
+/* ------------------------------------------------------------------------ */
+/* Allocator policy simulator                                               */
+/* ------------------------------------------------------------------------ */
+/* "The KV Cache Is an Allocator Problem", section "The experiment": one
+ * deterministic trace of requests replayed against a cache of `capacity`
+ * token slots under one policy. Each step t: (1) every request admitted
+ * before t that has generated fewer than `gen` tokens tries to grow by one
+ * slot, in trace order; a failure drops it (PK_SIM_DROP: its cache is
+ * released) or leaves it to retry next step (PK_SIM_STALL); (2) requests
+ * whose completion step is t release their cache; (3) requests arriving at
+ * t are admitted, in trace order, if their prompt's cache (for maximum
+ * reservation: prompt + max_new slots) can be allocated, else rejected.
+ * Contiguous placement is first fit; the paged policy runs this library's
+ * block manager on floor(capacity / B) blocks handed out 0, 1, 2, ...
+ * Host only; single-threaded; no allocation survives the call. */
+typedef struct {
+    int32_t arrival;     /* step the request arrives, >= 0                   */
+    int32_t prompt;      /* prompt tokens, >= 1                              */
+    int32_t max_new;     /* max_new_tokens (what maximum reservation holds)  */
+    int32_t gen;         /* tokens it generates, 0 <= gen <= max_new         */
+    int32_t completion;  /* step it leaves and releases its cache, > arrival */
+} pk_sim_request;
+
+enum {
+    PK_POLICY_MAX_RESERVATION = 0,
+    PK_POLICY_EXACT_CONTIGUOUS = 1,
+    PK_POLICY_PAGED = 2
+};
+enum { PK_SIM_DROP = 0, PK_SIM_STALL = 1 };
+
+typedef struct {
+    int64_t admitted, rejected;
+    int64_t rejected_despite_free;         /* free capacity >= what was asked */
+    int64_t growth_failures;
+    int64_t growth_failures_despite_free;  /* at least one slot was free      */
+    int64_t dropped, completed;
+    int64_t peak_live, peak_reserved, peak_waste; /* after every allocation    */
+    int64_t capacity;                      /* slots the policy can use        */
+    int32_t num_steps;                     /* samples the run produces        */
+} pk_sim_summary;
+
+/* End-of-step state: live tokens, reserved slots, waste = reserved - live,
+ * free = capacity - reserved, and the largest run of contiguous free slots
+ * (paged: of free blocks with consecutive ids, times B). */
+typedef struct {
+    int32_t step, active;
+    int64_t live, reserved, waste, free_slots, largest_free;
+} pk_sim_sample;
+
+/* Steps a trace spans: 1 + the largest arrival or completion step (-1 on a
+ * bad argument). */
+int32_t pk_sim_num_steps(const pk_sim_request *trace, int32_t n);
+
+/* Runs the trace; fills *summary and samples[0 .. min(max_samples,
+ * num_steps) - 1]. PK_ERR_INVALID_ARG for a malformed trace, policy, rule or
+ * a paged capacity below one block. */
+pk_status pk_sim_run(const pk_sim_request *trace, int32_t n, int32_t capacity, int32_t policy,
+                     int32_t block_size, int32_t rule, pk_sim_summary *summary,
+                     pk_sim_sample *samples, int32_t max_samples);
+
 /* Shared-prefix groups for cascade attention. Sequences of seq_ids[0..n-1]
  * whose tables begin with the same physical block (forks of one parent) are
  * grouped in batch order, in chunks of at most max_group_size; a chunk of two

@@ -54,8 +54,10 @@ EXPORTED = (
     "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
     "pk_swap_blocks", "pk_bm_set_swap_space", "pk_bm_swap_out", "pk_bm_swap_in", "pk_bm_is_swapped",
     "pk_bm_host_free", "pk_bm_add_seq_cached", "pk_bm_commit", "pk_bm_cache_match", "pk_bm_cache_stats",
-    "pk_bm_is_cached",
+    "pk_bm_is_cached", "pk_bm_free_blocks", "pk_sim_num_steps", "pk_sim_run",
 )
+PK_POLICY = {"max_reservation": 0, "exact_contiguous": 1, "paged": 2}
+PK_SIM_RULE = {"drop": 0, "stall": 1}
 PK_SWAP_OUT, PK_SWAP_IN = 0, 1
 
 
@@ -71,6 +73,23 @@ class StepBuffers(ctypes.Structure):
                 ("meta_host", ctypes.c_void_p), ("meta_dev", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
                 ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class SimRequest(ctypes.Structure):
+    _fields_ = [("arrival", ctypes.c_int32), ("prompt", ctypes.c_int32), ("max_new", ctypes.c_int32),
+                ("gen", ctypes.c_int32), ("completion", ctypes.c_int32)]
+
+
+class SimSummary(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "admitted", "rejected", "rejected_despite_free", "growth_failures", "growth_failures_despite_free",
+        "dropped", "completed", "peak_live", "peak_reserved", "peak_waste", "capacity")] + \
+        [("num_steps", ctypes.c_int32)]
+
+
+class SimSample(ctypes.Structure):
+    _fields_ = [("step", ctypes.c_int32), ("active", ctypes.c_int32)] + \
+        [(n, ctypes.c_int64) for n in ("live", "reserved", "waste", "free_slots", "largest_free")]
 
 
 class PagedKVError(RuntimeError):
@@ -135,6 +154,9 @@ def lib() -> ctypes.CDLL:
         "pk_bm_cache_match": (i32, [P, P, i32, P]),
         "pk_bm_cache_stats": (i32, [P, P, P, P, P]),
         "pk_bm_is_cached": (i32, [P, i32]),
+        "pk_bm_free_blocks": (i32, [P, P, i32, P]),
+        "pk_sim_num_steps": (i32, [P, i32]),
+        "pk_sim_run": (i32, [P, i32, i32, i32, i32, i32, ctypes.POINTER(SimSummary), P, i32]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
     }
     for name, (res, args) in sigs.items():
@@ -505,6 +527,14 @@ class BlockManager:
     def is_cached(self, block: int) -> bool:
         return int(self._L.pk_bm_is_cached(self._h, int(block))) == 1
 
+    def free_blocks(self) -> np.ndarray:
+        """The free list, next block to be handed out first."""
+        n = ctypes.c_int32(0)
+        _check(self._L.pk_bm_free_blocks(self._h, None, 0, ctypes.byref(n)), "pk_bm_free_blocks")
+        out = np.empty(max(n.value, 1), np.int32)
+        _check(self._L.pk_bm_free_blocks(self._h, _np_ptr(out), n.value, ctypes.byref(n)), "pk_bm_free_blocks")
+        return out[: n.value]
+
     def prefix_groups(self, seqs: Sequence[int], max_group_size: int, min_prefix_blocks: int = 1) -> dict:
         """Shared-prefix groups of the batch ``seqs`` (host numpy arrays)."""
         ids = np.ascontiguousarray(seqs, dtype=np.int64)
@@ -600,3 +630,27 @@ class DecodeStepper:
         self.launch(stream)
         (_torch().cuda.current_stream() if stream is None else stream).synchronize()
         return self.out_host
+
+
+# ---------------------------------------------------------------------------
+# Allocator policy simulator
+# ---------------------------------------------------------------------------
+def pk_sim_run(trace, capacity: int, policy: str, block_size: int = 0, rule: str = "drop") -> dict:
+    """Replays ``trace`` (dicts with arrival, prompt, max_new, gen, completion)
+    under ``policy`` ("max_reservation", "exact_contiguous", "paged").
+    Returns ``{"summary": dict, "samples": list of dicts}`` (one sample per step)."""
+    L = lib()
+    arr = (SimRequest * max(len(trace), 1))()
+    for k, r in enumerate(trace):
+        arr[k] = SimRequest(int(r["arrival"]), int(r["prompt"]), int(r["max_new"]), int(r["gen"]),
+                            int(r["completion"]))
+    steps = int(L.pk_sim_num_steps(arr, len(trace)))
+    if steps < 0:
+        raise ValueError("malformed trace")
+    samples = (SimSample * max(steps, 1))()
+    summ = SimSummary()
+    _check(L.pk_sim_run(arr, len(trace), int(capacity), PK_POLICY[policy], int(block_size), PK_SIM_RULE[rule],
+                        ctypes.byref(summ), samples, steps), "pk_sim_run")
+    summary = {name: int(getattr(summ, name)) for name, _ in SimSummary._fields_}
+    out = [{name: int(getattr(samples[t], name)) for name, _ in SimSample._fields_} for t in range(steps)]
+    return {"summary": summary, "samples": out}

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libpagedkv.so")
-SOURCES = ["attention.cu", "cache_ops.cu", "block_manager.cpp", "decode_step.cpp"]
+SOURCES = ["attention.cu", "cache_ops.cu", "block_manager.cpp", "decode_step.cpp", "allocator_sim.cpp"]
 HEADERS = [os.path.join(CSRC, "pk_device.cuh"), os.path.join(INCLUDE, "pagedkv.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

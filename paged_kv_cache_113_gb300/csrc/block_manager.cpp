@@ -620,6 +620,15 @@ pk_status pk_bm_cache_stats(const pk_bm *bm, int64_t *cached, int64_t *unreferen
   return PK_OK;
 }
 
+pk_status pk_bm_free_blocks(const pk_bm *bm, int32_t *out, int32_t cap, int32_t *n_out) {
+  if (!bm || cap < 0 || (cap > 0 && !out) || !n_out) return PK_ERR_INVALID_ARG;
+  const int32_t n = int32_t(bm->free_stack.size());
+  const int32_t m = std::min(cap, n);
+  for (int32_t k = 0; k < m; ++k) out[k] = bm->free_stack[size_t(n - 1 - k)];
+  *n_out = n;
+  return PK_OK;
+}
+
 int32_t pk_bm_is_cached(const pk_bm *bm, int32_t block) {
   if (!bm || block < 0 || block >= bm->num_blocks) return -1;
   return bm->entry[block].cached ? 1 : 0;

@@ -479,3 +479,55 @@ def _prefix_cache_trace(seed):
             assert ours.is_cached(b) == ref.is_cached(b)
     assert ref.cache_stats()["evictions"] > 0 and ref.cache_stats()["hits"] > 0
     return failures[0]
+
+
+def _sim_pair(trace, capacity, policy, B, rule):
+    from oracle import allocator_sim
+    ours = pk.pk_sim_run(trace, capacity, policy, B, rule)
+    ref = allocator_sim.simulate(trace, capacity, policy, B, rule)
+    s = dict(ours["summary"])
+    assert s.pop("capacity") == (capacity if policy != "paged" else (capacity // B) * B)
+    assert s.pop("num_steps") == len(ref["samples"])
+    assert s == ref["summary"], (policy, B, rule)
+    got = [dict(x, free=x.pop("free_slots")) for x in ours["samples"]]
+    assert got == ref["samples"], (policy, B, rule)
+    return ours
+
+
+POLICY_GRID = [("max_reservation", 0), ("exact_contiguous", 0), ("paged", 1), ("paged", 4), ("paged", 8),
+               ("paged", 16)]
+
+
+@pytest.mark.parametrize("rule", ["drop", "stall"])
+@pytest.mark.parametrize("seed", range(6))
+def test_allocator_sim_matches_oracle_on_random_traces(L, seed, rule):
+    rng = np.random.default_rng(4000 + seed)
+    C = int(rng.choice([48, 80, 100, 160]))
+    trace = []
+    for _ in range(int(rng.integers(4, 30))):
+        a = int(rng.integers(0, 40))
+        m = int(rng.integers(0, C // 3))
+        g = int(rng.integers(0, m + 1))
+        trace.append(dict(arrival=a, prompt=int(rng.integers(1, C // 4)), max_new=m, gen=g,
+                          completion=a + g + int(rng.integers(1, 4))))
+    for policy, B in POLICY_GRID:
+        _sim_pair(trace, C, policy, B, rule)
+
+
+@pytest.mark.parametrize("name,n", [("tight", None), ("serving", 120)])
+@pytest.mark.parametrize("rule", ["drop", "stall"])
+def test_allocator_sim_matches_oracle_on_workload_traces(L, name, n, rule):
+    from workloads import allocator_trace
+    C, trace = allocator_trace(name, n)
+    for policy, B in POLICY_GRID:
+        _sim_pair(trace, C, policy, B, rule)
+
+
+def test_allocator_sim_rejects_malformed_input(L):
+    good = [dict(arrival=0, prompt=4, max_new=4, gen=2, completion=3)]
+    for bad in ({"prompt": 0}, {"gen": 5}, {"completion": 0}, {"arrival": -1}):
+        with pytest.raises(pk.PagedKVError):
+            pk.pk_sim_run([dict(good[0], **bad)], 16, "exact_contiguous")
+    with pytest.raises(pk.PagedKVError):
+        pk.pk_sim_run(good, 3, "paged", 4)
+    assert pk.pk_sim_run([], 16, "paged", 4)["summary"]["num_steps"] == 1

@@ -48,6 +48,8 @@ __all__ = [
     "f32_to_bf16_bits",
     "bf16_bits_to_f32",
     "normal_values",
+    "allocator_trace",
+    "ALLOCATOR_TRACES",
 ]
 
 WORKLOAD_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix", "chat")
@@ -311,6 +313,49 @@ def make_workload(name: str, block_size: Optional[int] = None, num_seqs: Optiona
             wl.num_seqs = int(num_seqs)
         wl.ctx_lens = wl.ctx_lens[: wl.num_seqs].copy()
     return wl
+
+
+ALLOCATOR_TRACES = ("tight", "serving")
+
+
+def allocator_trace(name: str, num_requests: Optional[int] = None):
+    """A seeded request trace for the allocator policy simulator.
+
+    Returns ``(capacity_slots, requests)``; each request is a dict with
+    ``arrival`` (step), ``prompt``, ``max_new``, ``gen`` (tokens it
+    generates) and ``completion`` (the step after its last token).
+
+    * ``tight``   the pages' 80-slot cache; 14 requests, arrival gaps
+                  U{0..4}, prompts U{4..16}, max_new U{8..24}, gen
+                  U{max_new/2 .. max_new}.
+    * ``serving`` 131072 slots; 2000 requests, Poisson arrivals (1.5 per
+                  step), prompts U{32..512}, max_new 2048, gen lognormal
+                  (mean 200, sigma 1, capped at 2048).
+    ``num_requests`` keeps the first requests (a reduced case) and scales
+    the capacity in proportion.
+    """
+    if name == "tight":
+        rng = np.random.default_rng([1137, 0])
+        n, capacity = 14, 80
+        arrival = np.cumsum(rng.integers(0, 5, n))
+        prompt = rng.integers(4, 17, n)
+        max_new = rng.integers(8, 25, n)
+        gen = np.array([rng.integers(m // 2, m + 1) for m in max_new])
+    elif name == "serving":
+        rng = np.random.default_rng([1138, 0])
+        n, capacity = 2000, 131072
+        arrival = np.cumsum(rng.poisson(1.0 / 1.5, n))
+        prompt = rng.integers(32, 513, n)
+        max_new = np.full(n, 2048)
+        gen = _lognormal_outputs(rng, n, 200.0, 1.0, 2048)
+    else:
+        raise ValueError(f"unknown trace {name!r}; choose from {ALLOCATOR_TRACES}")
+    if num_requests is not None and num_requests < n:
+        capacity = max(1, capacity * int(num_requests) // n)
+        n = int(num_requests)
+    reqs = [dict(arrival=int(arrival[i]), prompt=int(prompt[i]), max_new=int(max_new[i]), gen=int(gen[i]),
+                 completion=int(arrival[i] + gen[i] + 1)) for i in range(n)]
+    return capacity, reqs
 
 
 def prefill_plan(wl: Workload) -> List[tuple]:
