@@ -1001,6 +1001,19 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d)
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Opts the tensor-core kernel into its dynamic shared memory (once).
+template <int D, int BS>
+cudaError_t mma_kernel_ready() {
+  using S = MmaShape<D, BS, kMmaWarps, kMmaStages>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES);
+  });
+  return attr_err;
+}
+
 template <int D, int BS>
 pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t stream) {
   using S = MmaShape<D, BS, kMmaWarps, kMmaStages>;
@@ -1009,13 +1022,7 @@ pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t s
   if (!encode_pool_map(&kmap, p.k_cache, d) || !encode_pool_map(&vmap, p.v_cache, d))
     return PK_ERR_CUDA;
   auto kern = attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    S::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return PK_ERR_CUDA;
+  if (mma_kernel_ready<D, BS>() != cudaSuccess) return PK_ERR_CUDA;
   dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions - p.prefix_slots);
   kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
@@ -1075,6 +1082,55 @@ int sm_count() {
 bool mma_supported(const pk_cache_desc &d, int group) {
   return d.dtype == PK_BF16 && (d.head_dim == 64 || d.head_dim == 128) &&
          (d.block_size == 8 || d.block_size == 16 || d.block_size == 32) && group <= kMaxGroup;
+}
+
+// CTAs of the attention kernel resident on one SM, from the occupancy
+// calculator (queried once per instantiation); without a device, the GB300
+// figures: 3 (head_dim 128) or 4 (head_dim 64) tensor-core CTAs.
+template <int D, int BS>
+int mma_resident_ctas() {
+  using S = MmaShape<D, BS, kMmaWarps, kMmaStages>;
+  static const int n = [] {
+    int v = 0;
+    if (mma_kernel_ready<D, BS>() == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &v, attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>, (kMmaWarps + 1) * 32,
+            S::SMEM_BYTES) == cudaSuccess &&
+        v > 0)
+      return v;
+    cudaGetLastError();
+    return D == 128 ? 3 : 4;
+  }();
+  return n;
+}
+
+template <typename T, int D>
+int simt_resident_ctas() {
+  static const int n = [] {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, attn_simt_kernel<T, D>, 128, 0) ==
+            cudaSuccess &&
+        v > 0)
+      return v;
+    cudaGetLastError();
+    return 8;
+  }();
+  return n;
+}
+
+int resident_ctas(const pk_cache_desc &d, int group) {
+  if (mma_supported(d, group)) {
+    const bool d128 = d.head_dim == 128;
+    switch (d.block_size) {
+      case 8: return d128 ? mma_resident_ctas<128, 8>() : mma_resident_ctas<64, 8>();
+      case 16: return d128 ? mma_resident_ctas<128, 16>() : mma_resident_ctas<64, 16>();
+      default: return d128 ? mma_resident_ctas<128, 32>() : mma_resident_ctas<64, 32>();
+    }
+  }
+  if (d.dtype == PK_F32)
+    return d.head_dim == 128 ? simt_resident_ctas<float, 128>() : simt_resident_ctas<float, 64>();
+  return d.head_dim == 128 ? simt_resident_ctas<__nv_bfloat16, 128>()
+                           : simt_resident_ctas<__nv_bfloat16, 64>();
 }
 
 // Split-K partials (when the partitioning splits).
@@ -1160,17 +1216,19 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
   if (partition_size > 0) return partition_size % B == 0 ? partition_size : -1;
   if (partition_size == 0) return 0;
   if (partition_size != -1) return -1;
-  // Automatic: every partition costs a CTA prologue/epilogue and merge
-  // traffic, so split only when the (sequence, KV head) units cannot fill the
-  // resident CTA slots twice over. Then cut each context into P equal
-  // partitions (multiples of 64 tokens, at least 512) with P chosen so that the
-  // work items fill the slots in four whole waves.
+  // Automatic: fill the resident CTA slots (SMs x CTAs per SM) once. When the
+  // (sequence, KV head) units already fill them, no split: every partition
+  // costs a prologue, an epilogue and merge traffic. Otherwise cut each
+  // context into P = floor(slots / units) equal partitions (multiples of 64
+  // tokens, at least 512), so the work runs as one wave with no tail. On
+  // GB300, 32K-token contexts over 64 units ran at 96.5% of the copy peak
+  // this way (7 partitions, 448 of 456 slots) against 90% in 2.67 waves.
   const int64_t units = int64_t(num_seqs) * desc->num_kv_heads;
-  // Waves are counted in units of two CTAs per SM: on GB300 32K-token
-  // contexts over 64 units ran fastest with 19 partitions (1728 tokens).
-  const int64_t slots = int64_t(sm_count()) * 2;
-  if (units >= 2 * slots || max_context_len <= 512) return 0;
-  const int64_t P = (4 * slots + units - 1) / units;
+  const int64_t slots =
+      int64_t(sm_count()) * resident_ctas(*desc, num_q_heads / desc->num_kv_heads);
+  if (units >= slots || max_context_len <= 512) return 0;
+  const int64_t P = slots / units;
+  if (P < 2) return 0;
   int64_t part = (max_context_len + P - 1) / P;
   part = (part + 63) / 64 * 64;
   if (part < 512) part = 512;

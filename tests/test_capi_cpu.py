@@ -220,11 +220,13 @@ def test_partition_resolution_and_workspace_size(L):
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 512, d) == 512
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 0, d) == 0
     assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, 40, d) == -1      # not a multiple of B
-    # Automatic (152 SMs when no GPU is visible): 64 units of 32K tokens split
-    # into 19 partitions of 1728 tokens (4 waves of 2 CTAs per SM).
-    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 1728
-    assert pk.pk_paged_attention_resolve_partition(2, 16, 32768, -1, d) == 512     # at least 512 tokens
-    assert pk.pk_paged_attention_resolve_partition(64, 64, 2048, -1, d) == 704     # 512 units: 3 partitions
+    # Automatic (no GPU visible: 152 SMs x 3 resident CTAs = 456 slots): 64
+    # units of 32K tokens fill the slots once with 7 partitions of 4736 tokens.
+    assert pk.pk_paged_attention_resolve_partition(8, 64, 32768, -1, d) == 4736
+    assert pk.pk_paged_attention_resolve_partition(2, 16, 32768, -1, d) == 1216    # 16 units: 28 partitions
+    assert pk.pk_paged_attention_resolve_partition(1, 8, 4096, -1, d) == 512       # at least 512 tokens
+    assert pk.pk_paged_attention_resolve_partition(40, 64, 8192, -1, d) == 0       # 320 units: one per slot
+    assert pk.pk_paged_attention_resolve_partition(64, 64, 2048, -1, d) == 0       # 512 units fill the slots
     assert pk.pk_paged_attention_resolve_partition(256, 64, 2048, -1, d) == 0      # 2048 units: whole
     assert pk.pk_paged_attention_resolve_partition(8, 64, 300, -1, d) == 0         # short: no split
     assert pk.pk_paged_attention_resolve_partition(8, 60, 300, -1, d) == -1        # Hq % Hk != 0
