@@ -99,6 +99,24 @@ pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot
                                int32_t num_tokens, void *k_cache, void *v_cache,
                                const pk_cache_desc *desc, void *stream);
 
+/* The slot scatter of one decode step plus its block-table bookkeeping on
+ * device-resident tables ("Paged KV Cache Allocation and the Block Table",
+ * append_token; "The KV Cache Is an Allocator Problem", the physical-address
+ * equation). Token i is the next token of row i: its position is
+ * pos = context_lens[i]; its K/V go to slot_mapping[i] as in
+ * pk_reshape_and_cache; block_tables[i][pos / B] becomes slot_mapping[i] / B
+ * (the block holding the token, whether newly opened or a copy-on-write
+ * replacement) and context_lens[i] becomes pos + 1. block_tables is
+ * [num_tokens, max_blocks_per_seq] int32 and context_lens [num_tokens] int32,
+ * both device memory, updated in place. A row whose pos is outside the table,
+ * or whose slot is not at offset pos mod B of its block, is left unchanged
+ * and recorded (PK_DEVERR_CONTEXT); its K/V are still written. */
+pk_status pk_reshape_and_cache_append(const void *k, const void *v, const int64_t *slot_mapping,
+                                      int32_t num_tokens, void *k_cache, void *v_cache,
+                                      const pk_cache_desc *desc, int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, int32_t *context_lens,
+                                      void *stream);
+
 /* Copy-on-write block copy: for each pair p, the whole block src = pairs[2p]
  * is copied to dst = pairs[2p+1] in both k_cache and v_cache (all B slots, all
  * heads). ("paged attention deep", "Copy-on-write for shared prefixes": the
@@ -511,31 +529,41 @@ typedef struct {
     void *out_host;      /* [S, Hq, d] its host copy                            */
     void *workspace;     /* split-K workspace (see pk_paged_attention_decode)   */
     size_t workspace_bytes;
+    /* In: nonzero when meta_dev already holds these sequences' block tables
+     * and context lengths as left by the previous successful pk_decode_step
+     * with the same seq_ids, max_blocks_per_seq and buffers, and the block
+     * manager has not touched them since (no fork, free, swap or append
+     * outside pk_decode_step). Out: 1 after a successful call, 0 otherwise.
+     * Set it to 0 whenever that does not hold. */
+    int32_t tables_resident;
 } pk_step_buffers;
 
 /* Bytes of pk_step_buffers.meta_host / meta_dev for S sequences and tables of
  * max_blocks_per_seq entries (0 for non-positive arguments). */
 size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
 
-/* One decode step of the whole path for the sequences seq_ids[0..S-1] (host):
- *   1. host: append one token to each sequence (pk_bm_append_batch), export
- *      the padded tables and lengths, order the sequences longest first --
- *      all into meta_host;
- *   2. copies host -> device: q, k, v from the caller's host buffers and the
- *      metadata in one transfer;
- *   3. device: pk_copy_blocks for the step's copy-on-write pairs, the slot
- *      scatter of k/v, the attention (automatic kernel, the given
+/* One decode step of the whole path for the distinct sequences
+ * seq_ids[0..S-1] (host):
+ *   1. copies host -> device of q, k, v from the caller's host buffers;
+ *   2. host: append one token to each sequence (pk_bm_append_batch); unless
+ *      buffers->tables_resident, export the padded tables and lengths and
+ *      order the sequences longest first -- into meta_host;
+ *   3. copy host -> device of the metadata in one transfer (resident mode:
+ *      only the slots and copy-on-write pairs);
+ *   4. device: pk_copy_blocks for the step's pairs, the slot scatter of k/v
+ *      (resident mode: pk_reshape_and_cache_append, which also advances the
+ *      device tables and lengths), the attention (automatic kernel, the given
  *      partition_size, the launch order);
- *   4. copy device -> host of the output into out_host.
+ *   5. copy device -> host of the output into out_host.
  * All work is enqueued on `stream`; out_host holds the result once the stream
- * is synchronised, and meta_host must not be reused before then. The paper has
- * no counterpart for this packaging; each step it performs is the pages'
- * (see the entry points above). On an error after step 1 the block manager
- * keeps the appended tokens. */
+ * is synchronised, and meta_host must not be reused before then. The pages
+ * have no counterpart for this packaging; each step it performs is theirs
+ * (see the entry points above). On an error after step 2 the block manager
+ * keeps the appended tokens and tables_resident is 0. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,
-                         const pk_step_buffers *buffers, void *stream);
+                         pk_step_buffers *buffers, void *stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ from ._build import LIB_PATH, build
 
 __all__ = [
     "build", "lib", "PagedKVError", "CacheDesc", "cache_desc",
-    "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
+    "pk_reshape_and_cache", "pk_reshape_and_cache_append", "pk_copy_blocks", "pk_paged_attention_decode",
     "pk_paged_attention_workspace_size", "pk_paged_attention_resolve_partition",
     "pk_get_device_error", "pk_status_string", "BlockManager",
     "PK_F32", "PK_BF16", "IMPLS", "DEVERR_NAMES",
@@ -43,7 +43,7 @@ DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5:
 
 # Every symbol include/pagedkv.h declares.
 EXPORTED = (
-    "pk_reshape_and_cache", "pk_copy_blocks", "pk_paged_attention_decode",
+    "pk_reshape_and_cache", "pk_reshape_and_cache_append", "pk_copy_blocks", "pk_paged_attention_decode",
     "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static",
     "pk_paged_attention_resolve_partition",
     "pk_paged_attention_workspace_size", "pk_longest_first_order", "pk_get_device_error", "pk_status_string",
@@ -72,7 +72,8 @@ class StepBuffers(ctypes.Structure):
                 ("q_dev", ctypes.c_void_p), ("k_dev", ctypes.c_void_p), ("v_dev", ctypes.c_void_p),
                 ("meta_host", ctypes.c_void_p), ("meta_dev", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
                 ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("tables_resident", ctypes.c_int32)]
 
 
 class SimRequest(ctypes.Structure):
@@ -114,6 +115,7 @@ def lib() -> ctypes.CDLL:
     D = ctypes.POINTER(CacheDesc)
     sigs = {
         "pk_reshape_and_cache": (i32, [P, P, P, i32, P, P, D, P]),
+        "pk_reshape_and_cache_append": (i32, [P, P, P, i32, P, P, D, P, i32, P, P]),
         "pk_copy_blocks": (i32, [P, P, P, i32, D, P]),
         "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D, P]),
         "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
@@ -233,6 +235,24 @@ def pk_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, stream=None):
     _check(lib().pk_reshape_and_cache(_dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping", torch.int64),
                                       T, _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                                       ctypes.byref(desc), _stream(stream)), "pk_reshape_and_cache")
+
+
+def pk_reshape_and_cache_append(k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, stream=None):
+    """Scatter of one decode step plus the device-side table update: row i's
+    next token goes to ``slot_mapping[i]``, ``block_tables[i][ctx/B]`` becomes
+    ``slot/B`` and ``context_lens[i]`` grows by one (int32 CUDA tensors)."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    T = int(k.shape[0])
+    if slot_mapping.dtype != torch.int64 or block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("slot_mapping int64, block_tables and context_lens int32")
+    if block_tables.shape[0] != T or context_lens.shape[0] != T or not block_tables.is_contiguous():
+        raise ValueError("block_tables [T, max_blocks] and context_lens [T]")
+    _check(lib().pk_reshape_and_cache_append(_dev(k, "k"), _dev(v, "v"), _dev(slot_mapping, "slot_mapping"), T,
+                                             _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                             _dev(block_tables, "block_tables"), int(block_tables.shape[1]),
+                                             _dev(context_lens, "context_lens"), _stream(stream)),
+           "pk_reshape_and_cache_append")
 
 
 def pk_copy_blocks(k_cache, v_cache, src_dst_pairs, stream=None):
@@ -575,10 +595,11 @@ class DecodeStepper:
     """Runs whole decode steps from pinned host buffers through pk_decode_step.
 
     Owns the pinned host staging (queries, new K/V, metadata, output) and the
-    device buffers of one batch shape. ``step(q, k, v)`` copies the step's
-    host arrays into the pinned staging, calls pk_decode_step (host append,
-    one metadata transfer, the kernels, the output copy) and synchronises;
-    the output is then in ``out_host``.
+    device buffers of one batch shape. ``step()`` calls pk_decode_step (host
+    append, one metadata transfer, the kernels, the output copy) and
+    synchronises; the output is then in ``out_host``. After the first step the
+    block tables stay resident on the device and each step uploads only its
+    slots and copy-on-write pairs; ``invalidate()`` forces a full upload.
     """
 
     def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
@@ -611,8 +632,13 @@ class DecodeStepper:
             self.meta_host.data_ptr(), self.meta_dev.data_ptr(), mb,
             self.out_dev.data_ptr(), self.out_host.data_ptr(),
             None if self.workspace is None else self.workspace.data_ptr(), wsb)
-        self.h2d_bytes = (self.q_host.numel() + self.k_host.numel() + self.v_host.numel()) * \
-            self.q_host.element_size() + mb
+        qkv = (self.q_host.numel() + self.k_host.numel() + self.v_host.numel()) * self.q_host.element_size()
+        # Host -> device bytes of a step: the whole metadata buffer on a full
+        # upload; only the slot section (plus 16 bytes per copy-on-write pair)
+        # once the tables are resident.
+        self.h2d_bytes_full = qkv + mb
+        self.h2d_bytes_resident = qkv + (8 * S + 255) // 256 * 256
+        self.h2d_bytes = self.h2d_bytes_full
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
 
     def launch(self, stream=None, q_host=None, k_host=None, v_host=None):
@@ -624,6 +650,11 @@ class DecodeStepper:
                                     self.partition, ctypes.c_void_p(self.k_cache.data_ptr()),
                                     ctypes.c_void_p(self.v_cache.data_ptr()), ctypes.byref(self.desc),
                                     ctypes.byref(self.buffers), _stream(stream)), "pk_decode_step")
+
+    def invalidate(self):
+        """The next step exports and uploads the whole tables again (call it
+        after any block-manager change outside the stepper: fork, free, swap)."""
+        self.buffers.tables_resident = 0
 
     def step(self, stream=None):
         """One step and a stream synchronise; returns the host output tensor."""

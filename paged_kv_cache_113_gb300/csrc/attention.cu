@@ -987,7 +987,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // A [N*B, Hk, D] bf16 view of one pool; each load is a box of B token rows of
 // one head and 64 elements (128 bytes), swizzled 128B in shared memory.
-bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d) {
+bool encode_pool_map_uncached(CUtensorMap *map, const void *pool, const pk_cache_desc &d) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {cuuint64_t(d.head_dim), cuuint64_t(d.num_kv_heads),
@@ -1002,6 +1002,43 @@ bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d)
 }
 
 // Opts the tensor-core kernel into its dynamic shared memory (once).
+// The pool's tensor map, encoded once per (pool address, geometry): a decode
+// loop launches on the same two pools every step. A few entries cover the K
+// and V pools of the layers a thread drives in turn.
+bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d) {
+  struct Entry {
+    const void *pool;
+    pk_cache_desc desc;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  static std::mutex mu;
+  static Entry cache[kEntries];
+  static int used = 0, next = 0;
+  auto same = [&](const Entry &e) {
+    return e.pool == pool && e.desc.num_blocks == d.num_blocks && e.desc.block_size == d.block_size &&
+           e.desc.num_kv_heads == d.num_kv_heads && e.desc.head_dim == d.head_dim &&
+           e.desc.dtype == d.dtype;
+  };
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (same(cache[i])) {
+        *map = cache[i].map;
+        return true;
+      }
+  }
+  if (!encode_pool_map_uncached(map, pool, d)) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry &e = cache[next];
+  e.pool = pool;
+  e.desc = d;
+  e.map = *map;
+  next = (next + 1) % kEntries;
+  used = used < kEntries ? used + 1 : used;
+  return true;
+}
+
 template <int D, int BS>
 cudaError_t mma_kernel_ready() {
   using S = MmaShape<D, BS, kMmaWarps, kMmaStages>;

@@ -42,7 +42,16 @@ struct Sequence {
   int64_t len = 0;
   std::vector<int32_t> table;  // device block ids, or host block ids when swapped
   bool swapped = false;
+  uint64_t batch_mark = 0;     // batch call that last counted this sequence
+  int64_t batch_grown = 0;     // tokens that call counted for it so far
 };
+
+// Room for `blocks` table entries, growing geometrically (an exact reserve
+// would reallocate the table every time it gains a block).
+inline void reserve_table(std::vector<int32_t> &t, int64_t blocks) {
+  if (int64_t(t.capacity()) < blocks)
+    t.reserve(size_t(std::max<int64_t>(blocks, 2 * int64_t(t.capacity()))));
+}
 
 // Prefix-cache entry of one block.
 struct CacheEntry {
@@ -93,6 +102,11 @@ struct pk_bm {
   int64_t clock = 0;
   int64_t cache_hits = 0;
   int64_t evictions = 0;
+  // batch pre-count: per-call marks instead of per-call maps
+  uint64_t batch_epoch = 0;
+  std::vector<uint64_t> given_up_mark;   // per block: call that last counted a CoW of it
+  std::vector<int32_t> given_up;         // CoW copies of the block that call counted
+  std::vector<Sequence *> batch_seqs;    // scratch of pk_bm_append_batch
 
   int64_t blocks_for(int64_t len) const { return (len + block_size - 1) / block_size; }
 
@@ -192,6 +206,8 @@ pk_status pk_bm_create(int32_t num_blocks, int32_t block_size, const int32_t *al
     bm->block_size = block_size;
     bm->refs.assign(num_blocks, 0);
     bm->entry.resize(num_blocks);
+    bm->given_up_mark.assign(num_blocks, 0);
+    bm->given_up.assign(num_blocks, 0);
     bm->free_stack.resize(num_blocks);
     std::vector<char> seen(num_blocks, 0);
     for (int32_t i = 0; i < num_blocks; ++i) {
@@ -238,7 +254,7 @@ pk_status pk_bm_append_slots(pk_bm *bm, int64_t seq_id, int32_t n, int64_t *slot
   const int64_t cow = (s.len % bm->block_size != 0 && bm->refs[s.table.back()] > 1) ? 1 : 0;
   if (fresh + cow > bm->available()) return PK_ERR_OUT_OF_BLOCKS;
   try {
-    s.table.reserve(size_t(bm->blocks_for(s.len + n)));
+    reserve_table(s.table, bm->blocks_for(s.len + n));
   } catch (const std::bad_alloc &) {
     return PK_ERR_NOMEM;
   }
@@ -258,39 +274,42 @@ pk_status pk_bm_append_batch(pk_bm *bm, const int64_t *seq_ids, int32_t n, int64
                              int64_t *cow_pairs_out, int32_t *n_cow_out) {
   if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out))) return PK_ERR_INVALID_ARG;
   if (n_cow_out) *n_cow_out = 0;
-  std::vector<Sequence *> seqp;
+  std::vector<Sequence *> &seqp = bm->batch_seqs;
   int64_t need = 0;
   try {
+    seqp.clear();
     seqp.reserve(n);
     // Count the blocks the whole batch takes before changing anything: a
     // token at a block boundary takes one; a token landing in a tail another
     // table still names takes a CoW copy (siblings earlier in the batch may
     // already have given that tail up). A sequence's tail is private after
     // its first token of the batch.
-    std::unordered_map<const Sequence *, int64_t> grown;
-    std::unordered_map<int32_t, int32_t> given_up;
+    const uint64_t ep = ++bm->batch_epoch;
     for (int32_t i = 0; i < n; ++i) {
       auto it = bm->seqs.find(seq_ids[i]);
       if (it == bm->seqs.end()) return PK_ERR_UNKNOWN_SEQ;
       Sequence &s = it->second;
       if (s.swapped) return PK_ERR_INVALID_ARG;
       seqp.push_back(&s);
-      int64_t &g = grown[&s];
-      if ((s.len + g) % bm->block_size == 0) {
+      if (s.batch_mark != ep) {
+        s.batch_mark = ep;
+        s.batch_grown = 0;
+      }
+      if ((s.len + s.batch_grown) % bm->block_size == 0) {
         ++need;
-      } else if (g == 0) {
+      } else if (s.batch_grown == 0) {
         const int32_t tail = s.table.back();
-        int32_t &gu = given_up[tail];
-        if (bm->refs[tail] - gu > 1) {
+        if (bm->given_up_mark[tail] != ep) {
+          bm->given_up_mark[tail] = ep;
+          bm->given_up[tail] = 0;
+        }
+        if (bm->refs[tail] - bm->given_up[tail] > 1) {
           ++need;
-          ++gu;
+          ++bm->given_up[tail];
         }
       }
-      ++g;
-    }
-    for (auto &kv : grown) {
-      Sequence *s = const_cast<Sequence *>(kv.first);
-      s->table.reserve(size_t(bm->blocks_for(s->len + kv.second)));
+      ++s.batch_grown;
+      reserve_table(s.table, bm->blocks_for(s.len + s.batch_grown));
     }
   } catch (const std::bad_alloc &) {
     return PK_ERR_NOMEM;

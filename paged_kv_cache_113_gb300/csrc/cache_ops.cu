@@ -20,10 +20,22 @@ __device__ int g_cache_ops_error;
 // Table", append_token: the token is written at physical * block_size +
 // slot). Each thread moves one 16-byte vector of K and one of V, so a whole
 // step's scatter is a single round trip to memory.
+//
+// With UPDATE, token i is the next token of row i of device-resident block
+// tables and context lengths, and the kernel also does that row's share of
+// the step's bookkeeping: the entry of the block holding position
+// pos = context_lens[i] becomes slot / B (a freshly opened block and a
+// copy-on-write replacement alike: the new token's slot names the tail block),
+// and context_lens[i] becomes pos + 1. A slot whose offset in its block is not
+// pos mod B means the resident tables are out of step with the host: the row
+// is left unchanged and the event is recorded (the K/V row is still written
+// to its slot, which was checked against the pool).
+template <bool UPDATE>
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
-    int32_t row_vecs) {
+    int32_t row_vecs, int32_t *__restrict__ tables, int32_t *__restrict__ lens,
+    int32_t max_blocks, int32_t block_size) {
   const int64_t i = blockIdx.x;
   const int32_t j = int32_t(blockIdx.y) * blockDim.x + threadIdx.x;
   const int64_t s = slots[i];
@@ -31,6 +43,16 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
   if (s >= num_slots) {
     if (threadIdx.x == 0 && blockIdx.y == 0) pk::record_error(&g_cache_ops_error, PK_DEVERR_SLOT, i);
     return;
+  }
+  if (UPDATE && blockIdx.y == 0 && threadIdx.x == 0) {
+    // One thread per token reads and advances the row's length.
+    const int32_t pos = lens[i];
+    if (pos < 0 || pos >= max_blocks * block_size || s % block_size != pos % block_size) {
+      pk::record_error(&g_cache_ops_error, PK_DEVERR_CONTEXT, i);
+    } else {
+      tables[i * max_blocks + pos / block_size] = int32_t(s / block_size);
+      lens[i] = pos + 1;
+    }
   }
   if (j >= row_vecs) return;
   const uint4 a = __ldg(k + i * row_vecs + j);
@@ -155,11 +177,38 @@ pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot
   const int64_t row_vecs = row_bytes / 16;
   const int64_t chunks = (row_vecs + 127) / 128;
   if (chunks > 65535) return PK_ERR_UNSUPPORTED;
-  reshape_and_cache_kernel<<<dim3(num_tokens, unsigned(chunks)), 128, 0,
-                             static_cast<cudaStream_t>(stream)>>>(
+  reshape_and_cache_kernel<false><<<dim3(num_tokens, unsigned(chunks)), 128, 0,
+                                    static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
-      int32_t(row_vecs));
+      int32_t(row_vecs), nullptr, nullptr, 0, desc->block_size);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+pk_status pk_reshape_and_cache_append(const void *k, const void *v, const int64_t *slot_mapping,
+                                      int32_t num_tokens, void *k_cache, void *v_cache,
+                                      const pk_cache_desc *desc, int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, int32_t *context_lens,
+                                      void *stream) {
+  pk_status st = check_desc(desc);
+  if (st != PK_OK) return st;
+  if (num_tokens < 0 || max_blocks_per_seq <= 0) return PK_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PK_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PK_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PK_ERR_INVALID_ARG;
+  if (int64_t(max_blocks_per_seq) * desc->block_size > INT32_MAX) return PK_ERR_UNSUPPORTED;
+  const int64_t row_bytes = int64_t(desc->num_kv_heads) * desc->head_dim * elem_size(desc->dtype);
+  const int64_t num_slots = int64_t(desc->num_blocks) * desc->block_size;
+  const int64_t row_vecs = row_bytes / 16;
+  const int64_t chunks = (row_vecs + 127) / 128;
+  if (chunks > 65535) return PK_ERR_UNSUPPORTED;
+  reshape_and_cache_kernel<true><<<dim3(num_tokens, unsigned(chunks)), 128, 0,
+                                   static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
+      int32_t(row_vecs), block_tables, context_lens, max_blocks_per_seq, desc->block_size);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 

@@ -1,11 +1,15 @@
-// One decode step from host buffers, in native code: the host block manager
-// appends a token to every sequence, the step's metadata (slots, copy-on-write
-// pairs, padded block tables, context lengths, launch order) is packed into
-// one pinned staging buffer and copied to the device with a single transfer,
-// the new tokens' K/V and the queries are copied from the caller's host
-// buffers, then copy_blocks (when pairs exist), the slot scatter and the
-// attention run, and the output is copied back to host memory. Everything is
-// enqueued on one stream; the call returns once the work is enqueued.
+// One decode step from host buffers, in native code. The step's new K/V and
+// queries are copied from the caller's host buffers first, so the copies run
+// while the host block manager appends a token to every sequence. The step's
+// metadata is packed into one pinned staging buffer and copied with a single
+// transfer: in full mode slots, copy-on-write pairs, launch order, context
+// lengths and padded block tables; in resident mode (the device already holds
+// this batch's tables and lengths) only slots and pairs -- the scatter kernel
+// then advances the device tables and lengths itself, and the launch order
+// (longest first) is unchanged because every sequence grew by one token. Then
+// copy_blocks (when pairs exist), the scatter and the attention run, and the
+// output is copied back to host memory. Everything is enqueued on one stream;
+// the call returns once the work is enqueued.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -21,8 +25,10 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// What changes every step comes first, so a resident-mode step copies one
+// short prefix of the buffer.
 struct MetaLayout {
-  size_t slots, pairs, tables, lens, order, total;
+  size_t slots, pairs, order, lens, tables, total;
 };
 
 MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
@@ -32,12 +38,12 @@ MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
   off = align_up(off + size_t(num_seqs) * sizeof(int64_t));
   m.pairs = off;
   off = align_up(off + size_t(num_seqs) * 2 * sizeof(int64_t));
-  m.tables = off;
-  off = align_up(off + size_t(num_seqs) * size_t(max_blocks) * sizeof(int32_t));
-  m.lens = off;
-  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
   m.order = off;
   off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
+  m.lens = off;
+  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
+  m.tables = off;
+  off = align_up(off + size_t(num_seqs) * size_t(max_blocks) * sizeof(int32_t));
   m.total = off;
   return m;
 }
@@ -56,7 +62,7 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq) {
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,
-                         const pk_step_buffers *b, void *stream) {
+                         pk_step_buffers *b, void *stream) {
   if (!bm || !desc || !b || num_seqs <= 0 || !seq_ids || max_blocks_per_seq <= 0)
     return PK_ERR_INVALID_ARG;
   const int64_t esz = elem_size(desc->dtype);
@@ -74,25 +80,40 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   int32_t *tables = reinterpret_cast<int32_t *>(mh + m.tables);
   int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
   int32_t *order = reinterpret_cast<int32_t *>(mh + m.order);
+  const bool resident = b->tables_resident != 0;
+  // Resident mode keeps the previous step's lengths in meta_host; every row
+  // must have room for one more token.
+  if (resident)
+    for (int32_t i = 0; i < num_seqs; ++i)
+      if (int64_t(lens[i]) + 1 > int64_t(max_blocks_per_seq) * desc->block_size)
+        return PK_ERR_INVALID_ARG;
+
+  // The step's tensors from the caller's host buffers: enqueued first, so
+  // the copies overlap the host block-manager work below.
+  const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
+  const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
+  if (cudaMemcpyAsync(b->q_dev, b->q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(b->k_dev, b->k_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(b->v_dev, b->v_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return PK_ERR_CUDA;
 
   // Host side of the step.
   int32_t npairs = 0;
   pk_status st = pk_bm_append_batch(bm, seq_ids, num_seqs, slots, pairs, &npairs);
   if (st != PK_OK) return st;
-  st = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
-  if (st != PK_OK) return st;
-  st = pk_longest_first_order(lens, num_seqs, order);
-  if (st != PK_OK) return st;
+  b->tables_resident = 0;  // until this step's metadata is on its way
+  size_t meta_copy = m.total;
+  if (resident) {
+    for (int32_t i = 0; i < num_seqs; ++i) lens[i] += 1;
+    meta_copy = m.pairs + size_t(npairs) * 2 * sizeof(int64_t);
+  } else {
+    st = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
+    if (st != PK_OK) return st;
+    st = pk_longest_first_order(lens, num_seqs, order);
+    if (st != PK_OK) return st;
+  }
   const int32_t max_ctx = *std::max_element(lens, lens + num_seqs);
-
-  // Transfers: the step's tensors from the caller's host buffers, the
-  // metadata in one copy.
-  const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
-  const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
-  if (cudaMemcpyAsync(b->q_dev, b->q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(b->k_dev, b->k_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(b->v_dev, b->v_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(md, mh, m.total, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (cudaMemcpyAsync(md, mh, meta_copy, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return PK_ERR_CUDA;
 
   // Device side of the step.
@@ -101,17 +122,22 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
                         desc, stream);
     if (st != PK_OK) return st;
   }
-  st = pk_reshape_and_cache(b->k_dev, b->v_dev, reinterpret_cast<const int64_t *>(md + m.slots),
-                            num_seqs, k_cache, v_cache, desc, stream);
+  const int64_t *dslots = reinterpret_cast<const int64_t *>(md + m.slots);
+  int32_t *dtables = reinterpret_cast<int32_t *>(md + m.tables);
+  int32_t *dlens = reinterpret_cast<int32_t *>(md + m.lens);
+  st = resident ? pk_reshape_and_cache_append(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache,
+                                              desc, dtables, max_blocks_per_seq, dlens, stream)
+                : pk_reshape_and_cache(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache, desc,
+                                       stream);
   if (st != PK_OK) return st;
   st = pk_paged_attention_decode_impl(
-      b->out_dev, b->q_dev, k_cache, v_cache, reinterpret_cast<const int32_t *>(md + m.tables),
-      reinterpret_cast<const int32_t *>(md + m.lens), scale, num_seqs, num_q_heads,
+      b->out_dev, b->q_dev, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
       max_blocks_per_seq, max_ctx, partition_size, b->workspace, b->workspace_bytes, desc,
       reinterpret_cast<const int32_t *>(md + m.order), PK_ATTN_AUTO, stream);
   if (st != PK_OK) return st;
   if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return PK_ERR_CUDA;
+  b->tables_resident = 1;
   return PK_OK;
 }
 

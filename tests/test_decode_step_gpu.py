@@ -56,3 +56,121 @@ def test_decode_step_matches_stepwise_path(name, nseq, B):
     assert np.array_equal(from_device(a.k_cache), from_device(b.k_cache))
     assert np.array_equal(from_device(a.v_cache), from_device(b.v_cache))
     b.bm.check_invariants()
+
+
+@pytest.mark.parametrize("name,nseq,B,steps", [("gqa8b", 24, None, 40), ("prefix", 8, 8, 20)])
+def test_resident_tables_over_many_steps(name, nseq, B, steps):
+    """After the first step the tables stay on the device and are advanced by
+    the scatter kernel: many steps (crossing block boundaries) still give the
+    step-by-step path's outputs bit for bit, and the device tables equal the
+    block manager's."""
+    wl = make_workload(name, block_size=B, num_seqs=nseq)
+    wl.enable_memo()
+    a = DecodeState(wl, "cuda", extra_tokens=steps)
+    b = DecodeState(wl, "cuda", extra_tokens=steps)
+    stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
+                               b.k_cache, b.v_cache)
+    for i in range(steps):
+        si = a.prepare_step(i)
+        d = a.upload(si)
+        out_a = a.new_out()
+        a.run_step(d, out_a, a.alloc_workspace(d["max_context_len"], -1))
+        q, k, v = wl.step_inputs(i)
+        stepper.q_host.copy_(_host(q, wl.dtype))
+        stepper.k_host.copy_(_host(k, wl.dtype))
+        stepper.v_host.copy_(_host(v, wl.dtype))
+        out_b = stepper.step()
+        assert stepper.buffers.tables_resident == 1
+        assert np.array_equal(from_device(out_a), from_device(out_b)), f"step {i}"
+    assert pk.pk_get_device_error()[0] == 0
+    S, maxb = wl.num_seqs, b.max_blocks
+    meta = from_device(stepper.meta_dev)
+    lay = _meta_layout(S, maxb)
+    tables, lens = b.bm.export_tables(range(S), maxb)
+    assert np.array_equal(meta[lay["tables"]: lay["tables"] + 4 * S * maxb].view(np.int32).reshape(S, maxb), tables)
+    assert np.array_equal(meta[lay["lens"]: lay["lens"] + 4 * S].view(np.int32), lens)
+
+
+def _meta_layout(S, maxb):
+    """Offsets of the decode-step metadata sections (256-byte aligned, in the
+    order slots, pairs, order, lens, tables) as documented by pk_decode_step."""
+    up = lambda x: (x + 255) // 256 * 256
+    slots = 0
+    pairs = up(slots + 8 * S)
+    order = up(pairs + 16 * S)
+    lens = up(order + 4 * S)
+    tables = up(lens + 4 * S)
+    assert up(tables + 4 * S * maxb) == pk.lib().pk_decode_step_meta_bytes(S, maxb)
+    return {"slots": slots, "pairs": pairs, "order": order, "lens": lens, "tables": tables}
+
+
+def test_invalidate_after_fork_reuploads_tables():
+    wl = make_workload("gqa8b", num_seqs=6)
+    wl.enable_memo()
+    b = DecodeState(wl, "cuda", extra_tokens=8)
+    ids = list(range(wl.num_seqs))
+    stepper = pk.DecodeStepper(b.bm, ids, wl.num_q_heads, wl.scale, b.max_blocks, b.k_cache, b.v_cache)
+    stepper.step()
+    # Free one sequence and fork another into its id: the rows' tables change.
+    b.bm.free_seq(2)
+    b.bm.fork(4, 2)
+    stepper.invalidate()
+    stepper.step()
+    assert pk.pk_get_device_error()[0] == 0
+    S, maxb = wl.num_seqs, b.max_blocks
+    lay = _meta_layout(S, maxb)
+    meta = from_device(stepper.meta_dev)
+    tables, lens = b.bm.export_tables(ids, maxb)
+    assert np.array_equal(meta[lay["tables"]: lay["tables"] + 4 * S * maxb].view(np.int32).reshape(S, maxb), tables)
+    b.bm.check_invariants()
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_scatter_append_updates_tables_like_the_block_manager(B):
+    """pk_reshape_and_cache_append against the host block manager on a batch
+    with forks (copy-on-write pairs) and sequences opening new blocks."""
+    rng = np.random.default_rng(B)
+    N, Hk, d = 256, 2, 64
+    bm = pk.BlockManager(N, B, rng.permutation(N).astype(np.int32))
+    for s, n in enumerate([5, B + 3, 3 * B, 2 * B + 1, 1, 4 * B - 1]):
+        bm.add_seq(s)
+        bm.append(s, n)
+    bm.fork(1, 6)                     # partial tails: the next tokens copy on write
+    bm.fork(3, 7)
+    bm.add_seq(8)
+    bm.append(8, B)                   # the next token opens a block
+    ids = list(range(9))
+    maxb = 8
+    tables0, lens0 = bm.export_tables(ids, maxb)
+    slots, pairs = bm.append_batch(ids)
+    assert len(pairs) == 2
+    tables1, lens1 = bm.export_tables(ids, maxb)
+    desc_pool = torch.zeros((N, B, Hk, d), dtype=torch.bfloat16, device="cuda")
+    v_pool = torch.zeros_like(desc_pool)
+    kk = torch.randn((len(ids), Hk, d), device="cuda").to(torch.bfloat16)
+    vv = torch.randn((len(ids), Hk, d), device="cuda").to(torch.bfloat16)
+    dt = torch.from_numpy(tables0).cuda()
+    dl = torch.from_numpy(lens0).cuda()
+    pk.pk_get_device_error()
+    pk.pk_reshape_and_cache_append(kk, vv, torch.from_numpy(slots).cuda(), desc_pool, v_pool, dt, dl)
+    torch.cuda.synchronize()
+    assert pk.pk_get_device_error()[0] == 0
+    assert np.array_equal(dt.cpu().numpy(), tables1)
+    assert np.array_equal(dl.cpu().numpy(), lens1)
+    flat = desc_pool.view(N * B, Hk, d)
+    assert torch.equal(flat[torch.from_numpy(slots).cuda()], kk)
+
+
+def test_scatter_append_records_a_row_out_of_step():
+    B, N = 16, 64
+    pool = torch.zeros((N, B, 2, 64), dtype=torch.bfloat16, device="cuda")
+    vpool = torch.zeros_like(pool)
+    kk = torch.ones((2, 2, 64), dtype=torch.bfloat16, device="cuda")
+    tables = torch.tensor([[3, -1], [5, -1]], dtype=torch.int32, device="cuda")
+    lens = torch.tensor([4, 7], dtype=torch.int32, device="cuda")
+    slots = torch.tensor([3 * B + 4, 5 * B + 9], dtype=torch.int64, device="cuda")   # row 1: offset 9 != 7
+    pk.pk_get_device_error()
+    pk.pk_reshape_and_cache_append(kk, kk, slots, pool, vpool, tables, lens)
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "context" and idx == 1
+    assert lens.tolist() == [5, 7] and tables.tolist() == [[3, -1], [5, -1]]
