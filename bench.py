@@ -57,7 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="mha7b", choices=["tiny", "mha7b", "gqa8b", "long", "prefix", "chat"])
+    p.add_argument("--workload", default="mha7b", choices=["tiny", "mha7b", "gqa8b", "long", "prefix", "chat", "mixed"])
     p.add_argument("--block-size", type=int, default=None, help="prefix workload only: 8, 16 or 32")
     p.add_argument("--partition", type=int, default=-1, help="0 = no split, -1 = auto, >0 tokens")
     p.add_argument("--attn-impl", default="auto", choices=["auto", "simt", "mma"])
@@ -68,6 +68,9 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="launch the timed steps eagerly, not as CUDA graphs")
     p.add_argument("--no-order", action="store_true", help="launch sequences in index order, not longest first")
+    p.add_argument("--grid", action="store_true",
+                   help="launch the (sequence, partition) grid in longest-first sequence order instead of the "
+                        "planned work list")
     p.add_argument("--cascade", action="store_true",
                    help="cascade attention: each shared prefix read once per group (prefix workload)")
     p.add_argument("--no-swap", action="store_true", help="skip the swap-out / swap-in bandwidth measurement")
@@ -331,10 +334,20 @@ def run_ours(args):
     st = DecodeState(wl, dev, extra_tokens=R + E + Ew + 1)
     host_steps = [st.prepare_step() for _ in range(R)]
     dsteps = [st.upload(si) for si in host_steps]
+    planned = not (args.cascade or args.grid or args.no_order)
+    if planned:
+        # The default schedule: each step's work list from the host planner
+        # (pk_attention_plan), longest item first.
+        for si, d in zip(host_steps, dsteps):
+            d["partition"], d["items"] = st.plan(si, args.partition)
     step_bytes = [wl.kv_bytes(si.ctx_lens) for si in host_steps]
     step_unique = [unique_kv_bytes(wl, si) for si in host_steps]
     max_ctx = max(si.max_context_len for si in host_steps) + E + Ew + 1
-    ws = st.alloc_workspace(max_ctx, args.partition)
+    if planned:
+        ws_bytes = max(st.workspace_bytes(max_ctx, d["partition"]) for d in dsteps)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    else:
+        ws = st.alloc_workspace(max_ctx, args.partition)
     out = st.new_out()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
@@ -355,10 +368,10 @@ def run_ours(args):
     # split-K merge (the tensor-core kernel merges inside its last partition).
     simt = args.attn_impl == "simt" or wl.dtype == "f32"
 
-    def launches(si):
+    def launches(si, d):
         if groups is not None and groups["num_groups"]:
             return (1 if len(si.pairs) else 0) + 3  # scatter, prefix kernel, suffix kernel
-        part = st.resolve_partition(si.max_context_len, args.partition)
+        part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
         return (1 if len(si.pairs) else 0) + 2 + (1 if split and simt else 0)
 
@@ -435,7 +448,7 @@ def run_ours(args):
         else:
             attend(d)
         e2.record()
-        n_launch += launches(host_steps[j])
+        n_launch += launches(host_steps[j], d)
         total_bytes += step_bytes[j]
         total_unique += step_unique[j]
     torch.cuda.synchronize()
@@ -473,6 +486,9 @@ def run_ours(args):
         cpu = cpu_baseline(wl, ref, args.cpu_seconds)
 
     part = st.resolve_partition(max(si.max_context_len for si in host_steps), args.partition)
+    if planned:
+        parts = sorted({d["partition"] for d in dsteps})
+        part = parts[0] if len(parts) == 1 else parts
     if groups is not None:
         part = args.partition if args.partition >= 0 else "auto (cascade)"
     mean_ms = 1e3 * t_step / args.steps
@@ -489,7 +505,8 @@ def run_ours(args):
                 "kv_bytes_per_step_mean": total_bytes / args.steps,
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
                 "launch": "CUDA graphs per step" if graphs else "eager",
-                "seq_order": "index" if args.no_order else "longest first (host)",
+                "seq_order": "index" if args.no_order else
+                             ("planned work list, longest item first (host)" if planned else "longest first (host)"),
                 "attention": (f"cascade: {groups['num_groups']} shared-prefix groups, prefix read once per group"
                               if groups is not None else "per sequence")}),
             "roofline": {"bound": "hbm",

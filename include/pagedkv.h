@@ -200,6 +200,53 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
 pk_status pk_longest_first_order(const int32_t *context_lens, int32_t num_seqs,
                                  int32_t *order_out);
 
+/* As pk_paged_attention_decode_impl, with the work given as a list of items
+ * instead of the (sequence, partition) grid: work_items is device int32
+ * [num_items][2], item y = (sequence, partition index), and one CTA per
+ * (KV head, item) runs. Only the listed items run, so a split whose longest
+ * context sets the partition count launches nothing for the shorter
+ * sequences' missing partitions. Precondition: the list holds every
+ * partition of every sequence exactly once for the resolved partition size
+ * (pk_paged_attention_resolve_partition) and the context lengths the kernel
+ * reads -- pk_attention_work_items builds it; an item outside the batch or
+ * the partition count is skipped and recorded (PK_DEVERR_ORDER). Results do
+ * not depend on the item order. 1 <= num_items <= 65535. */
+pk_status pk_paged_attention_decode_items(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, float scale,
+                                          int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, int32_t max_context_len,
+                                          int32_t partition_size, const int32_t *work_items,
+                                          int32_t num_items, void *workspace,
+                                          size_t workspace_bytes, const pk_cache_desc *desc,
+                                          pk_attn_impl impl, void *stream);
+
+/* Host helper for pk_paged_attention_decode_items: the items of sequences
+ * with host context_lens [n] cut into partitions of `partition` tokens (0 = no
+ * split; pass the resolved size), longest item first (ties: the longer
+ * sequence, then batch order, then the later partition) -- the
+ * longest-processing-time-first order. *num_items_out receives the count;
+ * PK_ERR_INVALID_ARG if it exceeds cap (items_out untouched). */
+pk_status pk_attention_work_items(const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t partition, int32_t *items_out, int32_t cap,
+                                  int32_t *num_items_out);
+
+/* Host planner for pk_paged_attention_decode_items: the partition size and
+ * the work list of a batch whose host context lengths are known.
+ * partition_size > 0 or 0 is used as given (0 = no split); -1 chooses from
+ * the lengths: with W = (sum of context lengths x Hk) / (SMs x resident CTAs
+ * per SM of the kernel that will run), a batch whose longest context is
+ * above 2W (and 1024 tokens) is cut into items of about W tokens -- k equal
+ * parts of the longest context, k = floor(max / W), multiples of 64 tokens,
+ * at least 512 -- else it stays whole. *partition_out receives the size (0 =
+ * no split); pass it as partition_size to the attention call and size the
+ * workspace with pk_paged_attention_workspace_size for it (any choice of -1
+ * is covered by the size for 512). Items as pk_attention_work_items. */
+pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t partition_size, const pk_cache_desc *desc,
+                            int32_t *partition_out, int32_t *items_out, int32_t cap,
+                            int32_t *num_items_out);
+
 /* Allocation-free decode attention. The pages have no counterpart: this is a
  * library convenience for callers that cannot allocate device memory -- a
  * serving engine whose memory planner already gave nearly all HBM to the KV
@@ -536,6 +583,10 @@ typedef struct {
      * outside pk_decode_step). Out: 1 after a successful call, 0 otherwise.
      * Set it to 0 whenever that does not hold. */
     int32_t tables_resident;
+    /* Library-managed (zero-initialise): the work plan of the resident steps,
+     * its partition size and item count (see pk_attention_plan). */
+    int32_t plan_partition;
+    int32_t plan_items;
 } pk_step_buffers;
 
 /* Bytes of pk_step_buffers.meta_host / meta_dev for S sequences and tables of
@@ -547,16 +598,21 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  *   1. copies host -> device of q, k, v from the caller's host buffers;
  *   2. host: append one token to each sequence (pk_bm_append_batch); unless
  *      buffers->tables_resident, export the padded tables and lengths and
- *      order the sequences longest first -- into meta_host;
+ *      plan the attention's work list (pk_attention_plan with partition_size)
+ *      -- into meta_host; a resident step keeps the plan's partition and
+ *      rebuilds the list only when a sequence starts a new partition;
  *   3. copy host -> device of the metadata in one transfer (resident mode:
  *      only the slots and copy-on-write pairs);
  *   4. device: pk_copy_blocks for the step's pairs, the slot scatter of k/v
  *      (resident mode: pk_reshape_and_cache_append, which also advances the
- *      device tables and lengths), the attention (automatic kernel, the given
- *      partition_size, the launch order);
+ *      device tables and lengths), the attention over the work list
+ *      (pk_paged_attention_decode_items, automatic kernel);
  *   5. copy device -> host of the output into out_host.
  * All work is enqueued on `stream`; out_host holds the result once the stream
- * is synchronised, and meta_host must not be reused before then. The pages
+ * is synchronised, and meta_host must not be reused before then. The
+ * workspace must cover the plan's partition: with partition_size = -1,
+ * pk_paged_attention_workspace_size for 512 tokens and the longest context
+ * the steps reach. The pages
  * have no counterpart for this packaging; each step it performs is theirs
  * (see the entry points above). On an error after step 2 the block manager
  * keeps the appended tokens and tables_resident is 0. */

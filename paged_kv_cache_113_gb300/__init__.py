@@ -44,7 +44,8 @@ DEVERR_NAMES = {0: "none", 1: "slot", 2: "block_id", 3: "pair", 4: "context", 5:
 # Every symbol include/pagedkv.h declares.
 EXPORTED = (
     "pk_reshape_and_cache", "pk_reshape_and_cache_append", "pk_copy_blocks", "pk_paged_attention_decode",
-    "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static",
+    "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static", "pk_paged_attention_decode_items",
+    "pk_attention_work_items", "pk_attention_plan",
     "pk_paged_attention_resolve_partition",
     "pk_paged_attention_workspace_size", "pk_longest_first_order", "pk_get_device_error", "pk_status_string",
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
@@ -73,7 +74,8 @@ class StepBuffers(ctypes.Structure):
                 ("meta_host", ctypes.c_void_p), ("meta_dev", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
                 ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("tables_resident", ctypes.c_int32)]
+                ("tables_resident", ctypes.c_int32), ("plan_partition", ctypes.c_int32),
+                ("plan_items", ctypes.c_int32)]
 
 
 class SimRequest(ctypes.Structure):
@@ -121,6 +123,10 @@ def lib() -> ctypes.CDLL:
         "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
                                                  P, i32, P]),
         "pk_longest_first_order": (i32, [P, i32, P]),
+        "pk_paged_attention_decode_items": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, i32, P, sz,
+                                                  D, i32, P]),
+        "pk_attention_work_items": (i32, [P, i32, i32, P, i32, P]),
+        "pk_attention_plan": (i32, [P, i32, i32, i32, D, P, P, i32, P]),
         "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),
         "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
         "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
@@ -287,9 +293,34 @@ def pk_longest_first_order(context_lens) -> np.ndarray:
     return out[: len(lens)]
 
 
+def pk_attention_work_items(context_lens, partition: int) -> np.ndarray:
+    """Host helper: the (sequence, partition) work items, longest first, int32 [n, 2]."""
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    n = ctypes.c_int32(0)
+    lib().pk_attention_work_items(_np_ptr(lens), len(lens), int(partition), None, 0, ctypes.byref(n))
+    out = np.empty((max(n.value, 1), 2), np.int32)
+    _check(lib().pk_attention_work_items(_np_ptr(lens), len(lens), int(partition), _np_ptr(out), n.value,
+                                         ctypes.byref(n)), "pk_attention_work_items")
+    return out[: n.value]
+
+
+def pk_attention_plan(context_lens, num_q_heads: int, desc: CacheDesc, partition_size: int = -1):
+    """Host planner: ``(partition, items int32 [n, 2])`` for the host context
+    lengths (see pk_attention_plan in the header)."""
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    part, n = ctypes.c_int32(0), ctypes.c_int32(0)
+    lib().pk_attention_plan(_np_ptr(lens), len(lens), int(num_q_heads), int(partition_size), ctypes.byref(desc),
+                            ctypes.byref(part), None, 0, ctypes.byref(n))
+    out = np.empty((max(n.value, 1), 2), np.int32)
+    _check(lib().pk_attention_plan(_np_ptr(lens), len(lens), int(num_q_heads), int(partition_size),
+                                   ctypes.byref(desc), ctypes.byref(part), _np_ptr(out), n.value, ctypes.byref(n)),
+           "pk_attention_plan")
+    return int(part.value), out[: n.value]
+
+
 def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                               max_context_len: int, partition_size: int = -1, workspace=None,
-                              impl: str = "auto", stream=None, seq_order=None):
+                              impl: str = "auto", stream=None, seq_order=None, work_items=None):
     """Decode attention through the block tables; writes ``out`` ``[S, Hq, d]``.
 
     ``block_tables`` int32 ``[S, max_blocks]``, ``context_lens`` int32 ``[S]``
@@ -298,6 +329,9 @@ def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_le
     of at least :func:`pk_paged_attention_workspace_size` bytes when the
     partitioning splits. ``seq_order``: optional int32 CUDA tensor ``[S]``, the
     launch order of the sequences (see :func:`pk_longest_first_order`).
+    ``work_items``: optional int32 CUDA tensor ``[n, 2]`` of (sequence,
+    partition) items for the resolved partition size (see
+    :func:`pk_attention_work_items`); replaces ``seq_order``.
     """
     torch = _torch()
     desc = cache_desc(k_cache)
@@ -313,6 +347,16 @@ def pk_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_le
         ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
     if impl not in IMPLS:
         raise ValueError(f"impl must be one of {sorted(IMPLS)}")
+    if work_items is not None:
+        if work_items.dim() != 2 or int(work_items.shape[1]) != 2:
+            raise ValueError("work_items must be [n, 2]")
+        _check(lib().pk_paged_attention_decode_items(
+            _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+            _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+            float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+            _dev(work_items, "work_items", torch.int32), int(work_items.shape[0]), ws_ptr, ws_bytes,
+            ctypes.byref(desc), IMPLS[impl], _stream(stream)), "pk_paged_attention_decode_items")
+        return
     _check(lib().pk_paged_attention_decode_impl(
         _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
@@ -624,7 +668,9 @@ class DecodeStepper:
         self.meta_host = torch.empty(mb, dtype=torch.uint8).pin_memory()
         self.meta_dev = torch.empty(mb, dtype=torch.uint8, device=dev)
         mc = self.maxb * self.desc.block_size if max_context_len is None else int(max_context_len)
-        wsb = pk_paged_attention_workspace_size(S, self.Hq, mc, self.partition, self.desc)
+        # The automatic plan may choose any partition of at least 512 tokens.
+        wsb = pk_paged_attention_workspace_size(S, self.Hq, mc, 512 if self.partition == -1 else self.partition,
+                                                self.desc)
         self.workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
         self.buffers = StepBuffers(
             self.q_host.data_ptr(), self.k_host.data_ptr(), self.v_host.data_ptr(),
@@ -637,7 +683,7 @@ class DecodeStepper:
         # upload; only the slot section (plus 16 bytes per copy-on-write pair)
         # once the tables are resident.
         self.h2d_bytes_full = qkv + mb
-        self.h2d_bytes_resident = qkv + (8 * S + 255) // 256 * 256
+        self.h2d_bytes_resident = qkv + (8 * S + 255) // 256 * 256   # + the work list when it changes
         self.h2d_bytes = self.h2d_bytes_full
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
 

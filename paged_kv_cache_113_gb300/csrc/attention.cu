@@ -34,6 +34,8 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "pagedkv.h"
 #include "pk_device.cuh"
@@ -70,6 +72,10 @@ struct AttnParams {
   int32_t block_size, max_blocks, num_blocks;
   int32_t partition;         // tokens per partition
   int32_t num_partitions;    // P (1 = no split: write `out` directly)
+  // Work list: CTA (h, y) serves (sequence items[2y], partition items[2y+1])
+  // instead of the (sequence, partition) grid; null when not used.
+  const int32_t *items;
+  int32_t num_items;
 };
 
 // Context length of sequence s, clamped to what the table and the grid can
@@ -96,6 +102,27 @@ __device__ __forceinline__ int launch_seq(const AttnParams &p) {
     return y;
   }
   return s;
+}
+
+// The (sequence, partition) this CTA serves. With a work list: item
+// blockIdx.y (an entry outside the batch or the partition count is recorded
+// and the CTA does nothing). Otherwise sequence launch_seq() and partition
+// gridDim.z - 1 - blockIdx.z: partitions launch last-first, since the higher
+// ones exist only for the longest sequences.
+__device__ __forceinline__ bool work_of(const AttnParams &p, int &s, int &part) {
+  if (p.items) {
+    const int y = int(blockIdx.y);
+    s = __ldg(p.items + 2 * y);
+    part = __ldg(p.items + 2 * y + 1);
+    if (s < 0 || s >= p.num_seqs || part < 0 || part >= p.num_partitions - p.prefix_slots) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) pk::record_error(&g_attn_error, PK_DEVERR_ORDER, y);
+      return false;
+    }
+    return true;
+  }
+  part = int(gridDim.z) - 1 - int(blockIdx.z);
+  s = launch_seq(p);
+  return true;
 }
 
 // Fused-merge ticket of one (sequence, KV head): returns how many of this
@@ -182,12 +209,9 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
   constexpr int NW = 4;
   constexpr int EPL = D / 32;  // elements per lane
-  // Partitions launch last-first: the higher ones exist only for the longest
-  // sequences, so the heaviest work starts early and short work fills the end.
-  const int kvh = blockIdx.x, part = int(gridDim.z) - 1 - int(blockIdx.z);
-  // Sequences launch in the caller's order when one is given (longest first
-  // keeps the longest work from trailing the launch).
-  const int s = launch_seq(p);
+  const int kvh = blockIdx.x;
+  int s, part;
+  if (!work_of(p, s, part)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -332,17 +356,16 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   auto full_bar = [&](int i) { return bars + 8u * i; };
   auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
 
-  // Partitions launch last-first: the higher ones exist only for the longest
-  // sequences, so the heaviest work starts early and short work fills the end.
-  const int kvh = blockIdx.x, part = int(gridDim.z) - 1 - int(blockIdx.z);
-  // Sequences launch in the caller's order when one is given (longest first
-  // keeps the longest work from trailing the launch).
-  const int s = launch_seq(p);
+  // The caller's work list, or the grid in the caller's sequence order (longest
+  // first keeps the longest work from trailing the launch).
+  const int kvh = blockIdx.x;
+  int s, part;
+  if (!work_of(p, s, part)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
   if (ctx == 0) {  // invalid length (recorded): a zero row, nothing to merge
-    if (blockIdx.z == 0)
+    if (part == 0)
       for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x)
         static_cast<__nv_bfloat16 *>(p.out)[(size_t(s) * p.num_q_heads + kvh * G + idx / D) * D +
                                             idx % D] = __float2bfloat16_rn(0.0f);
@@ -1060,7 +1083,8 @@ pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t s
     return PK_ERR_CUDA;
   auto kern = attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>;
   if (mma_kernel_ready<D, BS>() != cudaSuccess) return PK_ERR_CUDA;
-  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions - p.prefix_slots);
+  dim3 grid(p.num_kv_heads, p.items ? p.num_items : p.num_seqs,
+            p.items ? 1 : p.num_partitions - p.prefix_slots);
   kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
@@ -1094,7 +1118,7 @@ pk_status launch_prefix(const AttnParams &p, const pk_cache_desc &d, int num_gro
 
 template <typename T, int D>
 pk_status launch_simt(const AttnParams &p, cudaStream_t stream) {
-  dim3 grid(p.num_kv_heads, p.num_seqs, p.num_partitions);
+  dim3 grid(p.num_kv_heads, p.items ? p.num_items : p.num_seqs, p.items ? 1 : p.num_partitions);
   attn_simt_kernel<T, D><<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
@@ -1283,15 +1307,19 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
   return pb + ticket_bytes(num_seqs, desc->num_kv_heads, pb);
 }
 
-pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
-                                         const void *v_cache, const int32_t *block_tables,
-                                         const int32_t *context_lens, float scale,
-                                         int32_t num_seqs, int32_t num_q_heads,
-                                         int32_t max_blocks_per_seq, int32_t max_context_len,
-                                         int32_t partition_size, void *workspace,
-                                         size_t workspace_bytes, const pk_cache_desc *desc,
-                                         const int32_t *seq_order, pk_attn_impl impl,
-                                         void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of the per-sequence attention entry points: either a launch
+// order over the (sequence, partition) grid or a work list of items.
+pk_status decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, float scale,
+                           int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+                           int32_t max_context_len, int32_t partition_size, void *workspace,
+                           size_t workspace_bytes, const pk_cache_desc *desc,
+                           const int32_t *seq_order, const int32_t *items, int32_t num_items,
+                           pk_attn_impl impl, void *stream) {
   pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
   if (st != PK_OK) return st;
   if (num_seqs == 0) return PK_OK;
@@ -1341,6 +1369,9 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
     p.ws_l = p.ws_m + rows;
   }
   p.order = seq_order;
+  p.items = items;
+  p.num_items = num_items;
+  if (items && (num_items <= 0 || num_items > 65535)) return PK_ERR_UNSUPPORTED;
 
   const bool mma_ok = mma_supported(*desc, p.group);
   if (impl == PK_ATTN_MMA && !mma_ok) return PK_ERR_UNSUPPORTED;
@@ -1370,6 +1401,124 @@ pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k
   if (desc->dtype == PK_F32)
     return D == 128 ? launch_merge<float, 128>(p, s) : launch_merge<float, 64>(p, s);
   return D == 128 ? launch_merge<__nv_bfloat16, 128>(p, s) : launch_merge<__nv_bfloat16, 64>(p, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+pk_status pk_paged_attention_decode_impl(void *out, const void *q, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables,
+                                         const int32_t *context_lens, float scale,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         int32_t max_blocks_per_seq, int32_t max_context_len,
+                                         int32_t partition_size, void *workspace,
+                                         size_t workspace_bytes, const pk_cache_desc *desc,
+                                         const int32_t *seq_order, pk_attn_impl impl,
+                                         void *stream) {
+  return decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                          num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
+                          workspace, workspace_bytes, desc, seq_order, nullptr, 0, impl, stream);
+}
+
+pk_status pk_paged_attention_decode_items(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, float scale,
+                                          int32_t num_seqs, int32_t num_q_heads,
+                                          int32_t max_blocks_per_seq, int32_t max_context_len,
+                                          int32_t partition_size, const int32_t *work_items,
+                                          int32_t num_items, void *workspace,
+                                          size_t workspace_bytes, const pk_cache_desc *desc,
+                                          pk_attn_impl impl, void *stream) {
+  if (!work_items) return PK_ERR_INVALID_ARG;
+  return decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                          num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
+                          workspace, workspace_bytes, desc, nullptr, work_items, num_items, impl,
+                          stream);
+}
+
+pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t partition_size, const pk_cache_desc *desc,
+                            int32_t *partition_out, int32_t *items_out, int32_t cap,
+                            int32_t *num_items_out) {
+  if (!partition_out || !num_items_out || num_seqs <= 0 || !context_lens) return PK_ERR_INVALID_ARG;
+  *partition_out = 0;
+  *num_items_out = 0;
+  int32_t max_ctx = 1;
+  int64_t total = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    const int32_t c = std::max(context_lens[s], 1);
+    max_ctx = std::max(max_ctx, c);
+    total += c;
+  }
+  pk_status st = check_common(desc, num_seqs, num_q_heads, max_ctx);
+  if (st != PK_OK) return st;
+  const int32_t B = desc->block_size;
+  int32_t part = 0;
+  if (partition_size > 0) {
+    if (partition_size % B != 0) return PK_ERR_INVALID_ARG;
+    part = partition_size < max_ctx ? partition_size : 0;
+  } else if (partition_size == -1) {
+    // W = the (token, KV head) work one resident CTA slot gets when the batch
+    // is spread evenly. A context longer than 2W would outlast the rest of the
+    // launch on its own CTAs, so the batch splits into items of about W tokens
+    // (k equal parts of the longest context, k = floor(max / W), multiples of
+    // 64 tokens, at least 512): uniform long contexts get one wave; short or
+    // even batches stay whole.
+    const int64_t slots = int64_t(sm_count()) *
+                          resident_ctas(*desc, num_q_heads / desc->num_kv_heads);
+    const int64_t W = std::max<int64_t>(1, (total * desc->num_kv_heads + slots - 1) / slots);
+    if (max_ctx > 2 * W && max_ctx > 1024) {
+      const int64_t k = std::max<int64_t>(1, max_ctx / W);
+      int64_t p = (max_ctx + k - 1) / k;
+      p = std::max<int64_t>(512, (p + 63) / 64 * 64);
+      p = (p + B - 1) / B * B;
+      part = p < max_ctx ? int32_t(p) : 0;
+    }
+  } else if (partition_size != 0) {
+    return PK_ERR_INVALID_ARG;
+  }
+  *partition_out = part;
+  return pk_attention_work_items(context_lens, num_seqs, part, items_out, cap, num_items_out);
+}
+
+pk_status pk_attention_work_items(const int32_t *context_lens, int32_t num_seqs,
+                                  int32_t partition, int32_t *items_out, int32_t cap,
+                                  int32_t *num_items_out) {
+  if (!num_items_out || num_seqs < 0 || partition < 0 || cap < 0 || (num_seqs > 0 && !context_lens))
+    return PK_ERR_INVALID_ARG;
+  *num_items_out = 0;
+  struct Item {
+    int32_t len, ctx, seq, part;
+  };
+  std::vector<Item> items;
+  try {
+    items.reserve(size_t(num_seqs));
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      const int32_t c = std::max(context_lens[s], 1);  // an invalid length still gets its item
+      const int32_t n = partition > 0 ? (c + partition - 1) / partition : 1;
+      for (int32_t j = 0; j < n; ++j)
+        items.push_back({partition > 0 ? std::min(partition, c - j * partition) : c, c, s, j});
+    }
+  } catch (const std::bad_alloc &) {
+    return PK_ERR_NOMEM;
+  }
+  // Longest item first; ties: the longer sequence, then batch order, then the
+  // later partition.
+  std::sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
+    if (a.len != b.len) return a.len > b.len;
+    if (a.ctx != b.ctx) return a.ctx > b.ctx;
+    if (a.seq != b.seq) return a.seq < b.seq;
+    return a.part > b.part;
+  });
+  *num_items_out = int32_t(items.size());
+  if (int64_t(items.size()) > cap) return PK_ERR_INVALID_ARG;
+  if (!items.empty() && !items_out) return PK_ERR_INVALID_ARG;
+  for (size_t i = 0; i < items.size(); ++i) {
+    items_out[2 * i] = items[i].seq;
+    items_out[2 * i + 1] = items[i].part;
+  }
+  return PK_OK;
 }
 
 size_t pk_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,

@@ -2,14 +2,17 @@
 // queries are copied from the caller's host buffers first, so the copies run
 // while the host block manager appends a token to every sequence. The step's
 // metadata is packed into one pinned staging buffer and copied with a single
-// transfer: in full mode slots, copy-on-write pairs, launch order, context
+// transfer: in full mode slots, copy-on-write pairs, work items, context
 // lengths and padded block tables; in resident mode (the device already holds
 // this batch's tables and lengths) only slots and pairs -- the scatter kernel
-// then advances the device tables and lengths itself, and the launch order
-// (longest first) is unchanged because every sequence grew by one token. Then
+// then advances the device tables and lengths itself. Then
 // copy_blocks (when pairs exist), the scatter and the attention run, and the
 // output is copied back to host memory. Everything is enqueued on one stream;
 // the call returns once the work is enqueued.
+//
+// The attention runs a work list of (sequence, partition) items planned on the
+// host (pk_attention_plan). A full step plans afresh; a resident step keeps the
+// partition and rebuilds the list only when a sequence starts a new partition.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -25,10 +28,18 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Work items a batch can need: a partition is at least 512 tokens and a
+// context at most max_blocks * 32 tokens (B <= 32), so a sequence has at most
+// 1 + max_blocks / 16 items.
+int64_t item_capacity(int32_t num_seqs, int32_t max_blocks) {
+  return int64_t(num_seqs) * (1 + max_blocks / 16);
+}
+
 // What changes every step comes first, so a resident-mode step copies one
 // short prefix of the buffer.
 struct MetaLayout {
-  size_t slots, pairs, order, lens, tables, total;
+  size_t slots, pairs, items, lens, tables, total;
+  int32_t item_cap;
 };
 
 MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
@@ -38,8 +49,9 @@ MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
   off = align_up(off + size_t(num_seqs) * sizeof(int64_t));
   m.pairs = off;
   off = align_up(off + size_t(num_seqs) * 2 * sizeof(int64_t));
-  m.order = off;
-  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
+  m.items = off;
+  m.item_cap = int32_t(std::min<int64_t>(item_capacity(num_seqs, max_blocks), 65535));
+  off = align_up(off + size_t(m.item_cap) * 2 * sizeof(int32_t));
   m.lens = off;
   off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
   m.tables = off;
@@ -79,7 +91,7 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   int64_t *pairs = reinterpret_cast<int64_t *>(mh + m.pairs);
   int32_t *tables = reinterpret_cast<int32_t *>(mh + m.tables);
   int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
-  int32_t *order = reinterpret_cast<int32_t *>(mh + m.order);
+  int32_t *items = reinterpret_cast<int32_t *>(mh + m.items);
   const bool resident = b->tables_resident != 0;
   // Resident mode keeps the previous step's lengths in meta_host; every row
   // must have room for one more token.
@@ -104,12 +116,23 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   b->tables_resident = 0;  // until this step's metadata is on its way
   size_t meta_copy = m.total;
   if (resident) {
-    for (int32_t i = 0; i < num_seqs; ++i) lens[i] += 1;
+    const int32_t part = b->plan_partition;
+    bool new_part = false;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+      lens[i] += 1;
+      if (part > 0 && (lens[i] - 1) % part == 0) new_part = true;
+    }
     meta_copy = m.pairs + size_t(npairs) * 2 * sizeof(int64_t);
+    if (new_part) {
+      st = pk_attention_work_items(lens, num_seqs, part, items, m.item_cap, &b->plan_items);
+      if (st != PK_OK) return st;
+      meta_copy = m.items + size_t(b->plan_items) * 2 * sizeof(int32_t);
+    }
   } else {
     st = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
     if (st != PK_OK) return st;
-    st = pk_longest_first_order(lens, num_seqs, order);
+    st = pk_attention_plan(lens, num_seqs, num_q_heads, partition_size, desc, &b->plan_partition,
+                           items, m.item_cap, &b->plan_items);
     if (st != PK_OK) return st;
   }
   const int32_t max_ctx = *std::max_element(lens, lens + num_seqs);
@@ -130,10 +153,10 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
                 : pk_reshape_and_cache(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache, desc,
                                        stream);
   if (st != PK_OK) return st;
-  st = pk_paged_attention_decode_impl(
+  st = pk_paged_attention_decode_items(
       b->out_dev, b->q_dev, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
-      max_blocks_per_seq, max_ctx, partition_size, b->workspace, b->workspace_bytes, desc,
-      reinterpret_cast<const int32_t *>(md + m.order), PK_ATTN_AUTO, stream);
+      max_blocks_per_seq, max_ctx, b->plan_partition, reinterpret_cast<const int32_t *>(md + m.items),
+      b->plan_items, b->workspace, b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
   if (st != PK_OK) return st;
   if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return PK_ERR_CUDA;

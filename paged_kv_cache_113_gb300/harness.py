@@ -18,7 +18,8 @@ from typing import List, Optional
 
 import numpy as np
 
-from . import (BlockManager, pk_cascade_attention_decode, pk_cascade_workspace_size, pk_copy_blocks,
+from . import (BlockManager, pk_attention_plan, pk_attention_work_items, pk_cascade_attention_decode,
+               pk_cascade_workspace_size, pk_copy_blocks,
                pk_longest_first_order, pk_paged_attention_decode, pk_paged_attention_resolve_partition,
                pk_paged_attention_workspace_size, pk_reshape_and_cache, cache_desc)
 
@@ -179,12 +180,32 @@ class DecodeState:
         pk_reshape_and_cache(d["k"], d["v"], d["slots"], self.k_cache, self.v_cache, stream=stream)
         self.attention(d, out, workspace, partition_size, impl, stream)
 
+    def work_items(self, si: StepInputs, partition_size: int = -1):
+        """The step's (sequence, partition) work list as a device tensor,
+        for the partition size the library resolves from the batch shape."""
+        import torch
+        part = self.resolve_partition(si.max_context_len, partition_size)
+        return torch.from_numpy(pk_attention_work_items(si.ctx_lens, max(part, 0))).to(self.device)
+
+    def plan(self, si: StepInputs, partition_size: int = -1):
+        """The step's planned partition and work list (pk_attention_plan on the
+        host lengths); the work list as a device tensor."""
+        import torch
+        part, items = pk_attention_plan(si.ctx_lens, self.wl.num_q_heads, self.desc, partition_size)
+        return part, torch.from_numpy(items).to(self.device)
+
     def attention(self, d: dict, out, workspace=None, partition_size: int = -1, impl: str = "auto",
                   stream=None, ordered: bool = True):
-        """The attention call; ``ordered`` launches the longest sequences first."""
+        """The attention call; ``ordered`` launches the longest work first: by
+        the step's work list when ``d`` holds one (``items``), else by the
+        sequence order."""
+        items = d.get("items") if ordered else None
+        if items is not None and "partition" in d:
+            partition_size = d["partition"]   # the plan's partition goes with its work list
         pk_paged_attention_decode(out, d["q"], self.k_cache, self.v_cache, d["tables"], d["ctx_lens"],
                                   self.wl.scale, d["max_context_len"], partition_size, workspace, impl,
-                                  stream, seq_order=d.get("order") if ordered else None)
+                                  stream, seq_order=d.get("order") if ordered and items is None else None,
+                                  work_items=items)
 
     # -- cascade (shared-prefix) attention --------------------------------------
     def cascade_groups(self, min_prefix_blocks: int = 1, max_group_size: Optional[int] = None) -> dict:

@@ -533,3 +533,41 @@ def test_allocator_sim_rejects_malformed_input(L):
     with pytest.raises(pk.PagedKVError):
         pk.pk_sim_run(good, 3, "paged", 4)
     assert pk.pk_sim_run([], 16, "paged", 4)["summary"]["num_steps"] == 1
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_work_items_cover_every_partition_once_longest_first(L, seed):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, 5000, int(rng.integers(1, 60))).astype(np.int32)
+    for part in (0, 512, 1024, 1728):
+        got = pk.pk_attention_work_items(lens, part)
+        want = []
+        for s, c in enumerate(lens):
+            n = -(-int(c) // part) if part else 1
+            for j in range(n):
+                length = min(part, int(c) - j * part) if part else int(c)
+                want.append((-length, -int(c), s, -j))
+        want.sort()
+        assert [tuple(x) for x in got.tolist()] == [(s, -nj) for _, _, s, nj in want]
+
+
+def test_attention_plan_choices(L):
+    """The host plan on the workloads: long uniform contexts get one wave
+    (7 x 4736 tokens), the one 32K request among short ones is cut into
+    2048-token items, everything else stays whole (152 SMs x 3 CTAs when no
+    GPU is visible); explicit sizes pass through; the items are the work-list
+    helper's."""
+    want = {"mha7b": 0, "gqa8b": 0, "long": 4736, "chat": 0, "mixed": 2048, "prefix": 0}
+    for name, part in want.items():
+        wl = make_workload(name)
+        d = pk.CacheDesc(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, 1)
+        got, items = pk.pk_attention_plan(wl.ctx_lens, wl.num_q_heads, d, -1)
+        assert got == part, name
+        assert np.array_equal(items, pk.pk_attention_work_items(wl.ctx_lens, got))
+    wl = make_workload("mixed")
+    d = pk.CacheDesc(wl.num_blocks, wl.block_size, wl.num_kv_heads, wl.head_dim, 1)
+    assert pk.pk_attention_plan(wl.ctx_lens, 32, d, 1024)[0] == 1024
+    assert pk.pk_attention_plan(wl.ctx_lens, 32, d, 0)[0] == 0
+    assert pk.pk_attention_plan(wl.ctx_lens, 32, d, 40000)[0] == 0          # longer than every context
+    with pytest.raises(pk.PagedKVError):
+        pk.pk_attention_plan(wl.ctx_lens, 32, d, 1000)                    # not a multiple of B

@@ -27,6 +27,28 @@ def _host(a, dtype):
     return to_device(a, dtype, "cpu")
 
 
+class _Stepwise:
+    """The step-by-step path with pk_decode_step's schedule: the first step
+    plans (pk_attention_plan), later steps keep its partition and rebuild the
+    work list for the current lengths."""
+
+    def __init__(self, state):
+        self.st, self.part = state, None
+
+    def step(self, i):
+        st = self.st
+        si = st.prepare_step(i)
+        d = st.upload(si)
+        if self.part is None:
+            self.part, items = pk.pk_attention_plan(si.ctx_lens, st.wl.num_q_heads, st.desc, -1)
+        else:
+            items = pk.pk_attention_work_items(si.ctx_lens, self.part)
+        d["partition"], d["items"] = self.part, torch.from_numpy(items).cuda()
+        out = st.new_out()
+        st.run_step(d, out, st.alloc_workspace(d["max_context_len"], self.part))
+        return out
+
+
 @pytest.mark.parametrize("name,nseq,B", [("gqa8b", 24, None), ("prefix", 8, 32), ("long", 1, None),
                                          ("mha7b", 4, None), ("tiny", None, None)])
 def test_decode_step_matches_stepwise_path(name, nseq, B):
@@ -37,11 +59,9 @@ def test_decode_step_matches_stepwise_path(name, nseq, B):
     b = DecodeState(wl, "cuda", extra_tokens=steps)
     stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
                                b.k_cache, b.v_cache)
+    ref_path = _Stepwise(a)
     for i in range(steps):
-        si = a.prepare_step(i)
-        d = a.upload(si)
-        out_a = a.new_out()
-        a.run_step(d, out_a, a.alloc_workspace(d["max_context_len"], -1))
+        out_a = ref_path.step(i)
         q, k, v = wl.step_inputs(i)
         stepper.q_host.copy_(_host(q, wl.dtype))
         stepper.k_host.copy_(_host(k, wl.dtype))
@@ -58,7 +78,7 @@ def test_decode_step_matches_stepwise_path(name, nseq, B):
     b.bm.check_invariants()
 
 
-@pytest.mark.parametrize("name,nseq,B,steps", [("gqa8b", 24, None, 40), ("prefix", 8, 8, 20)])
+@pytest.mark.parametrize("name,nseq,B,steps", [("gqa8b", 24, None, 40), ("prefix", 8, 8, 20), ("mixed", 40, None, 20)])
 def test_resident_tables_over_many_steps(name, nseq, B, steps):
     """After the first step the tables stay on the device and are advanced by
     the scatter kernel: many steps (crossing block boundaries) still give the
@@ -70,17 +90,16 @@ def test_resident_tables_over_many_steps(name, nseq, B, steps):
     b = DecodeState(wl, "cuda", extra_tokens=steps)
     stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
                                b.k_cache, b.v_cache)
+    ref_path = _Stepwise(a)
     for i in range(steps):
-        si = a.prepare_step(i)
-        d = a.upload(si)
-        out_a = a.new_out()
-        a.run_step(d, out_a, a.alloc_workspace(d["max_context_len"], -1))
+        out_a = ref_path.step(i)
         q, k, v = wl.step_inputs(i)
         stepper.q_host.copy_(_host(q, wl.dtype))
         stepper.k_host.copy_(_host(k, wl.dtype))
         stepper.v_host.copy_(_host(v, wl.dtype))
         out_b = stepper.step()
         assert stepper.buffers.tables_resident == 1
+        assert stepper.buffers.plan_partition == ref_path.part
         assert np.array_equal(from_device(out_a), from_device(out_b)), f"step {i}"
     assert pk.pk_get_device_error()[0] == 0
     S, maxb = wl.num_seqs, b.max_blocks
@@ -93,15 +112,15 @@ def test_resident_tables_over_many_steps(name, nseq, B, steps):
 
 def _meta_layout(S, maxb):
     """Offsets of the decode-step metadata sections (256-byte aligned, in the
-    order slots, pairs, order, lens, tables) as documented by pk_decode_step."""
+    order slots, pairs, work items, lens, tables)."""
     up = lambda x: (x + 255) // 256 * 256
     slots = 0
     pairs = up(slots + 8 * S)
-    order = up(pairs + 16 * S)
-    lens = up(order + 4 * S)
+    items = up(pairs + 16 * S)
+    lens = up(items + 8 * min(S * (1 + maxb // 16), 65535))
     tables = up(lens + 4 * S)
     assert up(tables + 4 * S * maxb) == pk.lib().pk_decode_step_meta_bytes(S, maxb)
-    return {"slots": slots, "pairs": pairs, "order": order, "lens": lens, "tables": tables}
+    return {"slots": slots, "pairs": pairs, "items": items, "lens": lens, "tables": tables}
 
 
 def test_invalidate_after_fork_reuploads_tables():

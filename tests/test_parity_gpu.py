@@ -91,6 +91,7 @@ REDUCED = [
     ("prefix", 8, 16),
     ("prefix", 8, 32),
     ("chat", 12, None),
+    ("mixed", 40, None),
 ]
 
 
@@ -116,7 +117,7 @@ def _sample_rows(wl, ctx, n=48, seed=0):
 
 
 FULL = [("mha7b", None), ("gqa8b", None), ("long", None), ("prefix", 8), ("prefix", 16), ("prefix", 32),
-        ("chat", None)]
+        ("chat", None), ("mixed", None)]
 
 
 @pytest.mark.slow
@@ -363,3 +364,61 @@ def test_chat_prefix_cache_bookkeeping():
         if len(members) > 1 and full:
             assert (tables[members, :full] == tables[members[0], :full]).all()
     st.bm.check_invariants()
+
+
+@pytest.mark.parametrize("name,nseq,part", [("gqa8b", 40, 256), ("gqa8b", 40, 512), ("long", 2, 4736),
+                                            ("prefix", 8, 512), ("mha7b", 8, 0), ("tiny", None, 16)])
+@pytest.mark.parametrize("impl", ["mma", "simt"])
+def test_work_list_matches_grid_bit_for_bit(name, nseq, part, impl):
+    """The (sequence, partition) work list gives the grid launch's result bit
+    for bit (the same partials, merged in the same order) and the oracle's
+    within tolerance."""
+    wl = make_workload(name, num_seqs=nseq, block_size=8 if name == "prefix" else None)
+    if impl == "mma" and wl.dtype != "bf16":
+        pytest.skip("the tensor-core kernel is bf16 only")
+    st, d, _, ref = _build_pair(wl, compare_pool=False)
+    lens = from_device(d["ctx_lens"])
+    items = torch.from_numpy(pk.pk_attention_work_items(lens, st.resolve_partition(d["max_context_len"], part))).cuda()
+    ws = st.alloc_workspace(d["max_context_len"], part)
+    a, b = st.new_out(), st.new_out()
+    st.attention(d, a, ws, part, impl)
+    st.attention(dict(d, items=items), b, ws, part, impl)
+    torch.cuda.synchronize()
+    _no_device_error()
+    assert np.array_equal(from_device(a), from_device(b))
+    ref_out = oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"],
+                                     wl.scale, wl.dtype)
+    assert_close(from_device(b), ref_out, wl.dtype, f"{name} work list part={part}")
+
+
+def test_bad_work_item_is_recorded():
+    wl = make_workload("gqa8b", num_seqs=4)
+    st, d, _, _ = _build_pair(wl, compare_pool=False)
+    items = torch.tensor([[0, 0], [1, 0], [2, 0], [9, 0]], dtype=torch.int32, device="cuda")
+    pk.pk_get_device_error()
+    st.attention(dict(d, items=items), st.new_out(), None, 0, "mma")
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "order" and idx == 3
+
+
+@pytest.mark.parametrize("name", ["mixed", "long", "gqa8b"])
+def test_planned_work_list_full_size(name):
+    """The host plan (pk_attention_plan) at full size, as the benchmark runs it:
+    sampled rows against the oracle, every row bit for bit against the grid
+    launch at the plan's partition."""
+    wl = make_workload(name)
+    sel = _sample_rows(wl, wl.ctx_lens)
+    st, d, _, ref = _build_pair(wl, select=sel, compare_pool=False)
+    lens = from_device(d["ctx_lens"])
+    part, items = pk.pk_attention_plan(lens, wl.num_q_heads, st.desc, -1)
+    ws = st.alloc_workspace(d["max_context_len"], part)
+    a, b = st.new_out(), st.new_out()
+    st.attention(dict(d, items=torch.from_numpy(items).cuda(), partition=part), a, ws)
+    st.attention(d, b, ws, part)
+    torch.cuda.synchronize()
+    _no_device_error()
+    got = from_device(a)
+    assert np.array_equal(got, from_device(b))
+    rows_got = np.stack([got[s, h] for s, h in sel])
+    rows_ref = np.stack([ref["out"][s, h] for s, h in sel])
+    assert_close(rows_got, rows_ref, wl.dtype, f"{name} planned (partition {part})")

@@ -21,6 +21,9 @@ Workloads (shapes follow the pages' examples; all data is synthetic):
 * ``prefix`` 32 groups of 4 parallel samples sharing a 2000-token prompt, then
              1..500 divergent tokens each, 32 / 8 heads, head_dim 128, bf16,
              block size 8, 16 or 32, a pool of 524288 slots.
+* ``mixed``  one long request among short ones: 128 sequences, 32 query / 8 KV
+             heads, head_dim 128, bf16, 16-token blocks; 127 contexts uniform in
+             [256, 1024] and sequence 37 at 32768 tokens; 12288 blocks.
 * ``chat``   a chat server's decode batch: 128 requests, each one of 4 system
              prompts (1000, 1536, 2000, 600 tokens; popularity 1 : 1/2 : 1/3 :
              1/4) followed by a lognormal user turn (mean 200, sigma 1, capped
@@ -52,7 +55,7 @@ __all__ = [
     "ALLOCATOR_TRACES",
 ]
 
-WORKLOAD_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix", "chat")
+WORKLOAD_NAMES = ("tiny", "mha7b", "gqa8b", "long", "prefix", "chat", "mixed")
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -286,6 +289,12 @@ def make_workload(name: str, block_size: Optional[int] = None, num_seqs: Optiona
         div = rng.integers(1, 501, size=groups * n).astype(np.int64)
         wl = Workload("prefix", groups * n, 32, 8, 128, B, "bf16", 524288 // B, plen + div,
                       seed=seed, prefix_groups=groups, prefix_n=n, prefix_len=plen)
+    elif name == "mixed":
+        seed = 1139
+        rng = np.random.default_rng([seed, 0])
+        ctx = rng.integers(256, 1025, size=128).astype(np.int64)
+        ctx[37] = 32768
+        wl = Workload("mixed", 128, 32, 8, 128, 16, "bf16", 12288, ctx, seed=seed)
     elif name == "chat":
         seed = 1136
         rng = np.random.default_rng([seed, 0])
