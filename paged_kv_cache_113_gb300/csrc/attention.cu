@@ -344,6 +344,98 @@ struct MmaShape {
   static_assert(BS <= TPS && TPS % BS == 0 && BPS <= 32, "block size must divide the stage");
 };
 
+// One warp's 16-token tile: scores S^T (16 tokens x 8 query columns) =
+// K_tile Q^T, the online-softmax update of the running maxima m and sums l
+// (two query columns per lane: 2qd, 2qd+1) with the accumulator rescaled, and
+// O^T (D x 8) += V^T P^T. K and V are stored as D/64 slabs of `slab` bytes
+// (128-byte rows, 128B-swizzled); the tile is rows row0 .. row0+15, of which
+// the first nvalid (>= 1) hold tokens. Rows past them may hold stale or
+// unloaded data: their scores are -inf and their V rows are zeroed first, so a
+// zero weight never meets a NaN.
+template <int KSTEPS>
+__device__ __forceinline__ void attn_tile(uint32_t kbase, uint32_t vbase, int slab, int row0,
+                                          int nvalid, const uint32_t (&qb)[KSTEPS][2],
+                                          float (&o)[KSTEPS][4], float &m0, float &m1, float &l0,
+                                          float &l1, float sl, int lane) {
+  constexpr int HALVES = KSTEPS / 4;
+  const int rw = lane >> 2;
+  const int mi = lane >> 3, r8 = lane & 7;
+  if (nvalid < 16) {
+    const int nz = (16 - nvalid) * HALVES * 8;
+    for (int idx = lane; idx < nz; idx += 32) {
+      const int r = row0 + nvalid + idx / (HALVES * 8);
+      const int c = idx % (HALVES * 8);
+      const uint32_t a = vbase + (c >> 3) * slab + r * 128 + (c & 7) * 16;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+    }
+    __syncwarp();
+  }
+  // S^T = K_tile (16 x D) * Q^T (D x 8), as two independent accumulation
+  // chains (even and odd k-steps).
+  float sacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+#pragma unroll
+  for (int ks = 0; ks < KSTEPS; ++ks) {
+    const int r = row0 + (mi & 1) * 8 + r8;
+    const int chunk = ks * 2 + (mi >> 1);
+    const uint32_t a = kbase + (chunk >> 3) * slab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+    uint32_t a0, a1, a2, a3;
+    pk::ldmatrix_x4(a, a0, a1, a2, a3);
+    pk::mma_bf16_16816(sacc[ks & 1], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+  }
+  float x0 = (sacc[0][0] + sacc[1][0]) * sl, x1 = (sacc[0][1] + sacc[1][1]) * sl;
+  float x2 = (sacc[0][2] + sacc[1][2]) * sl, x3 = (sacc[0][3] + sacc[1][3]) * sl;
+  if (rw >= nvalid) x0 = x1 = -INFINITY;
+  if (rw + 8 >= nvalid) x2 = x3 = -INFINITY;
+  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: row 0 is valid
+  const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+  const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+  const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+  // Softmax weights enter the PV product as a bf16 pair hi + lo: rounding
+  // them to one bf16 would put ~2^-9 relative error on every output.
+  const uint32_t w01 = pk::pack_bf16x2(p0, p1);
+  const uint32_t w23 = pk::pack_bf16x2(p2, p3);
+  const uint32_t r01 = pk::pack_bf16x2(p0 - pk::bf16_lo(w01), p1 - pk::bf16_hi(w01));
+  const uint32_t r23 = pk::pack_bf16x2(p2 - pk::bf16_lo(w23), p3 - pk::bf16_hi(w23));
+  l0 = fmaf(l0, c0, p0 + p2);
+  l1 = fmaf(l1, c1, p1 + p3);
+  m0 = mn0;
+  m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt) {
+    o[mt][0] *= c0;
+    o[mt][1] *= c1;
+    o[mt][2] *= c0;
+    o[mt][3] *= c1;
+  }
+  // P^T (16 tokens x 8 heads) as the B operand: transpose the C fragments.
+  const uint32_t b0 = pk::movmatrix_trans(w01);
+  const uint32_t b1 = pk::movmatrix_trans(w23);
+  const uint32_t e0 = pk::movmatrix_trans(r01);
+  const uint32_t e1 = pk::movmatrix_trans(r23);
+  // O^T (D x 8) += V^T (D x 16 tokens) * P^T: all hi products first, then
+  // all lo products, so consecutive MMAs never share an accumulator.
+  uint32_t va[KSTEPS][4];
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt) {
+    const int r = row0 + (mi >> 1) * 8 + r8;
+    const int chunk = mt * 2 + (mi & 1);
+    const uint32_t a = vbase + (chunk >> 3) * slab + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+    pk::ldmatrix_x4_trans(a, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+  }
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt)
+    pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], b0, b1);
+#pragma unroll
+  for (int mt = 0; mt < KSTEPS; ++mt)
+    pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], e0, e1);
+}
+
 template <int D, int BS, int NW, int STAGES>
 __global__ void __launch_bounds__((NW + 1) * 32)
     attn_mma_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
@@ -469,7 +561,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   const float sl = p.scale_log2;
   const int row0 = warp * 16;
-  const int mi = lane >> 3, r8 = lane & 7;
 
   for (int st = 0; st < nst; ++st) {
     const int slot = st % STAGES;
@@ -480,86 +571,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const uint32_t kbase = stages + slot * S::STAGE_BYTES;
     const uint32_t vbase = kbase + S::KV_BYTES;
     const int nvalid = end - (start + st * S::TPS + row0);  // valid rows of this warp's tile
-    if (nvalid > 0) {
-      if (nvalid < 16) {
-        // Rows past the end hold stale or unloaded data: zero their V so that
-        // a zero softmax weight cannot meet a NaN.
-        const int nz = (16 - nvalid) * S::HALVES * 8;
-        for (int idx = lane; idx < nz; idx += 32) {
-          const int r = row0 + nvalid + idx / (S::HALVES * 8);
-          const int c = idx % (S::HALVES * 8);
-          const uint32_t a = vbase + (c >> 3) * S::SLAB_BYTES + r * 128 + (c & 7) * 16;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
-        }
-        __syncwarp();
-      }
-      // S^T (16 tokens x 8 heads) = K_tile (16 x D) * Q^T (D x 8), as two
-      // independent accumulation chains (even and odd k-steps).
-      float sacc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll
-      for (int ks = 0; ks < S::KSTEPS; ++ks) {
-        const int r = row0 + (mi & 1) * 8 + r8;
-        const int chunk = ks * 2 + (mi >> 1);
-        const uint32_t a = kbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
-                           (((chunk & 7) ^ (r & 7)) << 4);
-        uint32_t a0, a1, a2, a3;
-        pk::ldmatrix_x4(a, a0, a1, a2, a3);
-        pk::mma_bf16_16816(sacc[ks & 1], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-      }
-      float x0 = (sacc[0][0] + sacc[1][0]) * sl, x1 = (sacc[0][1] + sacc[1][1]) * sl;
-      float x2 = (sacc[0][2] + sacc[1][2]) * sl, x3 = (sacc[0][3] + sacc[1][3]) * sl;
-      if (rw >= nvalid) x0 = x1 = -INFINITY;
-      if (rw + 8 >= nvalid) x2 = x3 = -INFINITY;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: row 0 is valid
-      const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-      // Softmax weights enter the PV product as a bf16 pair hi + lo: rounding
-      // them to one bf16 would put ~2^-9 relative error on every output.
-      const uint32_t w01 = pk::pack_bf16x2(p0, p1);
-      const uint32_t w23 = pk::pack_bf16x2(p2, p3);
-      const uint32_t r01 = pk::pack_bf16x2(p0 - pk::bf16_lo(w01), p1 - pk::bf16_hi(w01));
-      const uint32_t r23 = pk::pack_bf16x2(p2 - pk::bf16_lo(w23), p3 - pk::bf16_hi(w23));
-      l0 = fmaf(l0, c0, p0 + p2);
-      l1 = fmaf(l1, c1, p1 + p3);
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < S::KSTEPS; ++mt) {
-        o[mt][0] *= c0;
-        o[mt][1] *= c1;
-        o[mt][2] *= c0;
-        o[mt][3] *= c1;
-      }
-      // P^T (16 tokens x 8 heads) as the B operand: transpose the C fragments.
-      const uint32_t b0 = pk::movmatrix_trans(w01);
-      const uint32_t b1 = pk::movmatrix_trans(w23);
-      const uint32_t e0 = pk::movmatrix_trans(r01);
-      const uint32_t e1 = pk::movmatrix_trans(r23);
-      // O^T (D x 8) += V^T (D x 16 tokens) * P^T: all hi products first, then
-      // all lo products, so consecutive MMAs never share an accumulator.
-      uint32_t va[S::KSTEPS][4];
-#pragma unroll
-      for (int mt = 0; mt < S::KSTEPS; ++mt) {
-        const int r = row0 + (mi >> 1) * 8 + r8;
-        const int chunk = mt * 2 + (mi & 1);
-        const uint32_t a = vbase + (chunk >> 3) * S::SLAB_BYTES + r * 128 +
-                           (((chunk & 7) ^ (r & 7)) << 4);
-        pk::ldmatrix_x4_trans(a, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < S::KSTEPS; ++mt)
-        pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], b0, b1);
-#pragma unroll
-      for (int mt = 0; mt < S::KSTEPS; ++mt)
-        pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], e0, e1);
-    }
+    if (nvalid > 0)
+      attn_tile<S::KSTEPS>(kbase, vbase, S::SLAB_BYTES, row0, nvalid, qb, o, m0, m1, l0, l1, sl,
+                           lane);
     __syncwarp();
     if (lane == 0) pk::mbar_arrive(empty_bar(slot));
   }
@@ -1025,9 +1039,10 @@ bool encode_pool_map_uncached(CUtensorMap *map, const void *pool, const pk_cache
 }
 
 // Opts the tensor-core kernel into its dynamic shared memory (once).
-// The pool's tensor map, encoded once per (pool address, geometry): a decode
-// loop launches on the same two pools every step. A few entries cover the K
-// and V pools of the layers a thread drives in turn.
+// The pool's tensor map (boxes of 64 columns x 1 head x one block), encoded
+// once per (pool address, geometry): a decode loop launches on the same two
+// pools every step. A few entries cover the K and V pools of the layers a
+// thread drives in turn.
 bool encode_pool_map(CUtensorMap *map, const void *pool, const pk_cache_desc &d) {
   struct Entry {
     const void *pool;
