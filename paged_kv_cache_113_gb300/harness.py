@@ -18,8 +18,8 @@ from typing import List, Optional
 
 import numpy as np
 
-from . import (BlockManager, pk_attention_plan, pk_attention_work_items, pk_cascade_attention_decode,
-               pk_cascade_workspace_size, pk_copy_blocks,
+from . import (BlockManager, pk_attention_plan, pk_cascade_attention_decode, pk_cascade_workspace_size,
+               pk_copy_blocks,
                pk_longest_first_order, pk_paged_attention_decode, pk_paged_attention_resolve_partition,
                pk_paged_attention_workspace_size, pk_reshape_and_cache, cache_desc)
 
@@ -179,13 +179,6 @@ class DecodeState:
             pk_copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
         pk_reshape_and_cache(d["k"], d["v"], d["slots"], self.k_cache, self.v_cache, stream=stream)
         self.attention(d, out, workspace, partition_size, impl, stream)
-
-    def work_items(self, si: StepInputs, partition_size: int = -1):
-        """The step's (sequence, partition) work list as a device tensor,
-        for the partition size the library resolves from the batch shape."""
-        import torch
-        part = self.resolve_partition(si.max_context_len, partition_size)
-        return torch.from_numpy(pk_attention_work_items(si.ctx_lens, max(part, 0))).to(self.device)
 
     def plan(self, si: StepInputs, partition_size: int = -1):
         """The step's planned partition and work list (pk_attention_plan on the
