@@ -11,19 +11,32 @@
 // partitions merged with a log-sum-exp reduction).
 //
 // Kernels:
-//   attn_mma_kernel   bf16. One CTA per (KV head, sequence, partition) serves
-//                     all G query heads of the group. A producer warp streams
-//                     the K and V rows of each block of the partition into a
-//                     ring of shared-memory stages with TMA tensor loads (the
-//                     physical block id from the table is the TMA coordinate),
-//                     128-byte swizzled. Consumer warps each take 16 tokens
-//                     per stage: S^T = K Q^T and O^T += V^T P^T on the tensor
-//                     cores (mma.sync m16n8k16, tokens as M, the group's heads
-//                     as N), with an online softmax in registers; the softmax
-//                     weights enter PV as a bf16 hi + lo pair.
-//   attn_simt_kernel  fp32 or bf16 on CUDA cores: one warp per token,
-//                     shuffle-reduced dot products, online softmax.
-//   attn_merge_kernel log-sum-exp merge of the split-K partials.
+//   attn_mma_kernel    bf16. One CTA per (KV head, sequence, partition) -- or
+//                      per (KV head, work item) of a host-planned list --
+//                      serves all G query heads of the group. A producer warp
+//                      streams the K and V rows of each block into a ring of
+//                      shared-memory stages with TMA tensor loads (the
+//                      physical block id from the table is the TMA
+//                      coordinate), 128-byte swizzled. Consumer warps each take
+//                      16 tokens per stage (attn_tile): S^T = K Q^T and
+//                      O^T += V^T P^T on the tensor cores (mma.sync m16n8k16,
+//                      tokens as M, the group's heads as N), with an online
+//                      softmax in registers; the softmax weights enter PV as a
+//                      bf16 hi + lo pair. Split partitions write partials and
+//                      the last one to finish merges them (log-sum-exp).
+//                      In cascade mode it covers each sequence's tokens after
+//                      its group's shared prefix.
+//   attn_prefix_kernel bf16, cascade attention: one CTA per (KV head, group,
+//                      prefix partition) streams a shared prefix once for all
+//                      of the group's query columns.
+//   attn_simt_kernel   fp32 or bf16 on CUDA cores: one warp per token,
+//                      shuffle-reduced dot products, online softmax.
+//   attn_merge_kernel  log-sum-exp merge of the CUDA-core kernel's partials.
+//
+// Host side: the entry points, the automatic partition (pk_paged_attention_
+// resolve_partition: fill the resident CTA slots once), the work-list
+// planner (pk_attention_plan, pk_attention_work_items) and the launch-order
+// helper.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>

@@ -6,8 +6,9 @@ pk_reshape_and_cache and pk_paged_attention_decode do the device work. The
 seeded inputs come from the ``workloads`` module.
 
 A decode step (one pass of the hot path) is, in order:
-  1. host: append one token to every sequence (pk_bm_append_batch) and export
-     the padded block tables and context lengths;
+  1. host: append one token to every sequence (pk_bm_append_batch), export
+     the padded block tables and context lengths, and order the work
+     (longest first, or a planned work list: DecodeState.plan);
   2. device: pk_copy_blocks for the step's copy-on-write pairs (if any),
      pk_reshape_and_cache of the new tokens' K/V, pk_paged_attention_decode.
 """
@@ -18,10 +19,9 @@ from typing import List, Optional
 
 import numpy as np
 
-from . import (BlockManager, pk_attention_plan, pk_cascade_attention_decode, pk_cascade_workspace_size,
-               pk_copy_blocks,
-               pk_longest_first_order, pk_paged_attention_decode, pk_paged_attention_resolve_partition,
-               pk_paged_attention_workspace_size, pk_reshape_and_cache, cache_desc)
+from . import (BlockManager, cache_desc, pk_attention_plan, pk_cascade_attention_decode,
+               pk_cascade_workspace_size, pk_copy_blocks, pk_longest_first_order, pk_paged_attention_decode,
+               pk_paged_attention_resolve_partition, pk_paged_attention_workspace_size, pk_reshape_and_cache)
 
 
 def to_device(a: np.ndarray, dtype: str, device):
