@@ -370,7 +370,7 @@ def run_ours(args):
 
     def launches(si, d):
         if groups is not None and groups["num_groups"]:
-            return (1 if len(si.pairs) else 0) + 3  # scatter, prefix kernel, suffix kernel
+            return (1 if len(si.pairs) else 0) + 2  # scatter, cascade kernel (prefix and suffix CTAs)
         part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
         return (1 if len(si.pairs) else 0) + 2 + (1 if split and simt else 0)
@@ -510,7 +510,7 @@ def run_ours(args):
                 "attention": (f"cascade: {groups['num_groups']} shared-prefix groups, prefix read once per group"
                               if groups is not None else "per sequence")}),
             "roofline": {"bound": "hbm",
-                         "kernel": ("attn_prefix_kernel + attn_mma_kernel" if groups is not None else
+                         "kernel": ("attn_cascade_kernel" if groups is not None else
                                     "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel"),
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",

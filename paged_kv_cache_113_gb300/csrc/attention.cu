@@ -26,9 +26,11 @@
 //                      the last one to finish merges them (log-sum-exp).
 //                      In cascade mode it covers each sequence's tokens after
 //                      its group's shared prefix.
-//   attn_prefix_kernel bf16, cascade attention: one CTA per (KV head, group,
-//                      prefix partition) streams a shared prefix once for all
-//                      of the group's query columns.
+//   attn_cascade_kernel bf16, cascade attention in one launch: prefix CTAs
+//                      (one per KV head, group and prefix partition) stream a
+//                      shared prefix once for all of the group's query
+//                      columns; suffix CTAs are attn_mma_kernel's in cascade
+//                      mode.
 //   attn_simt_kernel   fp32 or bf16 on CUDA cores: one warp per token,
 //                      shuffle-reduced dot products, online softmax.
 //   attn_merge_kernel  log-sum-exp merge of the CUDA-core kernel's partials.
@@ -103,38 +105,49 @@ __device__ __forceinline__ int context_len(const AttnParams &p, int s, bool reco
   return c;
 }
 
-// The sequence this CTA serves: order[blockIdx.y] when a launch order is
-// given (an out-of-range entry is recorded and falls back to blockIdx.y).
-__device__ __forceinline__ int launch_seq(const AttnParams &p) {
-  const int y = int(blockIdx.y);
+// A CTA's place in its kernel's (KV head, sequence or group, partition)
+// grid: the hardware block index, or a virtual one when one launch runs CTAs
+// of two kinds (cascade attention). nz is the grid's partition extent.
+struct CtaCoord {
+  int x, y, z, nz;
+};
+
+__device__ __forceinline__ CtaCoord hw_cta() {
+  return CtaCoord{int(blockIdx.x), int(blockIdx.y), int(blockIdx.z), int(gridDim.z)};
+}
+
+// The sequence this CTA serves: order[c.y] when a launch order is given (an
+// out-of-range entry is recorded and falls back to c.y).
+__device__ __forceinline__ int launch_seq(const AttnParams &p, const CtaCoord &c) {
+  const int y = c.y;
   if (!p.order) return y;
   const int s = __ldg(p.order + y);
   if (s < 0 || s >= p.num_seqs) {
-    if (blockIdx.x == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+    if (c.x == 0 && c.z == 0 && threadIdx.x == 0)
       pk::record_error(&g_attn_error, PK_DEVERR_ORDER, y);
     return y;
   }
   return s;
 }
 
-// The (sequence, partition) this CTA serves. With a work list: item
-// blockIdx.y (an entry outside the batch or the partition count is recorded
-// and the CTA does nothing). Otherwise sequence launch_seq() and partition
-// gridDim.z - 1 - blockIdx.z: partitions launch last-first, since the higher
-// ones exist only for the longest sequences.
-__device__ __forceinline__ bool work_of(const AttnParams &p, int &s, int &part) {
+// The (sequence, partition) this CTA serves. With a work list: item c.y (an
+// entry outside the batch or the partition count is recorded and the CTA does
+// nothing). Otherwise sequence launch_seq() and partition c.nz - 1 - c.z:
+// partitions launch last-first, since the higher ones exist only for the
+// longest sequences.
+__device__ __forceinline__ bool work_of(const AttnParams &p, const CtaCoord &c, int &s, int &part) {
   if (p.items) {
-    const int y = int(blockIdx.y);
+    const int y = c.y;
     s = __ldg(p.items + 2 * y);
     part = __ldg(p.items + 2 * y + 1);
     if (s < 0 || s >= p.num_seqs || part < 0 || part >= p.num_partitions - p.prefix_slots) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) pk::record_error(&g_attn_error, PK_DEVERR_ORDER, y);
+      if (c.x == 0 && threadIdx.x == 0) pk::record_error(&g_attn_error, PK_DEVERR_ORDER, y);
       return false;
     }
     return true;
   }
-  part = int(gridDim.z) - 1 - int(blockIdx.z);
-  s = launch_seq(p);
+  part = c.nz - 1 - c.z;
+  s = launch_seq(p, c);
   return true;
 }
 
@@ -222,9 +235,10 @@ template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnParams p) {
   constexpr int NW = 4;
   constexpr int EPL = D / 32;  // elements per lane
-  const int kvh = blockIdx.x;
+  const CtaCoord c = hw_cta();
+  const int kvh = c.x;
   int s, part;
-  if (!work_of(p, s, part)) return;
+  if (!work_of(p, c, s, part)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -449,10 +463,10 @@ __device__ __forceinline__ void attn_tile(uint32_t kbase, uint32_t vbase, int sl
     pk::mma_bf16_16816(o[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], e0, e1);
 }
 
+// The work of one attn_mma_kernel CTA at grid coordinate c.
 template <int D, int BS, int NW, int STAGES>
-__global__ void __launch_bounds__((NW + 1) * 32)
-    attn_mma_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
-                    const __grid_constant__ CUtensorMap vmap) {
+__device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *kmap,
+                                        const CUtensorMap *vmap, const CtaCoord c) {
   using S = MmaShape<D, BS, NW, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = pk::smem_addr(smem_raw);
@@ -463,9 +477,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
   // The caller's work list, or the grid in the caller's sequence order (longest
   // first keeps the longest work from trailing the launch).
-  const int kvh = blockIdx.x;
+  const int kvh = c.x;
   int s, part;
-  if (!work_of(p, s, part)) return;
+  if (!work_of(p, c, s, part)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int ctx = context_len(p, s, part == 0 && kvh == 0 && threadIdx.x == 0);
@@ -498,8 +512,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   if (warp == NW) {
     // ---------------- producer warp ----------------
     if (lane == 0) {
-      pk::prefetch_tensormap(&kmap);
-      pk::prefetch_tensormap(&vmap);
+      pk::prefetch_tensormap(kmap);
+      pk::prefetch_tensormap(vmap);
     }
     // The partition's table entries are read ahead in coalesced 32-entry
     // chunks (one entry per lane, one chunk in reserve), so no stage waits on
@@ -538,8 +552,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         const uint32_t kdst = stages + slot * S::STAGE_BYTES + lane * BS * 128;
 #pragma unroll
         for (int h = 0; h < S::HALVES; ++h) {
-          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, &kmap, full_bar(slot), h * 64, kvh, phys * BS);
-          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, &vmap, full_bar(slot), h * 64,
+          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, kmap, full_bar(slot), h * 64, kvh, phys * BS);
+          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, vmap, full_bar(slot), h * 64,
                           kvh, phys * BS);
         }
       }
@@ -668,6 +682,13 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   }
 }
 
+template <int D, int BS, int NW, int STAGES>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    attn_mma_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                    const __grid_constant__ CUtensorMap vmap) {
+  mma_cta<D, BS, NW, STAGES>(p, &kmap, &vmap, hw_cta());
+}
+
 // ---------------------------------------------------------------------------
 // Cascade attention, shared-prefix part (bf16, tensor cores).
 //
@@ -681,10 +702,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 // production": the shared prefix batched separately from the divergent
 // suffixes).
 // ---------------------------------------------------------------------------
+// The work of one prefix CTA of cascade attention at coordinate c (KV head,
+// group, prefix partition).
 template <int D, int BS, int NW, int STAGES>
-__global__ void __launch_bounds__((NW + 1) * 32)
-    attn_prefix_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap) {
+__device__ __forceinline__ void prefix_cta(const AttnParams &p, const CUtensorMap *kmap,
+                                           const CUtensorMap *vmap, const CtaCoord c) {
   using S = MmaShape<D, BS, NW, STAGES>;
   constexpr int NT = 2;            // n-tiles of 8 query columns
   constexpr int NC = 8 * NT;       // query columns per CTA
@@ -699,7 +721,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   auto full_bar = [&](int i) { return bars + 8u * i; };
   auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
 
-  const int kvh = blockIdx.x, grp = blockIdx.y;
+  const int kvh = c.x, grp = c.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int g0 = __ldg(p.group_offsets + grp);
@@ -707,7 +729,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   const int lead = __ldg(p.group_members + g0);
   const int pre = __ldg(p.group_prefix + grp);
   const int npre_g = (pre + p.partition - 1) / p.partition;
-  const int part = int(blockIdx.z);
+  const int part = c.z;
   if (part >= npre_g || nm <= 0 || nm * G > NC) return;
   const int start = part * p.partition;
   const int end = min(pre, start + p.partition);
@@ -726,8 +748,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   if (warp == NW) {
     // ---------------- producer warp (as in attn_mma_kernel) ----------------
     if (lane == 0) {
-      pk::prefetch_tensormap(&kmap);
-      pk::prefetch_tensormap(&vmap);
+      pk::prefetch_tensormap(kmap);
+      pk::prefetch_tensormap(vmap);
     }
     const int32_t *trow = p.tables + size_t(lead) * p.max_blocks + start / BS;
     const int nb = (end - start + BS - 1) / BS;
@@ -763,8 +785,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         const uint32_t kdst = stages + slot * S::STAGE_BYTES + lane * BS * 128;
 #pragma unroll
         for (int h = 0; h < S::HALVES; ++h) {
-          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, &kmap, full_bar(slot), h * 64, kvh, phys * BS);
-          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, &vmap, full_bar(slot), h * 64,
+          pk::tma_load_3d(kdst + h * S::SLAB_BYTES, kmap, full_bar(slot), h * 64, kvh, phys * BS);
+          pk::tma_load_3d(kdst + S::KV_BYTES + h * S::SLAB_BYTES, vmap, full_bar(slot), h * 64,
                           kvh, phys * BS);
         }
       }
@@ -983,6 +1005,31 @@ __global__ void __launch_bounds__((NW + 1) * 32)
   }
 }
 
+// Cascade attention in one launch: CTAs [0, npre) are prefix CTAs (KV head
+// fastest, then group, then prefix partition), the rest are suffix CTAs of
+// attn_mma_kernel in cascade mode (KV head fastest, then sequence in the
+// launch order, then partition, last first). The long prefix work starts
+// first and the short suffix work fills the SMs around and after it; one
+// launch pays one ramp-up and one drain. Both kinds use the same ring depth,
+// so they share one shared-memory size.
+template <int D, int BS, int NW, int STAGES>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    attn_cascade_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, int num_groups, int npre,
+                        int suffix_parts) {
+  const int b = int(blockIdx.x);
+  const int Hk = p.num_kv_heads;
+  if (b < npre) {
+    const int t = b / Hk;
+    prefix_cta<D, BS, NW, STAGES>(p, &kmap, &vmap,
+                                  CtaCoord{b % Hk, t % num_groups, t / num_groups, p.prefix_slots});
+  } else {
+    const int r = b - npre, t = r / Hk;
+    mma_cta<D, BS, NW, STAGES>(p, &kmap, &vmap,
+                               CtaCoord{r % Hk, t % p.num_seqs, t / p.num_seqs, suffix_parts});
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of split-K partials for the CUDA-core kernel (the
 // tensor-core kernel fuses the same merge into its last partition).
@@ -1117,21 +1164,23 @@ pk_status launch_mma(const AttnParams &p, const pk_cache_desc &d, cudaStream_t s
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
-// The prefix kernel holds 16 query columns (161 registers: 2 CTAs per SM),
-// so it affords a deeper ring than the suffix kernel.
+// Cascade CTAs hold up to 16 query columns (160 registers: 2 CTAs per SM),
+// so they afford a deeper ring than attn_mma_kernel alone.
 #ifndef PK_PREFIX_STAGES
 #define PK_PREFIX_STAGES 3
 #endif
 constexpr int kPrefixStages = PK_PREFIX_STAGES;
 
+// Cascade attention in one launch (attn_cascade_kernel): the prefix CTAs of
+// num_groups groups, then the suffix CTAs.
 template <int D, int BS>
-pk_status launch_prefix(const AttnParams &p, const pk_cache_desc &d, int num_groups,
-                        cudaStream_t stream) {
+pk_status launch_cascade(const AttnParams &p, const pk_cache_desc &d, int num_groups,
+                         cudaStream_t stream) {
   using S = MmaShape<D, BS, kMmaWarps, kPrefixStages>;
   CUtensorMap kmap, vmap;
   if (!encode_pool_map(&kmap, p.k_cache, d) || !encode_pool_map(&vmap, p.v_cache, d))
     return PK_ERR_CUDA;
-  auto kern = attn_prefix_kernel<D, BS, kMmaWarps, kPrefixStages>;
+  auto kern = attn_cascade_kernel<D, BS, kMmaWarps, kPrefixStages>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -1139,8 +1188,12 @@ pk_status launch_prefix(const AttnParams &p, const pk_cache_desc &d, int num_gro
                                     S::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return PK_ERR_CUDA;
-  dim3 grid(p.num_kv_heads, num_groups, p.prefix_slots);
-  kern<<<grid, (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap);
+  const int suffix_parts = p.num_partitions - p.prefix_slots;
+  const int64_t npre = int64_t(p.num_kv_heads) * num_groups * p.prefix_slots;
+  const int64_t total = npre + int64_t(p.num_kv_heads) * p.num_seqs * suffix_parts;
+  if (total > int64_t(INT32_MAX)) return PK_ERR_UNSUPPORTED;
+  kern<<<unsigned(total), (kMmaWarps + 1) * 32, S::SMEM_BYTES, stream>>>(p, kmap, vmap, num_groups,
+                                                                        int(npre), suffix_parts);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
@@ -1630,18 +1683,16 @@ pk_status pk_cascade_attention_decode(
   p.group_prefix = group_prefix_len;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, B = desc->block_size;
-  // The prefix grid first (its CTAs are the long ones), then the suffix grid;
+  // One launch: the prefix CTAs first (the long ones), then the suffix CTAs;
   // they meet only through the merge tickets.
   if (Ppre > 0) {
     if (D == 128)
-      st = B == 8 ? launch_prefix<128, 8>(p, *desc, num_groups, s)
-                  : (B == 16 ? launch_prefix<128, 16>(p, *desc, num_groups, s)
-                             : launch_prefix<128, 32>(p, *desc, num_groups, s));
-    else
-      st = B == 8 ? launch_prefix<64, 8>(p, *desc, num_groups, s)
-                  : (B == 16 ? launch_prefix<64, 16>(p, *desc, num_groups, s)
-                             : launch_prefix<64, 32>(p, *desc, num_groups, s));
-    if (st != PK_OK) return st;
+      return B == 8 ? launch_cascade<128, 8>(p, *desc, num_groups, s)
+                    : (B == 16 ? launch_cascade<128, 16>(p, *desc, num_groups, s)
+                               : launch_cascade<128, 32>(p, *desc, num_groups, s));
+    return B == 8 ? launch_cascade<64, 8>(p, *desc, num_groups, s)
+                  : (B == 16 ? launch_cascade<64, 16>(p, *desc, num_groups, s)
+                             : launch_cascade<64, 32>(p, *desc, num_groups, s));
   }
   if (D == 128)
     st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
