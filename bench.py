@@ -514,7 +514,8 @@ def run_ours(args):
                                     "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel"),
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
-                         "traffic": ncu_traffic(wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"),
+                         "traffic": ncu_traffic((wl.name if wl.name != "prefix" else f"prefix{wl.block_size}") +
+                                                ("_cascade" if groups is not None else "")),
                          "bytes_per_launch": total_bytes / args.steps, "ms_per_launch": 1e3 * t_attn / args.steps},
             "attention_gbs": attn_gbs,
             "attention_unique_gbs": total_unique / t_attn / 1e9,
