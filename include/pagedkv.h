@@ -587,6 +587,9 @@ typedef struct {
      * its partition size and item count (see pk_attention_plan). */
     int32_t plan_partition;
     int32_t plan_items;
+    /* Library-managed (NULL-initialise): the captured graph of the steady
+     * resident steps; free it with pk_decode_step_release. */
+    void *graph;
 } pk_step_buffers;
 
 /* Bytes of pk_step_buffers.meta_host / meta_dev for S sequences and tables of
@@ -615,11 +618,24 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  * the steps reach. The pages
  * have no counterpart for this packaging; each step it performs is theirs
  * (see the entry points above). On an error after step 2 the block manager
- * keeps the appended tokens and tables_resident is 0. */
+ * keeps the appended tokens and tables_resident is 0.
+ *
+ * On a stream the caller created (not the legacy or per-thread default
+ * stream, and not being captured), a steady resident step -- no
+ * copy-on-write pair, the same work list -- runs as one CUDA graph captured
+ * on the first such step: the input copies, the slot copy, the scatter, the
+ * attention and the output copy; only the q/k/v host addresses are patched
+ * when they change. The graph is rebuilt when the work list changes or after
+ * a full step. The per-step host work is then the block-manager append and
+ * one graph launch. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,
                          pk_step_buffers *buffers, void *stream);
+
+/* Frees the captured graph held in buffers->graph (if any) and sets it to
+ * NULL; call before freeing the buffers or destroying the stream. */
+void pk_decode_step_release(pk_step_buffers *buffers);
 
 #ifdef __cplusplus
 }

@@ -51,7 +51,7 @@ EXPORTED = (
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
-    "pk_decode_step_meta_bytes", "pk_decode_step",
+    "pk_decode_step_meta_bytes", "pk_decode_step", "pk_decode_step_release",
     "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
     "pk_swap_blocks", "pk_bm_set_swap_space", "pk_bm_swap_out", "pk_bm_swap_in", "pk_bm_is_swapped",
     "pk_bm_host_free", "pk_bm_add_seq_cached", "pk_bm_commit", "pk_bm_cache_match", "pk_bm_cache_stats",
@@ -75,7 +75,7 @@ class StepBuffers(ctypes.Structure):
                 ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("tables_resident", ctypes.c_int32), ("plan_partition", ctypes.c_int32),
-                ("plan_items", ctypes.c_int32)]
+                ("plan_items", ctypes.c_int32), ("graph", ctypes.c_void_p)]
 
 
 class SimRequest(ctypes.Structure):
@@ -166,6 +166,7 @@ def lib() -> ctypes.CDLL:
         "pk_sim_num_steps": (i32, [P, i32]),
         "pk_sim_run": (i32, [P, i32, i32, i32, i32, i32, ctypes.POINTER(SimSummary), P, i32]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
+        "pk_decode_step_release": (None, [ctypes.POINTER(StepBuffers)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -644,6 +645,9 @@ class DecodeStepper:
     synchronises; the output is then in ``out_host``. After the first step the
     block tables stay resident on the device and each step uploads only its
     slots and copy-on-write pairs; ``invalidate()`` forces a full upload.
+    Steps run on the stepper's own stream (``stream``), where steady steps
+    replay a captured CUDA graph; the first step, and the first after
+    ``invalidate()``, wait for the caller's current stream.
     """
 
     def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
@@ -656,6 +660,8 @@ class DecodeStepper:
         self.S, self.Hq, self.scale, self.maxb, self.partition = S, int(num_q_heads), float(scale), \
             int(max_blocks_per_seq), int(partition_size)
         dt, dev = k_cache.dtype, k_cache.device
+        self.stream = torch.cuda.Stream(device=dev)
+        self._order_after_caller = True
         self.q_host = torch.empty((S, self.Hq, d), dtype=dt).pin_memory()
         self.k_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
         self.v_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
@@ -685,27 +691,50 @@ class DecodeStepper:
         self.h2d_bytes_full = qkv + mb
         self.h2d_bytes_resident = qkv + (8 * S + 255) // 256 * 256   # + the work list when it changes
         self.h2d_bytes = self.h2d_bytes_full
+        # The call's arguments that never change, built once.
+        self._step_fn = lib().pk_decode_step
+        self._step_args = (bm._h, _np_ptr(self.ids), S, self.Hq, self.scale, self.maxb, self.partition,
+                           ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
+                           ctypes.byref(self.desc), ctypes.byref(self.buffers))
+        self._stream_arg = ctypes.c_void_p(self.stream.cuda_stream)
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
 
     def launch(self, stream=None, q_host=None, k_host=None, v_host=None):
         """Enqueues one step from q_host/k_host/v_host (the stepper's own pinned
-        buffers unless other pinned tensors are given)."""
+        buffers unless other pinned tensors are given) on ``stream`` (default:
+        the stepper's own stream, on which steady steps replay a captured graph)."""
         for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
             setattr(self.buffers, name, (getattr(self, name) if t is None else t).data_ptr())
-        _check(lib().pk_decode_step(self.bm._h, _np_ptr(self.ids), self.S, self.Hq, self.scale, self.maxb,
-                                    self.partition, ctypes.c_void_p(self.k_cache.data_ptr()),
-                                    ctypes.c_void_p(self.v_cache.data_ptr()), ctypes.byref(self.desc),
-                                    ctypes.byref(self.buffers), _stream(stream)), "pk_decode_step")
+        if self._order_after_caller:
+            # Work the caller enqueued before (the prefill, a copy after a
+            # fork) must finish before the step's kernels touch the pool.
+            self.stream.wait_stream(_torch().cuda.current_stream())
+            self._order_after_caller = False
+        st = self._stream_arg if stream is None else _stream(stream)
+        _check(self._step_fn(*self._step_args, st), "pk_decode_step")
+
+    def release(self):
+        """Frees the captured graph (the stepper stays usable)."""
+        if getattr(self, "buffers", None) is not None and self.buffers.graph:
+            lib().pk_decode_step_release(ctypes.byref(self.buffers))
+
+    def __del__(self):
+        try:
+            self.release()
+        except Exception:
+            pass
 
     def invalidate(self):
         """The next step exports and uploads the whole tables again (call it
-        after any block-manager change outside the stepper: fork, free, swap)."""
+        after any block-manager change outside the stepper: fork, free, swap).
+        The next step is also ordered after the caller's current stream."""
         self.buffers.tables_resident = 0
+        self._order_after_caller = True
 
     def step(self, stream=None):
         """One step and a stream synchronise; returns the host output tensor."""
         self.launch(stream)
-        (_torch().cuda.current_stream() if stream is None else stream).synchronize()
+        (self.stream if stream is None else stream).synchronize()
         return self.out_host
 
 

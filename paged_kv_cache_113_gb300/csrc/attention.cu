@@ -1430,10 +1430,10 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
   p.num_blocks = desc->num_blocks;
   if (P <= 1) {
     P = 1;
-    // One partition covering any context the table allows.
-    const int64_t cover = int64_t(max_context_len);
-    const int64_t rounded = (cover + desc->block_size - 1) / desc->block_size * desc->block_size;
-    p.partition = int32_t(rounded);
+    // One partition covering any context the table allows (independent of
+    // max_context_len, so that a step's launch parameters do not change as
+    // the contexts grow).
+    p.partition = int32_t(std::min<int64_t>(int64_t(max_blocks_per_seq) * desc->block_size, INT32_MAX));
   } else {
     p.partition = part;
   }

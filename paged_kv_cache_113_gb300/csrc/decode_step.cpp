@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <new>
 #include <vector>
 
 #include "pagedkv.h"
@@ -62,6 +63,39 @@ MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
 
 int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0); }
 
+// A captured resident step: the copies of q, k, v and the slots, the scatter
+// that advances the device tables, the attention over the unchanged work
+// list and the output copy. Every parameter of those is fixed while the work
+// list is, except the caller's q/k/v host addresses, which are patched.
+struct StepGraph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t copy_node[3] = {nullptr, nullptr, nullptr};  // q, k, v
+  const void *src[3] = {nullptr, nullptr, nullptr};
+  cudaStream_t stream = nullptr;
+  bool failed = false;  // capture is not possible on this stream: stop trying
+};
+
+void drop_graph(StepGraph *g) {
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  g->exec = nullptr;
+  g->graph = nullptr;
+  g->copy_node[0] = g->copy_node[1] = g->copy_node[2] = nullptr;
+}
+
+// A stream on which the library may capture: one the caller created, not the
+// legacy or per-thread default stream, and not being captured already.
+bool capturable(cudaStream_t s) {
+  if (s == nullptr || s == cudaStreamLegacy || s == cudaStreamPerThread) return false;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return cs == cudaStreamCaptureStatusNone;
+}
+
 }  // namespace
 
 extern "C" {
@@ -93,6 +127,7 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
   int32_t *items = reinterpret_cast<int32_t *>(mh + m.items);
   const bool resident = b->tables_resident != 0;
+  StepGraph *graph = static_cast<StepGraph *>(b->graph);
   // Resident mode keeps the previous step's lengths in meta_host; every row
   // must have room for one more token.
   if (resident)
@@ -100,14 +135,22 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
       if (int64_t(lens[i]) + 1 > int64_t(max_blocks_per_seq) * desc->block_size)
         return PK_ERR_INVALID_ARG;
 
-  // The step's tensors from the caller's host buffers: enqueued first, so
-  // the copies overlap the host block-manager work below.
   const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
   const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
-  if (cudaMemcpyAsync(b->q_dev, b->q_host, qbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(b->k_dev, b->k_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(b->v_dev, b->v_host, kvbytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return PK_ERR_CUDA;
+  const void *srcs[3] = {b->q_host, b->k_host, b->v_host};
+  void *dsts[3] = {b->q_dev, b->k_dev, b->v_dev};
+  const size_t sizes[3] = {qbytes, kvbytes, kvbytes};
+  auto enqueue_inputs = [&]() -> bool {
+    for (int k = 0; k < 3; ++k)
+      if (cudaMemcpyAsync(dsts[k], srcs[k], sizes[k], cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return false;
+    return true;
+  };
+
+  // The inputs are copied first, so the copies overlap the host work -- except
+  // on a resident step that may run as the captured graph (which copies them).
+  const bool may_replay = resident && !(graph && graph->failed) && capturable(s);
+  if (!may_replay && !enqueue_inputs()) return PK_ERR_CUDA;
 
   // Host side of the step.
   int32_t npairs = 0;
@@ -115,9 +158,9 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   if (st != PK_OK) return st;
   b->tables_resident = 0;  // until this step's metadata is on its way
   size_t meta_copy = m.total;
+  bool new_part = false;
   if (resident) {
     const int32_t part = b->plan_partition;
-    bool new_part = false;
     for (int32_t i = 0; i < num_seqs; ++i) {
       lens[i] += 1;
       if (part > 0 && (lens[i] - 1) % part == 0) new_part = true;
@@ -135,33 +178,109 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
                            items, m.item_cap, &b->plan_items);
     if (st != PK_OK) return st;
   }
+  if (graph && (!resident || new_part || graph->stream != s)) drop_graph(graph);
   const int32_t max_ctx = *std::max_element(lens, lens + num_seqs);
-  if (cudaMemcpyAsync(md, mh, meta_copy, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return PK_ERR_CUDA;
 
-  // Device side of the step.
-  if (npairs > 0) {
-    st = pk_copy_blocks(k_cache, v_cache, reinterpret_cast<const int64_t *>(md + m.pairs), npairs,
-                        desc, stream);
-    if (st != PK_OK) return st;
-  }
   const int64_t *dslots = reinterpret_cast<const int64_t *>(md + m.slots);
   int32_t *dtables = reinterpret_cast<int32_t *>(md + m.tables);
   int32_t *dlens = reinterpret_cast<int32_t *>(md + m.lens);
-  st = resident ? pk_reshape_and_cache_append(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache,
-                                              desc, dtables, max_blocks_per_seq, dlens, stream)
-                : pk_reshape_and_cache(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache, desc,
-                                       stream);
+  // Everything the device does in a step after the input copies.
+  auto enqueue_device = [&]() -> pk_status {
+    if (cudaMemcpyAsync(md, mh, meta_copy, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return PK_ERR_CUDA;
+    pk_status r = PK_OK;
+    if (npairs > 0) {
+      r = pk_copy_blocks(k_cache, v_cache, reinterpret_cast<const int64_t *>(md + m.pairs), npairs,
+                         desc, stream);
+      if (r != PK_OK) return r;
+    }
+    r = resident ? pk_reshape_and_cache_append(b->k_dev, b->v_dev, dslots, num_seqs, k_cache,
+                                               v_cache, desc, dtables, max_blocks_per_seq, dlens,
+                                               stream)
+                 : pk_reshape_and_cache(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache,
+                                        desc, stream);
+    if (r != PK_OK) return r;
+    r = pk_paged_attention_decode_items(
+        b->out_dev, b->q_dev, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
+        max_blocks_per_seq, max_ctx, b->plan_partition,
+        reinterpret_cast<const int32_t *>(md + m.items), b->plan_items, b->workspace,
+        b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
+    if (r != PK_OK) return r;
+    if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return PK_ERR_CUDA;
+    return PK_OK;
+  };
+
+  // A steady resident step (no copy-on-write pair, the same work list) runs
+  // as one captured graph.
+  const bool steady = may_replay && npairs == 0 && !new_part;
+  if (steady) {
+    if (!graph) {
+      graph = new (std::nothrow) StepGraph;
+      if (!graph) return PK_ERR_NOMEM;
+      b->graph = graph;
+    }
+    if (!graph->exec) {
+      graph->stream = s;
+      bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+      if (ok) {
+        const bool enq = enqueue_inputs() && enqueue_device() == PK_OK;
+        cudaGraph_t g = nullptr;
+        ok = cudaStreamEndCapture(s, &g) == cudaSuccess && enq && g;
+        graph->graph = g;
+        ok = ok && cudaGraphInstantiate(&graph->exec, g, 0) == cudaSuccess;
+        // The input copies' nodes, found by their destinations.
+        size_t n = 0;
+        if (ok) ok = cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess;
+        std::vector<cudaGraphNode_t> nodes(n);
+        if (ok && n) ok = cudaGraphGetNodes(g, nodes.data(), &n) == cudaSuccess;
+        for (size_t i = 0; ok && i < n; ++i) {
+          cudaGraphNodeType t;
+          if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeMemcpy)
+            continue;
+          cudaMemcpy3DParms mp{};
+          if (cudaGraphMemcpyNodeGetParams(nodes[i], &mp) != cudaSuccess) continue;
+          for (int k = 0; k < 3; ++k)
+            if (mp.dstPtr.ptr == dsts[k]) graph->copy_node[k] = nodes[i];
+        }
+        ok = ok && graph->copy_node[0] && graph->copy_node[1] && graph->copy_node[2];
+      }
+      if (!ok) {
+        cudaGetLastError();
+        drop_graph(graph);
+        graph->failed = true;
+        if (!enqueue_inputs()) return PK_ERR_CUDA;  // this step runs the normal way
+      } else {
+        for (int k = 0; k < 3; ++k) graph->src[k] = srcs[k];
+      }
+    }
+    if (graph->exec) {
+      for (int k = 0; k < 3; ++k)
+        if (graph->src[k] != srcs[k]) {
+          if (cudaGraphExecMemcpyNodeSetParams1D(graph->exec, graph->copy_node[k], dsts[k], srcs[k],
+                                                 sizes[k], cudaMemcpyHostToDevice) != cudaSuccess)
+            return PK_ERR_CUDA;
+          graph->src[k] = srcs[k];
+        }
+      if (cudaGraphLaunch(graph->exec, s) != cudaSuccess) return PK_ERR_CUDA;
+      b->tables_resident = 1;
+      return PK_OK;
+    }
+  }
+
+  if (may_replay && !steady && !enqueue_inputs()) return PK_ERR_CUDA;
+  st = enqueue_device();
   if (st != PK_OK) return st;
-  st = pk_paged_attention_decode_items(
-      b->out_dev, b->q_dev, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
-      max_blocks_per_seq, max_ctx, b->plan_partition, reinterpret_cast<const int32_t *>(md + m.items),
-      b->plan_items, b->workspace, b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
-  if (st != PK_OK) return st;
-  if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return PK_ERR_CUDA;
   b->tables_resident = 1;
   return PK_OK;
+}
+
+void pk_decode_step_release(pk_step_buffers *b) {
+  if (!b || !b->graph) return;
+  StepGraph *g = static_cast<StepGraph *>(b->graph);
+  drop_graph(g);
+  delete g;
+  b->graph = nullptr;
 }
 
 }  // extern "C"
