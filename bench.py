@@ -3,8 +3,11 @@
 
 One step = one decode step of the whole hot path over one batch: the host
 block manager appends one token to every sequence (slots, copy-on-write pairs,
-block tables), then pk_copy_blocks (when pairs exist), pk_reshape_and_cache
-and pk_paged_attention_decode (+ its log-sum-exp merge when it splits).
+block tables) and plans the attention's work list, then pk_copy_blocks (when
+pairs exist) and pk_paged_attention_decode_append -- the attention with the
+slot scatter of the step's new K/V fused into the same launch (and its
+log-sum-exp merge when it splits). --no-fuse runs pk_reshape_and_cache as its
+own kernel; --grid / --no-order launch the (sequence, partition) grid.
 
 Device timing (``value``): the host side of a window of steps is prepared and
 uploaded before the timed region, so inputs are resident in HBM; each timed
@@ -68,6 +71,8 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graphs", action="store_true", help="launch the timed steps eagerly, not as CUDA graphs")
     p.add_argument("--no-order", action="store_true", help="launch sequences in index order, not longest first")
+    p.add_argument("--no-fuse", action="store_true",
+                   help="run the slot scatter as its own kernel instead of inside the attention launch")
     p.add_argument("--grid", action="store_true",
                    help="launch the (sequence, partition) grid in longest-first sequence order instead of the "
                         "planned work list")
@@ -335,6 +340,9 @@ def run_ours(args):
     host_steps = [st.prepare_step() for _ in range(R)]
     dsteps = [st.upload(si) for si in host_steps]
     planned = not (args.cascade or args.grid or args.no_order)
+    # The default step: copy-on-write copies (if any), then one attention
+    # launch that also writes the step's new K/V (the scatter fused in).
+    fused = planned and not args.no_fuse and args.attn_impl == "auto"
     if planned:
         # The default schedule: each step's work list from the host planner
         # (pk_attention_plan), longest item first.
@@ -373,12 +381,14 @@ def run_ours(args):
             return (1 if len(si.pairs) else 0) + 2  # scatter, cascade kernel (prefix and suffix CTAs)
         part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, args.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
-        return (1 if len(si.pairs) else 0) + 2 + (1 if split and simt else 0)
+        scatter = 0 if fused and not simt else 1
+        return (1 if len(si.pairs) else 0) + scatter + 1 + (1 if split and simt else 0)
 
     def cache_writes(d):
         if d["pairs"].shape[0]:
             pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
-        pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
+        if not fused:
+            pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
 
     groups = st.cascade_groups() if args.cascade else None
     if groups is not None:
@@ -387,6 +397,10 @@ def run_ours(args):
     def attend(d):
         if groups is not None:
             st.attention_cascade(d, out, groups, ws, args.partition, ordered=not args.no_order)
+        elif fused:
+            pk.pk_paged_attention_decode_append(out, d["q"], d["k"], d["v"], d["slots"], st.k_cache, st.v_cache,
+                                                d["tables"], d["ctx_lens"], wl.scale, d["max_context_len"],
+                                                d["partition"], d["items"], ws)
         else:
             st.attention(d, out, ws, args.partition, args.attn_impl, ordered=not args.no_order)
 
@@ -406,9 +420,11 @@ def run_ours(args):
     if not args.no_graphs:
         graphs = []
         for d in dsteps:
-            g_w, g_a = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_w):
-                cache_writes(d)
+            g_w, g_a = None, torch.cuda.CUDAGraph()
+            if d["pairs"].shape[0] or not fused:  # nothing to capture when the scatter is fused
+                g_w = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_w):
+                    cache_writes(d)
             with torch.cuda.graph(g_a):
                 attend(d)
             graphs.append((g_w, g_a))
@@ -439,7 +455,8 @@ def run_ours(args):
         e0, e1, e2 = ev[i]
         e0.record()
         if graphs:
-            graphs[j][0].replay()
+            if graphs[j][0] is not None:
+                graphs[j][0].replay()
         else:
             cache_writes(d)
         e1.record()
@@ -505,6 +522,7 @@ def run_ours(args):
                 "kv_bytes_per_step_mean": total_bytes / args.steps,
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
                 "launch": "CUDA graphs per step" if graphs else "eager",
+                "scatter": "fused into the attention launch" if fused else "own kernel",
                 "seq_order": "index" if args.no_order else
                              ("planned work list, longest item first (host)" if planned else "longest first (host)"),
                 "attention": (f"cascade: {groups['num_groups']} shared-prefix groups, prefix read once per group"

@@ -221,6 +221,22 @@ pk_status pk_paged_attention_decode_items(void *out, const void *q, const void *
                                           size_t workspace_bytes, const pk_cache_desc *desc,
                                           pk_attn_impl impl, void *stream);
 
+/* One decode step's slot scatter fused into its attention: as
+ * pk_reshape_and_cache(k_new, v_new, slot_mapping, num_seqs, ...) followed by
+ * pk_paged_attention_decode_items, where token i of k_new / v_new
+ * ([num_seqs, Hk, d]) is the last token of sequence i (its context length
+ * counts it). The tensor-core kernel writes each sequence's new K/V for a KV
+ * head in the CTA that then reads that head -- the one whose partition holds
+ * the token -- ordering the write before its TMA reads, so the step needs no
+ * separate scatter launch; otherwise the scatter runs first as its own
+ * kernel. Copy-on-write copies (pk_copy_blocks) must be enqueued before. */
+pk_status pk_paged_attention_decode_append(
+    void *out, const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+    void *k_cache, void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+    float scale, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+    int32_t max_context_len, int32_t partition_size, const int32_t *work_items, int32_t num_items,
+    void *workspace, size_t workspace_bytes, const pk_cache_desc *desc, void *stream);
+
 /* Host helper for pk_paged_attention_decode_items: the items of sequences
  * with host context_lens [n] cut into partitions of `partition` tokens (0 = no
  * split; pass the resolved size), longest item first (ties: the longer

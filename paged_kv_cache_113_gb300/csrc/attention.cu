@@ -91,6 +91,12 @@ struct AttnParams {
   // instead of the (sequence, partition) grid; null when not used.
   const int32_t *items;
   int32_t num_items;
+  // Fused scatter: token s of new_k / new_v ([S, Hk, D]) is sequence s's last
+  // token, to be written to slot new_slots[s] before it is read; null when the
+  // caller scattered already.
+  const void *new_k;
+  const void *new_v;
+  const int64_t *new_slots;
 };
 
 // Context length of sequence s, clamped to what the table and the grid can
@@ -363,7 +369,7 @@ struct MmaShape {
   static constexpr int KSTEPS = D / 16;
   static constexpr int OUT_STRIDE = D + 4;          // padded row of the merge buffer
   static constexpr int MERGE_BYTES = NW * kMaxGroup * (OUT_STRIDE + 2) * 4 + 16;
-  static constexpr int BAR_BYTES = 2 * STAGES * 8;
+  static constexpr int BAR_BYTES = 2 * STAGES * 8 + 8;  // full, empty, scatter-done
   static constexpr int SMEM_BYTES = 1024 + BAR_BYTES +
                                     (STAGES * STAGE_BYTES > MERGE_BYTES ? STAGES * STAGE_BYTES
                                                                         : MERGE_BYTES);
@@ -474,6 +480,7 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
   const uint32_t stages = (bars + S::BAR_BYTES + 1023u) & ~1023u;
   auto full_bar = [&](int i) { return bars + 8u * i; };
   auto empty_bar = [&](int i) { return bars + 8u * (STAGES + i); };
+  const uint32_t scatter_bar = bars + 8u * (2 * STAGES);
 
   // The caller's work list, or the grid in the caller's sequence order (longest
   // first keeps the longest work from trailing the launch).
@@ -500,14 +507,39 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
   const int npre = (pre + p.partition - 1) / p.partition;
   const int nsuf = (ctx - pre + p.partition - 1) / p.partition;
 
+  // Fused scatter: the CTA whose partition holds the sequence's new (last)
+  // token writes that token's K and V for this KV head -- exactly the slice
+  // it reads. Consumer warp 0 writes them at its start and arrives on
+  // scatter_bar after a proxy fence; the producer waits on it only before the
+  // last stage's copies (the tail block), so the write costs no latency.
+  const bool fuse = p.new_k && end == ctx;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       pk::mbar_init(full_bar(i), 1);
       pk::mbar_init(empty_bar(i), NW);
     }
+    pk::mbar_init(scatter_bar, 32);
     pk::fence_barrier_init();
   }
   __syncthreads();
+
+  if (fuse && warp == 0) {
+    constexpr int VEC = D * 2 / 16;  // 16-byte vectors of one head's row
+    const int64_t slot = __ldg(p.new_slots + s);
+    if (slot < 0 || slot >= int64_t(p.num_blocks) * BS) {
+      if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_SLOT, s);
+    } else if (lane < 2 * VEC) {
+      const bool is_v = lane >= VEC;
+      const int j = is_v ? lane - VEC : lane;
+      const size_t row = size_t(s) * p.num_kv_heads + kvh;
+      const uint4 *src = static_cast<const uint4 *>(is_v ? p.new_v : p.new_k) + row * VEC + j;
+      uint4 *dst = static_cast<uint4 *>(const_cast<void *>(is_v ? p.v_cache : p.k_cache)) +
+                   (size_t(slot) * p.num_kv_heads + kvh) * VEC + j;
+      *dst = __ldg(src);
+      pk::fence_proxy_async();
+    }
+    pk::mbar_arrive(scatter_bar);
+  }
 
   if (warp == NW) {
     // ---------------- producer warp ----------------
@@ -535,6 +567,10 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
       }
       const int mine = __shfl_sync(0xffffffffu, cur, (b0 & 31) + min(lane, S::BPS - 1));
       if (st >= STAGES && !pk::mbar_wait(empty_bar(slot), ((st / STAGES) - 1) & 1)) {
+        if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, s);
+        break;
+      }
+      if (fuse && st == nst - 1 && !pk::mbar_wait(scatter_bar, 0)) {
         if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, s);
         break;
       }
@@ -1400,7 +1436,8 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
                            int32_t max_context_len, int32_t partition_size, void *workspace,
                            size_t workspace_bytes, const pk_cache_desc *desc,
                            const int32_t *seq_order, const int32_t *items, int32_t num_items,
-                           pk_attn_impl impl, void *stream) {
+                           pk_attn_impl impl, void *stream, const void *new_k = nullptr,
+                           const void *new_v = nullptr, const int64_t *new_slots = nullptr) {
   pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
   if (st != PK_OK) return st;
   if (num_seqs == 0) return PK_OK;
@@ -1461,6 +1498,18 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
   const bool use_mma = impl == PK_ATTN_MMA || (impl == PK_ATTN_AUTO && mma_ok);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, B = desc->block_size;
+  if (new_k) {
+    if (!new_v || !new_slots || !aligned16(new_k) || !aligned16(new_v)) return PK_ERR_INVALID_ARG;
+    if (use_mma) {  // the tensor-core kernel writes the new tokens itself
+      p.new_k = new_k;
+      p.new_v = new_v;
+      p.new_slots = new_slots;
+    } else {
+      st = pk_reshape_and_cache(new_k, new_v, new_slots, num_seqs, const_cast<void *>(k_cache),
+                                const_cast<void *>(v_cache), desc, stream);
+      if (st != PK_OK) return st;
+    }
+  }
   if (use_mma) {
     if (P > 1) {
       p.merge_tickets = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + pbytes);
@@ -1516,6 +1565,19 @@ pk_status pk_paged_attention_decode_items(void *out, const void *q, const void *
                           num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
                           workspace, workspace_bytes, desc, nullptr, work_items, num_items, impl,
                           stream);
+}
+
+pk_status pk_paged_attention_decode_append(
+    void *out, const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+    void *k_cache, void *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+    float scale, int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq,
+    int32_t max_context_len, int32_t partition_size, const int32_t *work_items, int32_t num_items,
+    void *workspace, size_t workspace_bytes, const pk_cache_desc *desc, void *stream) {
+  if (!work_items || !k_new || !v_new || !slot_mapping) return PK_ERR_INVALID_ARG;
+  return decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                          num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
+                          workspace, workspace_bytes, desc, nullptr, work_items, num_items,
+                          PK_ATTN_AUTO, stream, k_new, v_new, slot_mapping);
 }
 
 pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,

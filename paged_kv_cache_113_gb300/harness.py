@@ -21,7 +21,8 @@ import numpy as np
 
 from . import (BlockManager, cache_desc, pk_attention_plan, pk_cascade_attention_decode,
                pk_cascade_workspace_size, pk_copy_blocks, pk_longest_first_order, pk_paged_attention_decode,
-               pk_paged_attention_resolve_partition, pk_paged_attention_workspace_size, pk_reshape_and_cache)
+               pk_paged_attention_decode_append, pk_paged_attention_resolve_partition,
+               pk_paged_attention_workspace_size, pk_reshape_and_cache)
 
 
 def to_device(a: np.ndarray, dtype: str, device):
@@ -186,6 +187,16 @@ class DecodeState:
         import torch
         part, items = pk_attention_plan(si.ctx_lens, self.wl.num_q_heads, self.desc, partition_size)
         return part, torch.from_numpy(items).to(self.device)
+
+    def run_step_fused(self, d: dict, out, workspace=None, stream=None):
+        """The step with its scatter fused into the attention (needs the plan's
+        ``items`` and ``partition`` in ``d``): copy_blocks (if pairs), then
+        pk_paged_attention_decode_append."""
+        if d["pairs"].shape[0]:
+            pk_copy_blocks(self.k_cache, self.v_cache, d["pairs"], stream=stream)
+        pk_paged_attention_decode_append(out, d["q"], d["k"], d["v"], d["slots"], self.k_cache, self.v_cache,
+                                         d["tables"], d["ctx_lens"], self.wl.scale, d["max_context_len"],
+                                         d["partition"], d["items"], workspace, stream)
 
     def attention(self, d: dict, out, workspace=None, partition_size: int = -1, impl: str = "auto",
                   stream=None, ordered: bool = True):

@@ -422,3 +422,52 @@ def test_planned_work_list_full_size(name):
     rows_got = np.stack([got[s, h] for s, h in sel])
     rows_ref = np.stack([ref["out"][s, h] for s, h in sel])
     assert_close(rows_got, rows_ref, wl.dtype, f"{name} planned (partition {part})")
+
+
+FUSED_CASES = [("gqa8b", 40, None, -1), ("gqa8b", 40, None, 256), ("long", 2, None, -1), ("mixed", 40, None, -1),
+               ("prefix", 8, 8, -1), ("prefix", 8, 32, 512), ("mha7b", 8, None, -1), ("tiny", None, None, -1),
+               ("chat", 12, None, -1)]
+
+
+@pytest.mark.parametrize("name,nseq,B,part", FUSED_CASES)
+def test_scatter_fused_into_attention(name, nseq, B, part):
+    """pk_paged_attention_decode_append (the step's scatter inside the
+    attention launch) against the separate scatter + attention: pools and
+    outputs bit for bit, and the oracle's step within tolerance."""
+    wl = make_workload(name, num_seqs=nseq, block_size=B)
+    wl.enable_memo()
+    ref = oracle.run_workload(wl)
+    outs, pools = [], []
+    for fused in (False, True):
+        st = DecodeState(wl, "cuda")
+        si = st.prepare_step(0)
+        d = st.upload(si)
+        d["partition"], d["items"] = st.plan(si, part)
+        ws = st.alloc_workspace(d["max_context_len"], d["partition"])
+        out = st.new_out()
+        if fused:
+            st.run_step_fused(d, out, ws)
+        else:
+            st.run_step(d, out, ws, d["partition"])
+        torch.cuda.synchronize()
+        _no_device_error()
+        outs.append(from_device(out))
+        pools.append((from_device(st.k_cache), from_device(st.v_cache)))
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(pools[0][0], pools[1][0]) and np.array_equal(pools[0][1], pools[1][1])
+    assert np.array_equal(pools[1][0], ref["k_cache"]) and np.array_equal(pools[1][1], ref["v_cache"])
+    assert_close(outs[1], ref["out"], wl.dtype, f"{name} fused part={part}")
+
+
+def test_fused_scatter_bad_slot_is_recorded():
+    wl = make_workload("gqa8b", num_seqs=4)
+    st = DecodeState(wl, "cuda")
+    si = st.prepare_step(0)
+    d = st.upload(si)
+    d["partition"], d["items"] = st.plan(si, -1)
+    bad = d["slots"].clone()
+    bad[2] = wl.num_blocks * wl.block_size + 5
+    pk.pk_get_device_error()
+    st.run_step_fused(dict(d, slots=bad), st.new_out(), None)
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "slot" and idx == 2
