@@ -577,18 +577,21 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
 /* ------------------------------------------------------------------------ */
 /* Buffers of pk_decode_step. Host pointers should be pinned (page-locked) so
  * the copies are asynchronous; device pointers are caller-owned, 16-byte
- * aligned. */
+ * aligned. With q_dev, k_dev, v_dev and out_dev all NULL (zero-copy mode) the
+ * host buffers must be pinned, device-mapped memory: the kernels read q and
+ * the new K/V from, and write the output to, them directly -- the same bytes
+ * cross the host link, inside the kernels rather than as separate copies. */
 typedef struct {
     const void *q_host;  /* [S, Hq, d] queries of the step                     */
     const void *k_host;  /* [S, Hk, d] the step's new keys                      */
     const void *v_host;  /* [S, Hk, d] the step's new values                    */
-    void *q_dev;         /* device copies of the three above                   */
+    void *q_dev;         /* device copies of the three above (NULL: zero-copy) */
     void *k_dev;
     void *v_dev;
     void *meta_host;     /* pinned staging of pk_decode_step_meta_bytes bytes  */
     void *meta_dev;      /* device staging of the same size                    */
     size_t meta_bytes;
-    void *out_dev;       /* [S, Hq, d] attention output on the device           */
+    void *out_dev;       /* [S, Hq, d] attention output on the device (or NULL) */
     void *out_host;      /* [S, Hq, d] its host copy                            */
     void *workspace;     /* split-K workspace (see pk_paged_attention_decode)   */
     size_t workspace_bytes;
@@ -641,8 +644,9 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  * copy-on-write pair, the same work list -- runs as one CUDA graph captured
  * on the first such step: the input copies, the slot copy, the scatter, the
  * attention and the output copy; only the q/k/v host addresses are patched
- * when they change. The graph is rebuilt when the work list changes or after
- * a full step. The per-step host work is then the block-manager append and
+ * when they change (in zero-copy mode, or when out_host changes, the graph
+ * is rebuilt instead). The graph is rebuilt when the work list changes or
+ * after a full step. The per-step host work is then the block-manager append and
  * one graph launch. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,

@@ -673,11 +673,15 @@ class DecodeStepper:
     slots and copy-on-write pairs; ``invalidate()`` forces a full upload.
     Steps run on the stepper's own stream (``stream``), where steady steps
     replay a captured CUDA graph; the first step, and the first after
-    ``invalidate()``, wait for the caller's current stream.
+    ``invalidate()``, wait for the caller's current stream. ``zero_copy``: the
+    kernels read the inputs from, and write the output to, the stepper's
+    pinned host buffers directly (fill ``q_host``/``k_host``/``v_host`` before
+    each step).
     """
 
     def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
-                 k_cache, v_cache, partition_size: int = -1, max_context_len: Optional[int] = None):
+                 k_cache, v_cache, partition_size: int = -1, max_context_len: Optional[int] = None,
+                 zero_copy: bool = False):
         torch = _torch()
         self.bm, self.k_cache, self.v_cache = bm, k_cache, v_cache
         self.desc = cache_desc(k_cache)
@@ -692,10 +696,16 @@ class DecodeStepper:
         self.k_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
         self.v_host = torch.empty((S, Hk, d), dtype=dt).pin_memory()
         self.out_host = torch.empty((S, self.Hq, d), dtype=dt).pin_memory()
-        self.q_dev = torch.empty_like(self.q_host, device=dev)
-        self.k_dev = torch.empty_like(self.k_host, device=dev)
-        self.v_dev = torch.empty_like(self.v_host, device=dev)
-        self.out_dev = torch.empty_like(self.out_host, device=dev)
+        # Zero-copy: the kernels read the inputs from, and write the output to,
+        # the pinned host buffers directly (no device copies).
+        self.zero_copy = bool(zero_copy)
+        if self.zero_copy:
+            self.q_dev = self.k_dev = self.v_dev = self.out_dev = None
+        else:
+            self.q_dev = torch.empty_like(self.q_host, device=dev)
+            self.k_dev = torch.empty_like(self.k_host, device=dev)
+            self.v_dev = torch.empty_like(self.v_host, device=dev)
+            self.out_dev = torch.empty_like(self.out_host, device=dev)
         mb = int(lib().pk_decode_step_meta_bytes(S, self.maxb))
         self.meta_host = torch.empty(mb, dtype=torch.uint8).pin_memory()
         self.meta_dev = torch.empty(mb, dtype=torch.uint8, device=dev)
@@ -704,11 +714,12 @@ class DecodeStepper:
         wsb = pk_paged_attention_workspace_size(S, self.Hq, mc, 512 if self.partition == -1 else self.partition,
                                                 self.desc)
         self.workspace = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev) if wsb else None
+        ptr = lambda t: None if t is None else t.data_ptr()
         self.buffers = StepBuffers(
             self.q_host.data_ptr(), self.k_host.data_ptr(), self.v_host.data_ptr(),
-            self.q_dev.data_ptr(), self.k_dev.data_ptr(), self.v_dev.data_ptr(),
+            ptr(self.q_dev), ptr(self.k_dev), ptr(self.v_dev),
             self.meta_host.data_ptr(), self.meta_dev.data_ptr(), mb,
-            self.out_dev.data_ptr(), self.out_host.data_ptr(),
+            ptr(self.out_dev), self.out_host.data_ptr(),
             None if self.workspace is None else self.workspace.data_ptr(), wsb)
         qkv = (self.q_host.numel() + self.k_host.numel() + self.v_host.numel()) * self.q_host.element_size()
         # Host -> device bytes of a step: the whole metadata buffer on a full

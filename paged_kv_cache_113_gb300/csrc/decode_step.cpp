@@ -72,8 +72,10 @@ struct StepGraph {
   cudaGraphExec_t exec = nullptr;
   cudaGraphNode_t copy_node[3] = {nullptr, nullptr, nullptr};  // q, k, v
   const void *src[3] = {nullptr, nullptr, nullptr};
+  const void *out = nullptr;  // the host output buffer the graph writes
   cudaStream_t stream = nullptr;
-  bool failed = false;  // capture is not possible on this stream: stop trying
+  bool zero_copy = false;  // captured in zero-copy mode (no copy nodes)
+  bool failed = false;     // capture is not possible on this stream: stop trying
 };
 
 void drop_graph(StepGraph *g) {
@@ -113,9 +115,23 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
     return PK_ERR_INVALID_ARG;
   const int64_t esz = elem_size(desc->dtype);
   if (esz == 0) return PK_ERR_UNSUPPORTED;
-  if (!b->q_host || !b->k_host || !b->v_host || !b->q_dev || !b->k_dev || !b->v_dev ||
-      !b->meta_host || !b->meta_dev || !b->out_dev || !b->out_host)
+  if (!b->q_host || !b->k_host || !b->v_host || !b->meta_host || !b->meta_dev || !b->out_host)
     return PK_ERR_INVALID_ARG;
+  // Zero-copy mode (no device copies given): the kernels read q and the new
+  // K/V from, and write the output to, the pinned host buffers through their
+  // device mappings; the bytes still cross the host link every step, inside
+  // the kernels instead of as separate copies.
+  const bool zero_copy = !b->q_dev && !b->k_dev && !b->v_dev && !b->out_dev;
+  if (!zero_copy && (!b->q_dev || !b->k_dev || !b->v_dev || !b->out_dev)) return PK_ERR_INVALID_ARG;
+  void *qd = b->q_dev, *kd = b->k_dev, *vd = b->v_dev, *od = b->out_dev;
+  if (zero_copy &&
+      (cudaHostGetDevicePointer(&qd, const_cast<void *>(b->q_host), 0) != cudaSuccess ||
+       cudaHostGetDevicePointer(&kd, const_cast<void *>(b->k_host), 0) != cudaSuccess ||
+       cudaHostGetDevicePointer(&vd, const_cast<void *>(b->v_host), 0) != cudaSuccess ||
+       cudaHostGetDevicePointer(&od, b->out_host, 0) != cudaSuccess)) {
+    cudaGetLastError();
+    return PK_ERR_INVALID_ARG;  // not pinned, mapped host memory
+  }
   const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
   if (b->meta_bytes < m.total) return PK_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -138,9 +154,10 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
   const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
   const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
   const void *srcs[3] = {b->q_host, b->k_host, b->v_host};
-  void *dsts[3] = {b->q_dev, b->k_dev, b->v_dev};
+  void *dsts[3] = {qd, kd, vd};
   const size_t sizes[3] = {qbytes, kvbytes, kvbytes};
   auto enqueue_inputs = [&]() -> bool {
+    if (zero_copy) return true;
     for (int k = 0; k < 3; ++k)
       if (cudaMemcpyAsync(dsts[k], srcs[k], sizes[k], cudaMemcpyHostToDevice, s) != cudaSuccess)
         return false;
@@ -194,19 +211,18 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
                          desc, stream);
       if (r != PK_OK) return r;
     }
-    r = resident ? pk_reshape_and_cache_append(b->k_dev, b->v_dev, dslots, num_seqs, k_cache,
-                                               v_cache, desc, dtables, max_blocks_per_seq, dlens,
-                                               stream)
-                 : pk_reshape_and_cache(b->k_dev, b->v_dev, dslots, num_seqs, k_cache, v_cache,
-                                        desc, stream);
+    r = resident ? pk_reshape_and_cache_append(kd, vd, dslots, num_seqs, k_cache, v_cache, desc,
+                                               dtables, max_blocks_per_seq, dlens, stream)
+                 : pk_reshape_and_cache(kd, vd, dslots, num_seqs, k_cache, v_cache, desc, stream);
     if (r != PK_OK) return r;
     r = pk_paged_attention_decode_items(
-        b->out_dev, b->q_dev, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
+        od, qd, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
         max_blocks_per_seq, max_ctx, b->plan_partition,
         reinterpret_cast<const int32_t *>(md + m.items), b->plan_items, b->workspace,
         b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
     if (r != PK_OK) return r;
-    if (cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (!zero_copy &&
+        cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
       return PK_ERR_CUDA;
     return PK_OK;
   };
@@ -229,9 +245,10 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
         ok = cudaStreamEndCapture(s, &g) == cudaSuccess && enq && g;
         graph->graph = g;
         ok = ok && cudaGraphInstantiate(&graph->exec, g, 0) == cudaSuccess;
-        // The input copies' nodes, found by their destinations.
+        // The input copies' nodes, found by their destinations (zero-copy
+        // mode has none: its host addresses are part of the kernels' arguments).
         size_t n = 0;
-        if (ok) ok = cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess;
+        if (ok && !zero_copy) ok = cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess;
         std::vector<cudaGraphNode_t> nodes(n);
         if (ok && n) ok = cudaGraphGetNodes(g, nodes.data(), &n) == cudaSuccess;
         for (size_t i = 0; ok && i < n; ++i) {
@@ -243,7 +260,8 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
           for (int k = 0; k < 3; ++k)
             if (mp.dstPtr.ptr == dsts[k]) graph->copy_node[k] = nodes[i];
         }
-        ok = ok && graph->copy_node[0] && graph->copy_node[1] && graph->copy_node[2];
+        ok = ok && (zero_copy || (graph->copy_node[0] && graph->copy_node[1] && graph->copy_node[2]));
+        graph->zero_copy = zero_copy;
       }
       if (!ok) {
         cudaGetLastError();
@@ -252,9 +270,15 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
         if (!enqueue_inputs()) return PK_ERR_CUDA;  // this step runs the normal way
       } else {
         for (int k = 0; k < 3; ++k) graph->src[k] = srcs[k];
+        graph->out = b->out_host;
       }
     }
-    if (graph->exec) {
+    const bool moved = graph->zero_copy && (graph->src[0] != srcs[0] || graph->src[1] != srcs[1] ||
+                                            graph->src[2] != srcs[2]);
+    if (graph->exec && (moved || graph->out != b->out_host)) {
+      drop_graph(graph);  // other host buffers than the graph's arguments: run it the normal way
+      if (!enqueue_inputs()) return PK_ERR_CUDA;
+    } else if (graph->exec) {
       for (int k = 0; k < 3; ++k)
         if (graph->src[k] != srcs[k]) {
           if (cudaGraphExecMemcpyNodeSetParams1D(graph->exec, graph->copy_node[k], dsts[k], srcs[k],

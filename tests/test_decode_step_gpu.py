@@ -253,3 +253,32 @@ def test_graph_replay_follows_new_host_buffers():
     assert pk.pk_get_device_error()[0] == 0
     stepper.release()
     assert not stepper.buffers.graph
+
+
+@pytest.mark.parametrize("name,nseq,B", [("gqa8b", 24, None), ("prefix", 8, 32), ("mixed", 40, None)])
+def test_zero_copy_steps_match_the_copying_steps(name, nseq, B):
+    """Zero-copy mode (the kernels read q, k, v from and write out to pinned host
+    memory) gives the copying mode's outputs and pools bit for bit, over full,
+    resident and graph-replayed steps."""
+    wl = make_workload(name, block_size=B, num_seqs=nseq)
+    wl.enable_memo()
+    steps = 10
+    runs = []
+    for zero_copy in (False, True):
+        st = DecodeState(wl, "cuda", extra_tokens=steps)
+        stepper = pk.DecodeStepper(st.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, st.max_blocks,
+                                   st.k_cache, st.v_cache, zero_copy=zero_copy)
+        outs = []
+        for i in range(steps):
+            q, k, v = wl.step_inputs(i)
+            stepper.stream.synchronize()
+            stepper.q_host.copy_(_host(q, wl.dtype))
+            stepper.k_host.copy_(_host(k, wl.dtype))
+            stepper.v_host.copy_(_host(v, wl.dtype))
+            outs.append(from_device(stepper.step()).copy())
+        assert pk.pk_get_device_error()[0] == 0
+        runs.append((outs, from_device(st.k_cache), from_device(st.v_cache)))
+        stepper.release()
+    for a, b in zip(runs[0][0], runs[1][0]):
+        assert np.array_equal(a, b)
+    assert np.array_equal(runs[0][1], runs[1][1]) and np.array_equal(runs[0][2], runs[1][2])
