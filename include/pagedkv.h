@@ -606,13 +606,17 @@ typedef struct {
      * its partition size and item count (see pk_attention_plan). */
     int32_t plan_partition;
     int32_t plan_items;
-    /* Library-managed (NULL-initialise): the captured graph of the steady
-     * resident steps; free it with pk_decode_step_release. */
-    void *graph;
+    /* Library-managed (NULL-initialise): the prepared step and the captured
+     * graphs of the steady resident steps; free it with
+     * pk_decode_step_release. */
+    void *state;
 } pk_step_buffers;
 
-/* Bytes of pk_step_buffers.meta_host / meta_dev for S sequences and tables of
- * max_blocks_per_seq entries (0 for non-positive arguments). */
+/* Bytes of pk_step_buffers.meta_host / meta_dev (meta_bytes) for S sequences
+ * and tables of max_blocks_per_seq entries (0 for non-positive arguments).
+ * meta_host holds two staging halves that consecutive steps alternate
+ * between, so one step's metadata can be prepared while the previous step's
+ * is still being read; meta_dev uses the first half of this size. */
 size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
 
 /* One decode step of the whole path for the distinct sequences
@@ -631,30 +635,68 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  *      (pk_paged_attention_decode_items, automatic kernel);
  *   5. copy device -> host of the output into out_host.
  * All work is enqueued on `stream`; out_host holds the result once the stream
- * is synchronised, and meta_host must not be reused before then. The
- * workspace must cover the plan's partition: with partition_size = -1,
- * pk_paged_attention_workspace_size for 512 tokens and the longest context
- * the steps reach. The pages
+ * is synchronised. The workspace must cover the plan's partition: with
+ * partition_size = -1, pk_paged_attention_workspace_size for 512 tokens and
+ * the longest context the steps reach. The pages
  * have no counterpart for this packaging; each step it performs is theirs
  * (see the entry points above). On an error after step 2 the block manager
  * keeps the appended tokens and tables_resident is 0.
  *
  * On a stream the caller created (not the legacy or per-thread default
  * stream, and not being captured), a steady resident step -- no
- * copy-on-write pair, the same work list -- runs as one CUDA graph captured
- * on the first such step: the input copies, the slot copy, the scatter, the
- * attention and the output copy; only the q/k/v host addresses are patched
- * when they change (in zero-copy mode, or when out_host changes, the graph
- * is rebuilt instead). The graph is rebuilt when the work list changes or
- * after a full step. The per-step host work is then the block-manager append and
- * one graph launch. */
+ * copy-on-write pair, the same work list -- runs as one CUDA graph, captured
+ * on the first such step of each staging half: the input copies, the slot
+ * copy, the scatter, the attention and the output copy; only the q/k/v host
+ * addresses are patched when they change (in zero-copy mode, or when
+ * out_host changes, the graph is rebuilt instead). The graphs are rebuilt
+ * when the work list changes or after a full step. The per-step host work is
+ * then the block-manager append and one graph launch. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,
                          pk_step_buffers *buffers, void *stream);
 
-/* Frees the captured graph held in buffers->graph (if any) and sets it to
- * NULL; call before freeing the buffers or destroying the stream. */
+/* pk_decode_step in two halves, so that the host half of a step can overlap
+ * the device half of the step before -- as a serving loop does when it
+ * schedules the next step while the current one runs on the GPU.
+ *
+ * pk_decode_step_prepare is steps 2 of pk_decode_step (the block-manager
+ * append, and the tables, lengths and work plan unless tables_resident) into
+ * the staging half of meta_host that the step before the previous one used;
+ * it first waits until that step has finished reading it (an event recorded
+ * after its work), so at most one step is ever outstanding on a half. It
+ * enqueues no device work and reads no q/k/v. It sets tables_resident to 0
+ * after the append (the device tables do not yet hold the new token).
+ * PK_ERR_INVALID_ARG if a prepared step has not been launched yet, or if
+ * tables_resident is set for another shape than the last prepared step's.
+ *
+ * pk_decode_step_launch is steps 1 and 3-5 for the prepared step (the same
+ * num_seqs and max_blocks_per_seq): the input copies, the metadata copy from
+ * the prepared half, the kernels and the output copy, or the captured graph of
+ * that half; it sets tables_resident to 1 once the work is enqueued. The
+ * prepared step is consumed even when the launch fails (tables_resident then
+ * stays 0, and the next step is a full one). Inputs are read when the step
+ * runs, so q/k/v must not change until the stream has passed the step.
+ *
+ * pk_decode_step is prepare followed by launch. A pipelined loop is: prepare
+ * step 0; then for every step t: fill its inputs, launch it, prepare step
+ * t+1 (host work while step t runs), synchronise, read the output. */
+pk_status pk_decode_step_prepare(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                 int32_t partition_size, const pk_cache_desc *desc,
+                                 pk_step_buffers *buffers);
+pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float scale,
+                                int32_t max_blocks_per_seq, void *k_cache, void *v_cache,
+                                const pk_cache_desc *desc, pk_step_buffers *buffers,
+                                void *stream);
+
+/* Captured graphs currently held in buffers->state (0, 1 or 2: one per
+ * staging half). Host only. */
+int32_t pk_decode_step_graph_count(const pk_step_buffers *buffers);
+
+/* Frees the library-managed state in buffers->state (the captured graphs,
+ * events and any prepared step) and sets it to NULL; call before freeing the
+ * buffers or destroying the stream, after the last step has finished. */
 void pk_decode_step_release(pk_step_buffers *buffers);
 
 #ifdef __cplusplus

@@ -51,7 +51,8 @@ EXPORTED = (
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
     "pk_bm_fork", "pk_bm_free_seq", "pk_bm_seq_len", "pk_bm_block_table", "pk_bm_export_tables",
     "pk_bm_num_free", "pk_bm_refcount", "pk_bm_check_invariants", "pk_bm_stats",
-    "pk_decode_step_meta_bytes", "pk_decode_step", "pk_decode_step_release",
+    "pk_decode_step_meta_bytes", "pk_decode_step", "pk_decode_step_prepare", "pk_decode_step_launch",
+    "pk_decode_step_graph_count", "pk_decode_step_release",
     "pk_bm_prefix_groups", "pk_cascade_attention_decode", "pk_cascade_workspace_size",
     "pk_swap_blocks", "pk_bm_set_swap_space", "pk_bm_swap_out", "pk_bm_swap_in", "pk_bm_is_swapped",
     "pk_bm_host_free", "pk_bm_add_seq_cached", "pk_bm_commit", "pk_bm_cache_match", "pk_bm_cache_stats",
@@ -75,7 +76,7 @@ class StepBuffers(ctypes.Structure):
                 ("out_dev", ctypes.c_void_p), ("out_host", ctypes.c_void_p),
                 ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("tables_resident", ctypes.c_int32), ("plan_partition", ctypes.c_int32),
-                ("plan_items", ctypes.c_int32), ("graph", ctypes.c_void_p)]
+                ("plan_items", ctypes.c_int32), ("state", ctypes.c_void_p)]
 
 
 class SimRequest(ctypes.Structure):
@@ -168,6 +169,9 @@ def lib() -> ctypes.CDLL:
         "pk_sim_num_steps": (i32, [P, i32]),
         "pk_sim_run": (i32, [P, i32, i32, i32, i32, i32, ctypes.POINTER(SimSummary), P, i32]),
         "pk_decode_step": (i32, [P, P, i32, i32, f32, i32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
+        "pk_decode_step_prepare": (i32, [P, P, i32, i32, i32, i32, D, ctypes.POINTER(StepBuffers)]),
+        "pk_decode_step_launch": (i32, [i32, i32, f32, i32, P, P, D, ctypes.POINTER(StepBuffers), P]),
+        "pk_decode_step_graph_count": (i32, [ctypes.POINTER(StepBuffers)]),
         "pk_decode_step_release": (None, [ctypes.POINTER(StepBuffers)]),
     }
     for name, (res, args) in sigs.items():
@@ -677,6 +681,11 @@ class DecodeStepper:
     kernels read the inputs from, and write the output to, the stepper's
     pinned host buffers directly (fill ``q_host``/``k_host``/``v_host`` before
     each step).
+
+    ``prepare()`` and ``launch_prepared()`` are the two halves of a step
+    (pk_decode_step_prepare / pk_decode_step_launch): preparing step t+1
+    right after launching step t overlaps its host work with step t on the
+    GPU.
     """
 
     def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
@@ -725,7 +734,7 @@ class DecodeStepper:
         # Host -> device bytes of a step: the whole metadata buffer on a full
         # upload; only the slot section (plus 16 bytes per copy-on-write pair)
         # once the tables are resident.
-        self.h2d_bytes_full = qkv + mb
+        self.h2d_bytes_full = qkv + mb // 2     # one staging half
         self.h2d_bytes_resident = qkv + (8 * S + 255) // 256 * 256   # + the work list when it changes
         self.h2d_bytes = self.h2d_bytes_full
         # The call's arguments that never change, built once.
@@ -734,12 +743,16 @@ class DecodeStepper:
                            ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
                            ctypes.byref(self.desc), ctypes.byref(self.buffers))
         self._stream_arg = ctypes.c_void_p(self.stream.cuda_stream)
+        self._prepare_fn = lib().pk_decode_step_prepare
+        self._prepare_args = (bm._h, _np_ptr(self.ids), S, self.Hq, self.maxb, self.partition,
+                              ctypes.byref(self.desc), ctypes.byref(self.buffers))
+        self._launch_fn = lib().pk_decode_step_launch
+        self._launch_args = (S, self.Hq, self.scale, self.maxb, ctypes.c_void_p(k_cache.data_ptr()),
+                             ctypes.c_void_p(v_cache.data_ptr()), ctypes.byref(self.desc),
+                             ctypes.byref(self.buffers))
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
 
-    def launch(self, stream=None, q_host=None, k_host=None, v_host=None):
-        """Enqueues one step from q_host/k_host/v_host (the stepper's own pinned
-        buffers unless other pinned tensors are given) on ``stream`` (default:
-        the stepper's own stream, on which steady steps replay a captured graph)."""
+    def _bind(self, stream, q_host, k_host, v_host):
         for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
             setattr(self.buffers, name, (getattr(self, name) if t is None else t).data_ptr())
         if self._order_after_caller:
@@ -747,12 +760,33 @@ class DecodeStepper:
             # fork) must finish before the step's kernels touch the pool.
             self.stream.wait_stream(_torch().cuda.current_stream())
             self._order_after_caller = False
-        st = self._stream_arg if stream is None else _stream(stream)
+        return self._stream_arg if stream is None else _stream(stream)
+
+    def launch(self, stream=None, q_host=None, k_host=None, v_host=None):
+        """Enqueues one step from q_host/k_host/v_host (the stepper's own pinned
+        buffers unless other pinned tensors are given) on ``stream`` (default:
+        the stepper's own stream, on which steady steps replay a captured graph)."""
+        st = self._bind(stream, q_host, k_host, v_host)
         _check(self._step_fn(*self._step_args, st), "pk_decode_step")
 
+    def prepare(self):
+        """The host half of the next step (block-manager append, metadata);
+        may run while the previous step is still on the GPU."""
+        _check(self._prepare_fn(*self._prepare_args), "pk_decode_step_prepare")
+
+    def launch_prepared(self, stream=None, q_host=None, k_host=None, v_host=None):
+        """Enqueues the prepared step (arguments as ``launch``)."""
+        st = self._bind(stream, q_host, k_host, v_host)
+        _check(self._launch_fn(*self._launch_args, st), "pk_decode_step_launch")
+
+    @property
+    def graph_count(self) -> int:
+        """Captured graphs the stepper holds (one per staging half at most)."""
+        return int(lib().pk_decode_step_graph_count(ctypes.byref(self.buffers)))
+
     def release(self):
-        """Frees the captured graph (the stepper stays usable)."""
-        if getattr(self, "buffers", None) is not None and self.buffers.graph:
+        """Frees the captured graphs (the stepper stays usable)."""
+        if getattr(self, "buffers", None) is not None and self.buffers.state:
             lib().pk_decode_step_release(ctypes.byref(self.buffers))
 
     def __del__(self):

@@ -67,23 +67,49 @@ int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0);
 // that advances the device tables, the attention over the unchanged work
 // list and the output copy. Every parameter of those is fixed while the work
 // list is, except the caller's q/k/v host addresses, which are patched.
-struct StepGraph {
+struct GraphSlot {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   cudaGraphNode_t copy_node[3] = {nullptr, nullptr, nullptr};  // q, k, v
   const void *src[3] = {nullptr, nullptr, nullptr};
   const void *out = nullptr;  // the host output buffer the graph writes
-  cudaStream_t stream = nullptr;
-  bool zero_copy = false;  // captured in zero-copy mode (no copy nodes)
-  bool failed = false;     // capture is not possible on this stream: stop trying
 };
 
-void drop_graph(StepGraph *g) {
-  if (g->exec) cudaGraphExecDestroy(g->exec);
-  if (g->graph) cudaGraphDestroy(g->graph);
-  g->exec = nullptr;
-  g->graph = nullptr;
-  g->copy_node[0] = g->copy_node[1] = g->copy_node[2] = nullptr;
+// Library-managed state behind pk_step_buffers.state: the prepared step
+// (pk_decode_step_prepare) and, per staging half, the captured graph of the
+// steady resident steps that read that half and an event recorded after the
+// last step that read it.
+struct StepState {
+  GraphSlot slot[2];
+  cudaEvent_t done[2] = {nullptr, nullptr};
+  cudaStream_t stream = nullptr;  // the stream the graphs were captured on
+  bool zero_copy = false;         // the graphs were captured in zero-copy mode
+  bool failed = false;            // capture is not possible on this stream: stop trying
+  // The prepared step.
+  bool prepared = false;
+  int half = 1;  // staging half of the last prepared step; the next one takes the other
+  bool resident = false;
+  bool new_part = false;
+  int32_t npairs = 0;
+  int32_t max_ctx = 0;
+  size_t meta_copy = 0;
+  int32_t num_seqs = 0, max_blocks = 0;
+};
+
+void drop_slot(GraphSlot &g) {
+  if (g.exec) cudaGraphExecDestroy(g.exec);  // freed once a launch in flight completes
+  if (g.graph) cudaGraphDestroy(g.graph);
+  g = GraphSlot{};
+}
+
+void drop_graphs(StepState *st) {
+  drop_slot(st->slot[0]);
+  drop_slot(st->slot[1]);
+}
+
+StepState *state_of(pk_step_buffers *b) {
+  if (!b->state) b->state = new (std::nothrow) StepState;
+  return static_cast<StepState *>(b->state);
 }
 
 // A stream on which the library may capture: one the caller created, not the
@@ -104,19 +130,93 @@ extern "C" {
 
 size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq) {
   if (num_seqs <= 0 || max_blocks_per_seq <= 0) return 0;
-  return layout(num_seqs, max_blocks_per_seq).total;
+  return 2 * layout(num_seqs, max_blocks_per_seq).total;  // two staging halves
 }
 
-pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
-                         float scale, int32_t max_blocks_per_seq, int32_t partition_size,
-                         void *k_cache, void *v_cache, const pk_cache_desc *desc,
-                         pk_step_buffers *b, void *stream) {
-  if (!bm || !desc || !b || num_seqs <= 0 || !seq_ids || max_blocks_per_seq <= 0)
+pk_status pk_decode_step_prepare(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                 int32_t partition_size, const pk_cache_desc *desc,
+                                 pk_step_buffers *b) {
+  if (!bm || !desc || !b || num_seqs <= 0 || !seq_ids || max_blocks_per_seq <= 0 ||
+      !b->meta_host)
     return PK_ERR_INVALID_ARG;
+  if (elem_size(desc->dtype) == 0) return PK_ERR_UNSUPPORTED;
+  const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
+  if (b->meta_bytes < 2 * m.total) return PK_ERR_INVALID_ARG;
+  StepState *st = state_of(b);
+  if (!st) return PK_ERR_NOMEM;
+  if (st->prepared) return PK_ERR_INVALID_ARG;  // the prepared step has not been launched
+  const bool resident = b->tables_resident != 0;
+  if (resident && (st->num_seqs != num_seqs || st->max_blocks != max_blocks_per_seq))
+    return PK_ERR_INVALID_ARG;
+  const int h = st->half ^ 1;
+  // The step that last read this half (two steps back) must be done with it.
+  if (st->done[h] && cudaEventSynchronize(st->done[h]) != cudaSuccess) return PK_ERR_CUDA;
+  uint8_t *mh = static_cast<uint8_t *>(b->meta_host) + size_t(h) * m.total;
+  int64_t *slots = reinterpret_cast<int64_t *>(mh + m.slots);
+  int64_t *pairs = reinterpret_cast<int64_t *>(mh + m.pairs);
+  int32_t *tables = reinterpret_cast<int32_t *>(mh + m.tables);
+  int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
+  int32_t *items = reinterpret_cast<int32_t *>(mh + m.items);
+  if (resident) {
+    // The lengths as the previous step left them (the host mirror of the
+    // device lengths); every row must have room for one more token.
+    const uint8_t *prev = static_cast<const uint8_t *>(b->meta_host) + size_t(h ^ 1) * m.total;
+    std::memcpy(lens, prev + m.lens, size_t(num_seqs) * sizeof(int32_t));
+    for (int32_t i = 0; i < num_seqs; ++i)
+      if (int64_t(lens[i]) + 1 > int64_t(max_blocks_per_seq) * desc->block_size)
+        return PK_ERR_INVALID_ARG;
+  }
+
+  int32_t npairs = 0;
+  pk_status rc = pk_bm_append_batch(bm, seq_ids, num_seqs, slots, pairs, &npairs);
+  if (rc != PK_OK) return rc;
+  b->tables_resident = 0;  // until this step's metadata is on its way
+  size_t meta_copy = m.total;
+  bool new_part = false;
+  if (resident) {
+    const int32_t part = b->plan_partition;
+    for (int32_t i = 0; i < num_seqs; ++i) {
+      lens[i] += 1;
+      if (part > 0 && (lens[i] - 1) % part == 0) new_part = true;
+    }
+    meta_copy = m.pairs + size_t(npairs) * 2 * sizeof(int64_t);
+    if (new_part) {
+      rc = pk_attention_work_items(lens, num_seqs, part, items, m.item_cap, &b->plan_items);
+      if (rc != PK_OK) return rc;
+      meta_copy = m.items + size_t(b->plan_items) * 2 * sizeof(int32_t);
+    }
+  } else {
+    rc = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
+    if (rc != PK_OK) return rc;
+    rc = pk_attention_plan(lens, num_seqs, num_q_heads, partition_size, desc, &b->plan_partition,
+                           items, m.item_cap, &b->plan_items);
+    if (rc != PK_OK) return rc;
+  }
+  st->prepared = true;
+  st->half = h;
+  st->resident = resident;
+  st->new_part = new_part;
+  st->npairs = npairs;
+  st->meta_copy = meta_copy;
+  st->max_ctx = *std::max_element(lens, lens + num_seqs);
+  st->num_seqs = num_seqs;
+  st->max_blocks = max_blocks_per_seq;
+  return PK_OK;
+}
+
+pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float scale,
+                                int32_t max_blocks_per_seq, void *k_cache, void *v_cache,
+                                const pk_cache_desc *desc, pk_step_buffers *b, void *stream) {
+  if (!desc || !b || num_seqs <= 0 || max_blocks_per_seq <= 0) return PK_ERR_INVALID_ARG;
+  StepState *st = static_cast<StepState *>(b->state);
+  if (!st || !st->prepared || st->num_seqs != num_seqs || st->max_blocks != max_blocks_per_seq)
+    return PK_ERR_INVALID_ARG;  // nothing prepared for this shape
   const int64_t esz = elem_size(desc->dtype);
   if (esz == 0) return PK_ERR_UNSUPPORTED;
   if (!b->q_host || !b->k_host || !b->v_host || !b->meta_host || !b->meta_dev || !b->out_host)
     return PK_ERR_INVALID_ARG;
+  st->prepared = false;  // consumed, whatever happens below
   // Zero-copy mode (no device copies given): the kernels read q and the new
   // K/V from, and write the output to, the pinned host buffers through their
   // device mappings; the bytes still cross the host link every step, inside
@@ -133,23 +233,16 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
     return PK_ERR_INVALID_ARG;  // not pinned, mapped host memory
   }
   const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
-  if (b->meta_bytes < m.total) return PK_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t *mh = static_cast<uint8_t *>(b->meta_host);
+  const int h = st->half;
+  const uint8_t *mh = static_cast<const uint8_t *>(b->meta_host) + size_t(h) * m.total;
   uint8_t *md = static_cast<uint8_t *>(b->meta_dev);
-  int64_t *slots = reinterpret_cast<int64_t *>(mh + m.slots);
-  int64_t *pairs = reinterpret_cast<int64_t *>(mh + m.pairs);
-  int32_t *tables = reinterpret_cast<int32_t *>(mh + m.tables);
-  int32_t *lens = reinterpret_cast<int32_t *>(mh + m.lens);
-  int32_t *items = reinterpret_cast<int32_t *>(mh + m.items);
-  const bool resident = b->tables_resident != 0;
-  StepGraph *graph = static_cast<StepGraph *>(b->graph);
-  // Resident mode keeps the previous step's lengths in meta_host; every row
-  // must have room for one more token.
-  if (resident)
-    for (int32_t i = 0; i < num_seqs; ++i)
-      if (int64_t(lens[i]) + 1 > int64_t(max_blocks_per_seq) * desc->block_size)
-        return PK_ERR_INVALID_ARG;
+  const bool resident = st->resident;
+  const int32_t npairs = st->npairs;
+  const size_t meta_copy = st->meta_copy;
+  const int32_t max_ctx = st->max_ctx;
+  if (!st->done[h] && cudaEventCreateWithFlags(&st->done[h], cudaEventDisableTiming) != cudaSuccess)
+    return PK_ERR_CUDA;
 
   const size_t qbytes = size_t(num_seqs) * num_q_heads * desc->head_dim * esz;
   const size_t kvbytes = size_t(num_seqs) * desc->num_kv_heads * desc->head_dim * esz;
@@ -164,40 +257,7 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
     return true;
   };
 
-  // The inputs are copied first, so the copies overlap the host work -- except
-  // on a resident step that may run as the captured graph (which copies them).
-  const bool may_replay = resident && !(graph && graph->failed) && capturable(s);
-  if (!may_replay && !enqueue_inputs()) return PK_ERR_CUDA;
-
-  // Host side of the step.
-  int32_t npairs = 0;
-  pk_status st = pk_bm_append_batch(bm, seq_ids, num_seqs, slots, pairs, &npairs);
-  if (st != PK_OK) return st;
-  b->tables_resident = 0;  // until this step's metadata is on its way
-  size_t meta_copy = m.total;
-  bool new_part = false;
-  if (resident) {
-    const int32_t part = b->plan_partition;
-    for (int32_t i = 0; i < num_seqs; ++i) {
-      lens[i] += 1;
-      if (part > 0 && (lens[i] - 1) % part == 0) new_part = true;
-    }
-    meta_copy = m.pairs + size_t(npairs) * 2 * sizeof(int64_t);
-    if (new_part) {
-      st = pk_attention_work_items(lens, num_seqs, part, items, m.item_cap, &b->plan_items);
-      if (st != PK_OK) return st;
-      meta_copy = m.items + size_t(b->plan_items) * 2 * sizeof(int32_t);
-    }
-  } else {
-    st = pk_bm_export_tables(bm, seq_ids, num_seqs, max_blocks_per_seq, tables, lens);
-    if (st != PK_OK) return st;
-    st = pk_attention_plan(lens, num_seqs, num_q_heads, partition_size, desc, &b->plan_partition,
-                           items, m.item_cap, &b->plan_items);
-    if (st != PK_OK) return st;
-  }
-  if (graph && (!resident || new_part || graph->stream != s)) drop_graph(graph);
-  const int32_t max_ctx = *std::max_element(lens, lens + num_seqs);
-
+  if (!resident || st->new_part || st->stream != s) drop_graphs(st);
   const int64_t *dslots = reinterpret_cast<const int64_t *>(md + m.slots);
   int32_t *dtables = reinterpret_cast<int32_t *>(md + m.tables);
   int32_t *dlens = reinterpret_cast<int32_t *>(md + m.lens);
@@ -226,31 +286,35 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
       return PK_ERR_CUDA;
     return PK_OK;
   };
+  // After the step's work (never captured into a graph): the staging half is
+  // free again once the stream passes this point.
+  auto mark_half = [&]() -> pk_status {
+    if (cudaEventRecord(st->done[h], s) != cudaSuccess) return PK_ERR_CUDA;
+    b->tables_resident = 1;
+    return PK_OK;
+  };
 
   // A steady resident step (no copy-on-write pair, the same work list) runs
-  // as one captured graph.
-  const bool steady = may_replay && npairs == 0 && !new_part;
+  // as the captured graph of its staging half.
+  const bool may_replay = resident && !st->failed && capturable(s);
+  const bool steady = may_replay && npairs == 0 && !st->new_part;
   if (steady) {
-    if (!graph) {
-      graph = new (std::nothrow) StepGraph;
-      if (!graph) return PK_ERR_NOMEM;
-      b->graph = graph;
-    }
-    if (!graph->exec) {
-      graph->stream = s;
+    GraphSlot &g = st->slot[h];
+    if (!g.exec) {
+      st->stream = s;
       bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
       if (ok) {
         const bool enq = enqueue_inputs() && enqueue_device() == PK_OK;
-        cudaGraph_t g = nullptr;
-        ok = cudaStreamEndCapture(s, &g) == cudaSuccess && enq && g;
-        graph->graph = g;
-        ok = ok && cudaGraphInstantiate(&graph->exec, g, 0) == cudaSuccess;
+        cudaGraph_t cg = nullptr;
+        ok = cudaStreamEndCapture(s, &cg) == cudaSuccess && enq && cg;
+        g.graph = cg;
+        ok = ok && cudaGraphInstantiate(&g.exec, cg, 0) == cudaSuccess;
         // The input copies' nodes, found by their destinations (zero-copy
         // mode has none: its host addresses are part of the kernels' arguments).
         size_t n = 0;
-        if (ok && !zero_copy) ok = cudaGraphGetNodes(g, nullptr, &n) == cudaSuccess;
+        if (ok && !zero_copy) ok = cudaGraphGetNodes(cg, nullptr, &n) == cudaSuccess;
         std::vector<cudaGraphNode_t> nodes(n);
-        if (ok && n) ok = cudaGraphGetNodes(g, nodes.data(), &n) == cudaSuccess;
+        if (ok && n) ok = cudaGraphGetNodes(cg, nodes.data(), &n) == cudaSuccess;
         for (size_t i = 0; ok && i < n; ++i) {
           cudaGraphNodeType t;
           if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeMemcpy)
@@ -258,53 +322,71 @@ pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, in
           cudaMemcpy3DParms mp{};
           if (cudaGraphMemcpyNodeGetParams(nodes[i], &mp) != cudaSuccess) continue;
           for (int k = 0; k < 3; ++k)
-            if (mp.dstPtr.ptr == dsts[k]) graph->copy_node[k] = nodes[i];
+            if (mp.dstPtr.ptr == dsts[k]) g.copy_node[k] = nodes[i];
         }
-        ok = ok && (zero_copy || (graph->copy_node[0] && graph->copy_node[1] && graph->copy_node[2]));
-        graph->zero_copy = zero_copy;
+        ok = ok && (zero_copy || (g.copy_node[0] && g.copy_node[1] && g.copy_node[2]));
+        st->zero_copy = zero_copy;
       }
       if (!ok) {
         cudaGetLastError();
-        drop_graph(graph);
-        graph->failed = true;
-        if (!enqueue_inputs()) return PK_ERR_CUDA;  // this step runs the normal way
+        drop_graphs(st);
+        st->failed = true;
       } else {
-        for (int k = 0; k < 3; ++k) graph->src[k] = srcs[k];
-        graph->out = b->out_host;
+        for (int k = 0; k < 3; ++k) g.src[k] = srcs[k];
+        g.out = b->out_host;
       }
     }
-    const bool moved = graph->zero_copy && (graph->src[0] != srcs[0] || graph->src[1] != srcs[1] ||
-                                            graph->src[2] != srcs[2]);
-    if (graph->exec && (moved || graph->out != b->out_host)) {
-      drop_graph(graph);  // other host buffers than the graph's arguments: run it the normal way
-      if (!enqueue_inputs()) return PK_ERR_CUDA;
-    } else if (graph->exec) {
+    const bool moved = st->zero_copy &&
+                       (g.src[0] != srcs[0] || g.src[1] != srcs[1] || g.src[2] != srcs[2]);
+    if (g.exec && (moved || g.out != b->out_host || st->zero_copy != zero_copy)) {
+      drop_graphs(st);  // other host buffers than the graph's arguments: run it the normal way
+    } else if (g.exec) {
       for (int k = 0; k < 3; ++k)
-        if (graph->src[k] != srcs[k]) {
-          if (cudaGraphExecMemcpyNodeSetParams1D(graph->exec, graph->copy_node[k], dsts[k], srcs[k],
+        if (g.src[k] != srcs[k]) {
+          if (cudaGraphExecMemcpyNodeSetParams1D(g.exec, g.copy_node[k], dsts[k], srcs[k],
                                                  sizes[k], cudaMemcpyHostToDevice) != cudaSuccess)
             return PK_ERR_CUDA;
-          graph->src[k] = srcs[k];
+          g.src[k] = srcs[k];
         }
-      if (cudaGraphLaunch(graph->exec, s) != cudaSuccess) return PK_ERR_CUDA;
-      b->tables_resident = 1;
-      return PK_OK;
+      if (cudaGraphLaunch(g.exec, s) != cudaSuccess) return PK_ERR_CUDA;
+      return mark_half();
     }
   }
 
-  if (may_replay && !steady && !enqueue_inputs()) return PK_ERR_CUDA;
-  st = enqueue_device();
-  if (st != PK_OK) return st;
-  b->tables_resident = 1;
-  return PK_OK;
+  if (!enqueue_inputs()) return PK_ERR_CUDA;
+  const pk_status r = enqueue_device();
+  if (r != PK_OK) return r;
+  return mark_half();
+}
+
+pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
+                         float scale, int32_t max_blocks_per_seq, int32_t partition_size,
+                         void *k_cache, void *v_cache, const pk_cache_desc *desc,
+                         pk_step_buffers *b, void *stream) {
+  const pk_status r = pk_decode_step_prepare(bm, seq_ids, num_seqs, num_q_heads,
+                                             max_blocks_per_seq, partition_size, desc, b);
+  if (r != PK_OK) return r;
+  return pk_decode_step_launch(num_seqs, num_q_heads, scale, max_blocks_per_seq, k_cache, v_cache,
+                               desc, b, stream);
+}
+
+int32_t pk_decode_step_graph_count(const pk_step_buffers *b) {
+  if (!b || !b->state) return 0;
+  const StepState *st = static_cast<const StepState *>(b->state);
+  return int32_t(st->slot[0].exec != nullptr) + int32_t(st->slot[1].exec != nullptr);
 }
 
 void pk_decode_step_release(pk_step_buffers *b) {
-  if (!b || !b->graph) return;
-  StepGraph *g = static_cast<StepGraph *>(b->graph);
-  drop_graph(g);
-  delete g;
-  b->graph = nullptr;
+  if (!b || !b->state) return;
+  StepState *st = static_cast<StepState *>(b->state);
+  drop_graphs(st);
+  for (cudaEvent_t &e : st->done)
+    if (e) {
+      cudaEventDestroy(e);
+      e = nullptr;
+    }
+  delete st;
+  b->state = nullptr;
 }
 
 }  // extern "C"

@@ -571,3 +571,42 @@ def test_attention_plan_choices(L):
     assert pk.pk_attention_plan(wl.ctx_lens, 32, d, 40000)[0] == 0          # longer than every context
     with pytest.raises(pk.PagedKVError):
         pk.pk_attention_plan(wl.ctx_lens, 32, d, 1000)                    # not a multiple of B
+
+
+def test_decode_step_prepare_and_launch_pair_up(L):
+    """The two halves of pk_decode_step pair up: a launch with nothing
+    prepared and a second prepare before the launch are refused before any
+    device work; a full prepare appends one token to every sequence and packs
+    its slots and lengths into the first staging half."""
+    S, maxb, B, nblk = 3, 8, 16, 64
+    bm = pk.BlockManager(nblk, B)
+    for s in range(S):
+        bm.add_seq(s)
+        bm.append(s, 15 + s)                      # lengths 15, 16, 17
+    before = [bm.table(s).copy() for s in range(S)]
+    desc = pk.CacheDesc(nblk, B, 2, 64, pk.PK_BF16)
+    mb = int(L.pk_decode_step_meta_bytes(S, maxb))
+    meta = np.zeros(mb, dtype=np.uint8)
+    buf = pk.StepBuffers()
+    buf.meta_host = meta.ctypes.data
+    buf.meta_bytes = mb
+    ids = np.arange(S, dtype=np.int64)
+    args = (bm._h, ids.ctypes.data, S, 4, maxb, 0, ctypes.byref(desc), ctypes.byref(buf))
+    assert L.pk_decode_step_launch(S, 4, 0.125, maxb, None, None, ctypes.byref(desc), ctypes.byref(buf),
+                                   None) == pk.PK_ERR_INVALID_ARG
+    assert L.pk_decode_step_prepare(*args) == pk.PK_OK
+    assert [bm.seq_len(s) for s in range(S)] == [16, 17, 18]
+    assert buf.tables_resident == 0 and buf.state
+    half = mb // 2
+    slots = meta[:8 * S].view(np.int64)
+    tables = [bm.table(s) for s in range(S)]
+    expect = [int(tables[s][t // B]) * B + t % B for s, t in zip(range(S), (15, 16, 17))]
+    assert list(slots) == expect
+    assert tables[0].tolist() == before[0].tolist()          # 15 -> 16 stays in block 0
+    assert len(tables[1]) == len(before[1]) + 1               # 16 -> 17 takes a new block
+    assert not meta[half:].any()                              # the second half is untouched
+    assert L.pk_decode_step_prepare(*args) == pk.PK_ERR_INVALID_ARG
+    assert [bm.seq_len(s) for s in range(S)] == [16, 17, 18]
+    bm.check_invariants()
+    L.pk_decode_step_release(ctypes.byref(buf))
+    assert not buf.state

@@ -119,7 +119,7 @@ def _meta_layout(S, maxb):
     items = up(pairs + 16 * S)
     lens = up(items + 8 * min(S * (1 + maxb // 16), 65535))
     tables = up(lens + 4 * S)
-    assert up(tables + 4 * S * maxb) == pk.lib().pk_decode_step_meta_bytes(S, maxb)
+    assert 2 * up(tables + 4 * S * maxb) == pk.lib().pk_decode_step_meta_bytes(S, maxb)  # two halves
     return {"slots": slots, "pairs": pairs, "items": items, "lens": lens, "tables": tables}
 
 
@@ -249,10 +249,10 @@ def test_graph_replay_follows_new_host_buffers():
         stepper.launch(q_host=q, k_host=k, v_host=v)
         stepper.stream.synchronize()
         assert np.array_equal(from_device(out_a), from_device(stepper.out_host)), f"step {i}"
-    assert stepper.buffers.graph, "steady steps should run as a captured graph"
+    assert stepper.graph_count == 2, "steady steps should run as captured graphs (one per staging half)"
     assert pk.pk_get_device_error()[0] == 0
     stepper.release()
-    assert not stepper.buffers.graph
+    assert not stepper.buffers.state and stepper.graph_count == 0
 
 
 @pytest.mark.parametrize("name,nseq,B", [("gqa8b", 24, None), ("prefix", 8, 32), ("mixed", 40, None)])
@@ -282,3 +282,38 @@ def test_zero_copy_steps_match_the_copying_steps(name, nseq, B):
     for a, b in zip(runs[0][0], runs[1][0]):
         assert np.array_equal(a, b)
     assert np.array_equal(runs[0][1], runs[1][1]) and np.array_equal(runs[0][2], runs[1][2])
+
+
+@pytest.mark.parametrize("name,nseq,B,zero_copy", [("gqa8b", 24, None, True), ("prefix", 8, 8, False),
+                                                   ("mixed", 40, None, True), ("long", 1, None, False)])
+def test_pipelined_steps_match_the_stepwise_path(name, nseq, B, zero_copy):
+    """The overlapped loop: the host half of step t+1 (prepare) runs right
+    after step t is launched, while step t is on the GPU. Outputs and pools
+    equal the step-by-step path's bit for bit over steps that cross block
+    boundaries, start partitions and (prefix) copy on write."""
+    wl = make_workload(name, block_size=B, num_seqs=nseq)
+    wl.enable_memo()
+    steps = 20
+    a = DecodeState(wl, "cuda", extra_tokens=steps + 1)
+    b = DecodeState(wl, "cuda", extra_tokens=steps + 1)
+    stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
+                               b.k_cache, b.v_cache, zero_copy=zero_copy)
+    ref_path = _Stepwise(a)
+    stepper.prepare()
+    for i in range(steps):
+        out_a = ref_path.step(i)
+        q, k, v = wl.step_inputs(i)
+        stepper.q_host.copy_(_host(q, wl.dtype))
+        stepper.k_host.copy_(_host(k, wl.dtype))
+        stepper.v_host.copy_(_host(v, wl.dtype))
+        stepper.launch_prepared()
+        stepper.prepare()                  # step i + 1's host half while step i runs
+        stepper.stream.synchronize()
+        assert stepper.buffers.tables_resident == 0   # the prepared step is not launched yet
+        assert np.array_equal(from_device(out_a), from_device(stepper.out_host)), f"step {i}"
+    assert pk.pk_get_device_error()[0] == 0
+    assert np.array_equal(from_device(a.k_cache), from_device(b.k_cache))
+    assert np.array_equal(from_device(a.v_cache), from_device(b.v_cache))
+    with pytest.raises(pk.PagedKVError):
+        stepper.prepare()                  # one prepared step at a time
+    stepper.release()
