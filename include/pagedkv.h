@@ -237,6 +237,37 @@ pk_status pk_paged_attention_decode_append(
     int32_t max_context_len, int32_t partition_size, const int32_t *work_items, int32_t num_items,
     void *workspace, size_t workspace_bytes, const pk_cache_desc *desc, void *stream);
 
+/* One decode step on device-resident block tables in one launch: the step's
+ * slot scatter, its block-table bookkeeping and the attention ("Paged KV
+ * Cache Allocation and the Block Table", append_token; "PagedAttention",
+ * S06). The same result as pk_reshape_and_cache_append followed by
+ * pk_paged_attention_decode_items over the advanced lengths, with:
+ *   context_lens      int32 [S] (device), each sequence's length before the
+ *                     step's token; read only;
+ *   context_lens_out  int32 [S] (device), receives context_lens + 1; must not
+ *                     alias context_lens (alternate two buffers between
+ *                     steps). A row whose slot is not at offset
+ *                     context_lens[i] mod B of its block receives
+ *                     context_lens[i] unchanged and is recorded
+ *                     (PK_DEVERR_CONTEXT);
+ *   block_tables      updated in place: row i's entry of the block holding
+ *                     position context_lens[i] becomes slot_mapping[i] / B
+ *                     (a newly opened block or a copy-on-write replacement);
+ *   max_context_len, partition_size, work_items: for the advanced lengths.
+ * The tensor-core kernel does all of it inside the attention launch: the CTA
+ * holding a sequence's new token takes that token's block from its slot
+ * instead of the table, writes the token's K/V for its KV head, and for KV
+ * head 0 also writes the table entry and the new length. The CUDA-core
+ * kernel runs the scatter and bookkeeping as its own kernel first.
+ * Copy-on-write copies (pk_copy_blocks) must be enqueued before. */
+pk_status pk_paged_attention_decode_advance(
+    void *out, const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+    void *k_cache, void *v_cache, int32_t *block_tables, const int32_t *context_lens,
+    int32_t *context_lens_out, float scale, int32_t num_seqs, int32_t num_q_heads,
+    int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
+    const int32_t *work_items, int32_t num_items, void *workspace, size_t workspace_bytes,
+    const pk_cache_desc *desc, void *stream);
+
 /* Host helper for pk_paged_attention_decode_items: the items of sequences
  * with host context_lens [n] cut into partitions of `partition` tokens (0 = no
  * split; pass the resolved size), longest item first (ties: the longer
@@ -628,11 +659,15 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  *      -- into meta_host; a resident step keeps the plan's partition and
  *      rebuilds the list only when a sequence starts a new partition;
  *   3. copy host -> device of the metadata in one transfer (resident mode:
- *      only the slots and copy-on-write pairs);
- *   4. device: pk_copy_blocks for the step's pairs, the slot scatter of k/v
- *      (resident mode: pk_reshape_and_cache_append, which also advances the
- *      device tables and lengths), the attention over the work list
- *      (pk_paged_attention_decode_items, automatic kernel);
+ *      only the slots and copy-on-write pairs, and the work list when it
+ *      changed; in zero-copy mode the resident kernel reads the slots from
+ *      meta_host itself, so a steady step copies no metadata);
+ *   4. device: pk_copy_blocks for the step's pairs, then a full step runs the
+ *      slot scatter (pk_reshape_and_cache) and the attention over the work
+ *      list (pk_paged_attention_decode_items, automatic kernel); a resident
+ *      step runs both and the device-side table and length bookkeeping as
+ *      one pk_paged_attention_decode_advance launch, the lengths alternating
+ *      between two device buffers;
  *   5. copy device -> host of the output into out_host.
  * All work is enqueued on `stream`; out_host holds the result once the stream
  * is synchronised. The workspace must cover the plan's partition: with

@@ -46,6 +46,7 @@ EXPORTED = (
     "pk_reshape_and_cache", "pk_reshape_and_cache_append", "pk_copy_blocks", "pk_paged_attention_decode",
     "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static", "pk_paged_attention_decode_items",
     "pk_attention_work_items", "pk_attention_plan", "pk_paged_attention_decode_append",
+    "pk_paged_attention_decode_advance",
     "pk_paged_attention_resolve_partition",
     "pk_paged_attention_workspace_size", "pk_longest_first_order", "pk_get_device_error", "pk_status_string",
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
@@ -130,6 +131,8 @@ def lib() -> ctypes.CDLL:
         "pk_attention_plan": (i32, [P, i32, i32, i32, D, P, P, i32, P]),
         "pk_paged_attention_decode_append": (i32, [P, P, P, P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P,
                                                    i32, P, sz, D, P]),
+        "pk_paged_attention_decode_advance": (i32, [P, P, P, P, P, P, P, P, P, P, f32, i32, i32, i32, i32, i32,
+                                                     P, i32, P, sz, D, P]),
         "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),
         "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
         "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
@@ -395,6 +398,31 @@ def pk_paged_attention_decode_append(out, q, k_new, v_new, slot_mapping, k_cache
         float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
         _dev(work_items, "work_items", torch.int32), int(work_items.shape[0]), ws_ptr, ws_bytes,
         ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_append")
+
+
+def pk_paged_attention_decode_advance(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                                      context_lens, context_lens_out, scale: float, max_context_len: int,
+                                      partition_size: int, work_items, workspace=None, stream=None):
+    """One step on device-resident tables (see the header): ``context_lens``
+    are the lengths before the step's token, ``context_lens_out`` receives
+    them plus one, ``block_tables`` is updated in place; ``max_context_len``
+    and ``work_items`` are for the advanced lengths."""
+    torch = _torch()
+    desc = cache_desc(k_cache)
+    S, Hq, d = (int(x) for x in q.shape)
+    if out.shape != q.shape or tuple(k_new.shape) != (S, desc.num_kv_heads, d) or v_new.shape != k_new.shape:
+        raise ValueError("shape mismatch")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(lib().pk_paged_attention_decode_advance(
+        _dev(out, "out"), _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
+        _dev(context_lens_out, "context_lens_out", torch.int32), float(scale), S, Hq,
+        int(block_tables.shape[1]), int(max_context_len), int(partition_size),
+        _dev(work_items, "work_items", torch.int32), int(work_items.shape[0]), ws_ptr, ws_bytes,
+        ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_advance")
 
 
 def pk_paged_attention_decode_static(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -55,6 +55,17 @@
 #include "pagedkv.h"
 #include "pk_device.cuh"
 
+// The resident-table scatter of cache_ops.cu with separate input and output
+// lengths (library-internal).
+extern "C" pk_status pkx_reshape_and_cache_advance(const void *k, const void *v,
+                                                   const int64_t *slot_mapping, int32_t num_tokens,
+                                                   void *k_cache, void *v_cache,
+                                                   const pk_cache_desc *desc,
+                                                   int32_t *block_tables,
+                                                   int32_t max_blocks_per_seq,
+                                                   const int32_t *lens_in, int32_t *lens_out,
+                                                   void *stream);
+
 namespace {
 
 __device__ int g_attn_error;
@@ -97,12 +108,17 @@ struct AttnParams {
   const void *new_k;
   const void *new_v;
   const int64_t *new_slots;
+  // Advance mode (device-resident tables; needs new_k): ctx_lens holds the
+  // lengths before the step's token, and the CTA holding sequence s's new
+  // token for KV head 0 writes the token's block into tables[s] and the new
+  // length into lens_out[s]; null otherwise.
+  int32_t *lens_out;
 };
 
 // Context length of sequence s, clamped to what the table and the grid can
 // hold. Invalid lengths are recorded once (by the CTA for partition 0, head 0).
 __device__ __forceinline__ int context_len(const AttnParams &p, int s, bool record) {
-  int c = __ldg(p.ctx_lens + s);
+  int c = __ldg(p.ctx_lens + s) + (p.lens_out ? 1 : 0);  // advance mode counts the new token
   const int cap = min(p.max_blocks * p.block_size, p.num_partitions * p.partition);
   if (c < 1 || c > cap) {
     if (record) pk::record_error(&g_attn_error, PK_DEVERR_CONTEXT, s);
@@ -526,6 +542,21 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
   if (fuse && warp == 0) {
     constexpr int VEC = D * 2 / 16;  // 16-byte vectors of one head's row
     const int64_t slot = __ldg(p.new_slots + s);
+    if (p.lens_out && kvh == 0 && lane == 0) {
+      // Advance mode: the step's bookkeeping on the resident tables. The
+      // entry of the block holding position pos = ctx - 1 becomes slot / B
+      // (a freshly opened block and a copy-on-write replacement alike) and the
+      // length becomes ctx. A slot that is not at offset pos mod B means the
+      // tables are out of step with the host: the row keeps its length.
+      const int pos = ctx - 1;
+      if (slot >= 0 && slot < int64_t(p.num_blocks) * BS && slot % BS == pos % BS) {
+        const_cast<int32_t *>(p.tables)[size_t(s) * p.max_blocks + pos / BS] = int32_t(slot / BS);
+        p.lens_out[s] = ctx;
+      } else {
+        pk::record_error(&g_attn_error, PK_DEVERR_CONTEXT, s);
+        p.lens_out[s] = pos;
+      }
+    }
     if (slot < 0 || slot >= int64_t(p.num_blocks) * BS) {
       if (lane == 0) pk::record_error(&g_attn_error, PK_DEVERR_SLOT, s);
     } else if (lane < 2 * VEC) {
@@ -552,8 +583,21 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
     // a dependent global load before its copies can be issued.
     const int32_t *trow = p.tables + size_t(s) * p.max_blocks + start / BS;
     const int nb = (end - start + BS - 1) / BS;  // blocks of this partition
-    int cur = lane < nb ? __ldg(trow + lane) : 0;
-    int nxt = 32 + lane < nb ? __ldg(trow + 32 + lane) : 0;
+    // Advance mode: the block holding the new token (partition-relative index
+    // tail) is the token's slot / B -- its table entry is written during this
+    // launch, so it is not read. A slot that is not at offset pos mod B of a
+    // pool block (recorded by the bookkeeping above) reads block 0 instead.
+    int tail = -1, tail_blk = 0;
+    if (p.lens_out && fuse) {
+      const int64_t slot = __ldg(p.new_slots + s);
+      const int pos = ctx - 1;
+      tail = pos / BS - start / BS;
+      if (slot >= 0 && slot < int64_t(p.num_blocks) * BS && slot % BS == pos % BS)
+        tail_blk = int(slot / BS);
+    }
+    auto entry = [&](int j) { return j == tail ? tail_blk : (j < nb ? __ldg(trow + j) : 0); };
+    int cur = entry(lane);
+    int nxt = entry(32 + lane);
     int chunk = 0;
     int issued = 0;
     for (int st = 0; st < nst; ++st) {
@@ -562,8 +606,7 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
       if (b0 >= 32 * (chunk + 1)) {
         ++chunk;
         cur = nxt;
-        const int j = 32 * (chunk + 1) + lane;
-        nxt = j < nb ? __ldg(trow + j) : 0;
+        nxt = entry(32 * (chunk + 1) + lane);
       }
       const int mine = __shfl_sync(0xffffffffu, cur, (b0 & 31) + min(lane, S::BPS - 1));
       if (st >= STAGES && !pk::mbar_wait(empty_bar(slot), ((st / STAGES) - 1) & 1)) {
@@ -1437,7 +1480,8 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
                            size_t workspace_bytes, const pk_cache_desc *desc,
                            const int32_t *seq_order, const int32_t *items, int32_t num_items,
                            pk_attn_impl impl, void *stream, const void *new_k = nullptr,
-                           const void *new_v = nullptr, const int64_t *new_slots = nullptr) {
+                           const void *new_v = nullptr, const int64_t *new_slots = nullptr,
+                           int32_t *lens_out = nullptr) {
   pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
   if (st != PK_OK) return st;
   if (num_seqs == 0) return PK_OK;
@@ -1504,6 +1548,16 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
       p.new_k = new_k;
       p.new_v = new_v;
       p.new_slots = new_slots;
+      p.lens_out = lens_out;
+    } else if (lens_out) {
+      // The scatter and the table bookkeeping first, then attention over the
+      // new lengths.
+      st = pkx_reshape_and_cache_advance(new_k, new_v, new_slots, num_seqs,
+                                         const_cast<void *>(k_cache), const_cast<void *>(v_cache),
+                                         desc, const_cast<int32_t *>(block_tables),
+                                         max_blocks_per_seq, context_lens, lens_out, stream);
+      if (st != PK_OK) return st;
+      p.ctx_lens = lens_out;
     } else {
       st = pk_reshape_and_cache(new_k, new_v, new_slots, num_seqs, const_cast<void *>(k_cache),
                                 const_cast<void *>(v_cache), desc, stream);
@@ -1578,6 +1632,22 @@ pk_status pk_paged_attention_decode_append(
                           num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
                           workspace, workspace_bytes, desc, nullptr, work_items, num_items,
                           PK_ATTN_AUTO, stream, k_new, v_new, slot_mapping);
+}
+
+pk_status pk_paged_attention_decode_advance(
+    void *out, const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+    void *k_cache, void *v_cache, int32_t *block_tables, const int32_t *context_lens,
+    int32_t *context_lens_out, float scale, int32_t num_seqs, int32_t num_q_heads,
+    int32_t max_blocks_per_seq, int32_t max_context_len, int32_t partition_size,
+    const int32_t *work_items, int32_t num_items, void *workspace, size_t workspace_bytes,
+    const pk_cache_desc *desc, void *stream) {
+  if (!work_items || !k_new || !v_new || !slot_mapping || !context_lens_out ||
+      context_lens_out == context_lens)
+    return PK_ERR_INVALID_ARG;
+  return decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                          num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
+                          workspace, workspace_bytes, desc, nullptr, work_items, num_items,
+                          PK_ATTN_AUTO, stream, k_new, v_new, slot_mapping, context_lens_out);
 }
 
 pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,

@@ -34,7 +34,7 @@ template <bool UPDATE>
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     const uint4 *__restrict__ k, const uint4 *__restrict__ v, const int64_t *__restrict__ slots,
     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, int64_t num_slots,
-    int32_t row_vecs, int32_t *__restrict__ tables, int32_t *__restrict__ lens,
+    int32_t row_vecs, int32_t *__restrict__ tables, const int32_t *lens_in, int32_t *lens_out,
     int32_t max_blocks, int32_t block_size) {
   const int64_t i = blockIdx.x;
   const int32_t j = int32_t(blockIdx.y) * blockDim.x + threadIdx.x;
@@ -45,13 +45,15 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     return;
   }
   if (UPDATE && blockIdx.y == 0 && threadIdx.x == 0) {
-    // One thread per token reads and advances the row's length.
-    const int32_t pos = lens[i];
+    // One thread per token reads and advances the row's length (lens_out may
+    // be lens_in: in place).
+    const int32_t pos = lens_in[i];
     if (pos < 0 || pos >= max_blocks * block_size || s % block_size != pos % block_size) {
       pk::record_error(&g_cache_ops_error, PK_DEVERR_CONTEXT, i);
+      lens_out[i] = pos;
     } else {
       tables[i * max_blocks + pos / block_size] = int32_t(s / block_size);
-      lens[i] = pos + 1;
+      lens_out[i] = pos + 1;
     }
   }
   if (j >= row_vecs) return;
@@ -181,20 +183,39 @@ pk_status pk_reshape_and_cache(const void *k, const void *v, const int64_t *slot
                                     static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
-      int32_t(row_vecs), nullptr, nullptr, 0, desc->block_size);
+      int32_t(row_vecs), nullptr, nullptr, nullptr, 0, desc->block_size);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
+
+pk_status pkx_reshape_and_cache_advance(const void *k, const void *v, const int64_t *slot_mapping,
+                                        int32_t num_tokens, void *k_cache, void *v_cache,
+                                        const pk_cache_desc *desc, int32_t *block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t *lens_in,
+                                        int32_t *lens_out, void *stream);
 
 pk_status pk_reshape_and_cache_append(const void *k, const void *v, const int64_t *slot_mapping,
                                       int32_t num_tokens, void *k_cache, void *v_cache,
                                       const pk_cache_desc *desc, int32_t *block_tables,
                                       int32_t max_blocks_per_seq, int32_t *context_lens,
                                       void *stream) {
+  return pkx_reshape_and_cache_advance(k, v, slot_mapping, num_tokens, k_cache, v_cache, desc,
+                                       block_tables, max_blocks_per_seq, context_lens,
+                                       context_lens, stream);
+}
+
+// pk_reshape_and_cache_append reading the lengths from lens_in and writing
+// the advanced lengths to lens_out (library-internal; the fused attention's
+// CUDA-core fallback uses it with two buffers).
+pk_status pkx_reshape_and_cache_advance(const void *k, const void *v, const int64_t *slot_mapping,
+                                        int32_t num_tokens, void *k_cache, void *v_cache,
+                                        const pk_cache_desc *desc, int32_t *block_tables,
+                                        int32_t max_blocks_per_seq, const int32_t *lens_in,
+                                        int32_t *lens_out, void *stream) {
   pk_status st = check_desc(desc);
   if (st != PK_OK) return st;
   if (num_tokens < 0 || max_blocks_per_seq <= 0) return PK_ERR_INVALID_ARG;
   if (num_tokens == 0) return PK_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !block_tables || !context_lens)
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !block_tables || !lens_in || !lens_out)
     return PK_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
     return PK_ERR_INVALID_ARG;
@@ -208,7 +229,7 @@ pk_status pk_reshape_and_cache_append(const void *k, const void *v, const int64_
                                    static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
-      int32_t(row_vecs), block_tables, context_lens, max_blocks_per_seq, desc->block_size);
+      int32_t(row_vecs), block_tables, lens_in, lens_out, max_blocks_per_seq, desc->block_size);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 

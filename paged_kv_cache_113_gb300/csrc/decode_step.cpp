@@ -1,14 +1,17 @@
-// One decode step from host buffers, in native code. The step's new K/V and
-// queries are copied from the caller's host buffers first, so the copies run
-// while the host block manager appends a token to every sequence. The step's
-// metadata is packed into one pinned staging buffer and copied with a single
-// transfer: in full mode slots, copy-on-write pairs, work items, context
-// lengths and padded block tables; in resident mode (the device already holds
-// this batch's tables and lengths) only slots and pairs -- the scatter kernel
-// then advances the device tables and lengths itself. Then
-// copy_blocks (when pairs exist), the scatter and the attention run, and the
-// output is copied back to host memory. Everything is enqueued on one stream;
-// the call returns once the work is enqueued.
+// One decode step from host buffers, in native code, in two halves. The host
+// half (prepare) appends a token to every sequence in the host block manager
+// and packs the step's metadata into one of two pinned staging halves, so it
+// can run while the previous step, reading the other half, is still on the
+// GPU. The device half (launch) copies the new K/V and queries (unless the
+// kernels read them from pinned host memory: zero-copy), copies the metadata
+// with a single transfer -- in full mode slots, copy-on-write pairs, work
+// items, context lengths and padded block tables; in resident mode (the
+// device already holds this batch's tables and lengths) only what changed --
+// and runs copy_blocks (when pairs exist) and the step's kernels: the scatter
+// and the attention in full mode, one launch that also advances the device
+// tables and lengths in resident mode. The output is copied back to host
+// memory. Everything is enqueued on one stream; the call returns once the
+// work is enqueued.
 //
 // The attention runs a work list of (sequence, partition) items planned on the
 // host (pk_attention_plan). A full step plans afresh; a resident step keeps the
@@ -37,9 +40,11 @@ int64_t item_capacity(int32_t num_seqs, int32_t max_blocks) {
 }
 
 // What changes every step comes first, so a resident-mode step copies one
-// short prefix of the buffer.
+// short prefix of the buffer. On the device, lens and lens_b hold the
+// lengths of alternate resident steps (each step reads one and writes the
+// other); a full step uploads the lengths into lens.
 struct MetaLayout {
-  size_t slots, pairs, items, lens, tables, total;
+  size_t slots, pairs, items, lens, tables, lens_b, total;
   int32_t item_cap;
 };
 
@@ -57,6 +62,8 @@ MetaLayout layout(int32_t num_seqs, int32_t max_blocks) {
   off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
   m.tables = off;
   off = align_up(off + size_t(num_seqs) * size_t(max_blocks) * sizeof(int32_t));
+  m.lens_b = off;
+  off = align_up(off + size_t(num_seqs) * sizeof(int32_t));
   m.total = off;
   return m;
 }
@@ -73,6 +80,7 @@ struct GraphSlot {
   cudaGraphNode_t copy_node[3] = {nullptr, nullptr, nullptr};  // q, k, v
   const void *src[3] = {nullptr, nullptr, nullptr};
   const void *out = nullptr;  // the host output buffer the graph writes
+  int lens_cur = 0;           // the device length buffer it reads
 };
 
 // Library-managed state behind pk_step_buffers.state: the prepared step
@@ -94,6 +102,7 @@ struct StepState {
   int32_t max_ctx = 0;
   size_t meta_copy = 0;
   int32_t num_seqs = 0, max_blocks = 0;
+  int lens_cur = 0;  // device buffer holding the current lengths: 0 = lens, 1 = lens_b
 };
 
 void drop_slot(GraphSlot &g) {
@@ -172,7 +181,7 @@ pk_status pk_decode_step_prepare(pk_bm *bm, const int64_t *seq_ids, int32_t num_
   pk_status rc = pk_bm_append_batch(bm, seq_ids, num_seqs, slots, pairs, &npairs);
   if (rc != PK_OK) return rc;
   b->tables_resident = 0;  // until this step's metadata is on its way
-  size_t meta_copy = m.total;
+  size_t meta_copy = m.lens_b;  // a full step: everything up to the tables
   bool new_part = false;
   if (resident) {
     const int32_t part = b->plan_partition;
@@ -258,12 +267,29 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   };
 
   if (!resident || st->new_part || st->stream != s) drop_graphs(st);
-  const int64_t *dslots = reinterpret_cast<const int64_t *>(md + m.slots);
   int32_t *dtables = reinterpret_cast<int32_t *>(md + m.tables);
-  int32_t *dlens = reinterpret_cast<int32_t *>(md + m.lens);
+  // The step's slots: in zero-copy mode the resident kernel reads them from
+  // the staging half through its device mapping, so a steady step copies no
+  // metadata at all; otherwise from the device copy.
+  const int64_t *dslots = reinterpret_cast<const int64_t *>(md + m.slots);
+  bool slots_mapped = false;
+  if (zero_copy && resident) {
+    void *p = nullptr;
+    if (cudaHostGetDevicePointer(&p, const_cast<uint8_t *>(mh + m.slots), 0) == cudaSuccess) {
+      dslots = static_cast<const int64_t *>(p);
+      slots_mapped = true;
+    } else {
+      cudaGetLastError();  // not mapped: copy the slots as in the copying mode
+    }
+  }
+  const bool copy_meta = !(slots_mapped && npairs == 0 && !st->new_part);
+  // A resident step reads the lengths from one device buffer and writes the
+  // advanced lengths to the other; a full step uploads them into lens.
+  int32_t *lens_in = reinterpret_cast<int32_t *>(md + (st->lens_cur ? m.lens_b : m.lens));
+  int32_t *lens_out = reinterpret_cast<int32_t *>(md + (st->lens_cur ? m.lens : m.lens_b));
   // Everything the device does in a step after the input copies.
   auto enqueue_device = [&]() -> pk_status {
-    if (cudaMemcpyAsync(md, mh, meta_copy, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    if (copy_meta && cudaMemcpyAsync(md, mh, meta_copy, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return PK_ERR_CUDA;
     pk_status r = PK_OK;
     if (npairs > 0) {
@@ -271,15 +297,22 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
                          desc, stream);
       if (r != PK_OK) return r;
     }
-    r = resident ? pk_reshape_and_cache_append(kd, vd, dslots, num_seqs, k_cache, v_cache, desc,
-                                               dtables, max_blocks_per_seq, dlens, stream)
-                 : pk_reshape_and_cache(kd, vd, dslots, num_seqs, k_cache, v_cache, desc, stream);
-    if (r != PK_OK) return r;
-    r = pk_paged_attention_decode_items(
-        od, qd, k_cache, v_cache, dtables, dlens, scale, num_seqs, num_q_heads,
-        max_blocks_per_seq, max_ctx, b->plan_partition,
-        reinterpret_cast<const int32_t *>(md + m.items), b->plan_items, b->workspace,
-        b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
+    const int32_t *ditems = reinterpret_cast<const int32_t *>(md + m.items);
+    if (resident) {
+      // One launch: the scatter, the table bookkeeping and the attention.
+      r = pk_paged_attention_decode_advance(
+          od, qd, kd, vd, dslots, k_cache, v_cache, dtables, lens_in, lens_out, scale, num_seqs,
+          num_q_heads, max_blocks_per_seq, max_ctx, b->plan_partition, ditems, b->plan_items,
+          b->workspace, b->workspace_bytes, desc, stream);
+    } else {
+      int32_t *dlens = reinterpret_cast<int32_t *>(md + m.lens);
+      r = pk_reshape_and_cache(kd, vd, dslots, num_seqs, k_cache, v_cache, desc, stream);
+      if (r != PK_OK) return r;
+      r = pk_paged_attention_decode_items(od, qd, k_cache, v_cache, dtables, dlens, scale,
+                                          num_seqs, num_q_heads, max_blocks_per_seq, max_ctx,
+                                          b->plan_partition, ditems, b->plan_items, b->workspace,
+                                          b->workspace_bytes, desc, PK_ATTN_AUTO, stream);
+    }
     if (r != PK_OK) return r;
     if (!zero_copy &&
         cudaMemcpyAsync(b->out_host, b->out_dev, qbytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
@@ -290,6 +323,7 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   // free again once the stream passes this point.
   auto mark_half = [&]() -> pk_status {
     if (cudaEventRecord(st->done[h], s) != cudaSuccess) return PK_ERR_CUDA;
+    st->lens_cur = resident ? st->lens_cur ^ 1 : 0;
     b->tables_resident = 1;
     return PK_OK;
   };
@@ -300,6 +334,7 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   const bool steady = may_replay && npairs == 0 && !st->new_part;
   if (steady) {
     GraphSlot &g = st->slot[h];
+    if (g.exec && g.lens_cur != st->lens_cur) drop_slot(g);  // captured on the other length buffer
     if (!g.exec) {
       st->stream = s;
       bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
@@ -334,6 +369,7 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
       } else {
         for (int k = 0; k < 3; ++k) g.src[k] = srcs[k];
         g.out = b->out_host;
+        g.lens_cur = st->lens_cur;
       }
     }
     const bool moved = st->zero_copy &&

@@ -107,20 +107,24 @@ def test_resident_tables_over_many_steps(name, nseq, B, steps):
     lay = _meta_layout(S, maxb)
     tables, lens = b.bm.export_tables(range(S), maxb)
     assert np.array_equal(meta[lay["tables"]: lay["tables"] + 4 * S * maxb].view(np.int32).reshape(S, maxb), tables)
-    assert np.array_equal(meta[lay["lens"]: lay["lens"] + 4 * S].view(np.int32), lens)
+    # The resident steps alternate two length buffers, starting from the full
+    # step's upload into the first.
+    cur = lay["lens_b"] if (steps - 1) % 2 else lay["lens"]
+    assert np.array_equal(meta[cur: cur + 4 * S].view(np.int32), lens)
 
 
 def _meta_layout(S, maxb):
     """Offsets of the decode-step metadata sections (256-byte aligned, in the
-    order slots, pairs, work items, lens, tables)."""
+    order slots, pairs, work items, lens, tables, second lens)."""
     up = lambda x: (x + 255) // 256 * 256
     slots = 0
     pairs = up(slots + 8 * S)
     items = up(pairs + 16 * S)
     lens = up(items + 8 * min(S * (1 + maxb // 16), 65535))
     tables = up(lens + 4 * S)
-    assert 2 * up(tables + 4 * S * maxb) == pk.lib().pk_decode_step_meta_bytes(S, maxb)  # two halves
-    return {"slots": slots, "pairs": pairs, "items": items, "lens": lens, "tables": tables}
+    lens_b = up(tables + 4 * S * maxb)
+    assert 2 * up(lens_b + 4 * S) == pk.lib().pk_decode_step_meta_bytes(S, maxb)  # two halves
+    return {"slots": slots, "pairs": pairs, "items": items, "lens": lens, "tables": tables, "lens_b": lens_b}
 
 
 def test_invalidate_after_fork_reuploads_tables():
@@ -317,3 +321,77 @@ def test_pipelined_steps_match_the_stepwise_path(name, nseq, B, zero_copy):
     with pytest.raises(pk.PagedKVError):
         stepper.prepare()                  # one prepared step at a time
     stepper.release()
+
+
+@pytest.mark.parametrize("name,nseq,B,part", [("gqa8b", 24, None, -1), ("gqa8b", 24, None, 256),
+                                              ("prefix", 8, 8, -1), ("mixed", 40, None, -1),
+                                              ("long", 1, None, 1024), ("tiny", None, None, -1)])
+def test_advance_matches_append_then_attention(name, nseq, B, part):
+    """pk_paged_attention_decode_advance (scatter, table bookkeeping and
+    attention in one launch on resident tables, lengths alternating between
+    two buffers) against pk_reshape_and_cache_append followed by the
+    attention over the work list: outputs, pools, tables and lengths bit for
+    bit over steps that open blocks, copy on write (prefix) and start
+    partitions."""
+    wl = make_workload(name, block_size=B, num_seqs=nseq)
+    wl.enable_memo()
+    steps = 12
+    a = DecodeState(wl, "cuda", extra_tokens=steps)
+    b = DecodeState(wl, "cuda", extra_tokens=steps)
+    S, maxb = wl.num_seqs, a.max_blocks
+    ta, la = (torch.from_numpy(x).cuda() for x in a.bm.export_tables(range(S), maxb))
+    tb = ta.clone()
+    lb = [la.clone(), torch.full_like(la, -7)]
+    rp = None
+    for i in range(steps):
+        sa, sb = a.prepare_step(i), b.prepare_step(i)
+        assert np.array_equal(sa.slots, sb.slots)
+        da, db = a.upload(sa), b.upload(sb)
+        if rp is None:
+            rp, items = pk.pk_attention_plan(sa.ctx_lens, wl.num_q_heads, a.desc, part)
+        else:
+            items = pk.pk_attention_work_items(sa.ctx_lens, rp)
+        items = torch.from_numpy(items).cuda()
+        ws = a.alloc_workspace(sa.max_context_len, rp)
+        if len(sa.pairs):
+            pk.pk_copy_blocks(a.k_cache, a.v_cache, da["pairs"])
+            pk.pk_copy_blocks(b.k_cache, b.v_cache, db["pairs"])
+        out_a, out_b = a.new_out(), b.new_out()
+        pk.pk_reshape_and_cache_append(da["k"], da["v"], da["slots"], a.k_cache, a.v_cache, ta, la)
+        pk.pk_paged_attention_decode(out_a, da["q"], a.k_cache, a.v_cache, ta, la, wl.scale, sa.max_context_len,
+                                     rp, ws, work_items=items)
+        pk.pk_paged_attention_decode_advance(out_b, db["q"], db["k"], db["v"], db["slots"], b.k_cache, b.v_cache,
+                                             tb, lb[i % 2], lb[(i + 1) % 2], wl.scale, sb.max_context_len, rp,
+                                             items, ws)
+        torch.cuda.synchronize()
+        assert pk.pk_get_device_error()[0] == 0, f"step {i}"
+        assert np.array_equal(from_device(out_a), from_device(out_b)), f"step {i}"
+        assert np.array_equal(from_device(lb[(i + 1) % 2]), sa.ctx_lens), f"step {i}"
+        assert np.array_equal(from_device(la), sa.ctx_lens)
+        assert np.array_equal(from_device(tb), from_device(ta)), f"step {i}"
+        assert np.array_equal(from_device(tb), sa.tables), f"step {i}"
+    assert np.array_equal(from_device(a.k_cache), from_device(b.k_cache))
+    assert np.array_equal(from_device(a.v_cache), from_device(b.v_cache))
+
+
+def test_advance_records_a_slot_out_of_step():
+    """A slot that is not at offset len mod B of its block: recorded, and the
+    row's length is carried over unchanged."""
+    wl = make_workload("gqa8b", num_seqs=4)
+    st = DecodeState(wl, "cuda", extra_tokens=2)
+    S, maxb = wl.num_seqs, st.max_blocks
+    t, l_in = (torch.from_numpy(x).cuda() for x in st.bm.export_tables(range(S), maxb))
+    si = st.prepare_step(0)
+    d = st.upload(si)
+    rp, items = pk.pk_attention_plan(si.ctx_lens, wl.num_q_heads, st.desc, 0)
+    bad = d["slots"].clone()
+    bad[1] += 1
+    l_out = torch.full_like(l_in, -7)
+    pk.pk_get_device_error()
+    pk.pk_paged_attention_decode_advance(st.new_out(), d["q"], d["k"], d["v"], bad, st.k_cache, st.v_cache, t,
+                                         l_in, l_out, wl.scale, si.max_context_len, rp,
+                                         torch.from_numpy(items).cuda(), None)
+    kind, idx = pk.pk_get_device_error()
+    assert pk.DEVERR_NAMES[kind] == "context" and idx == 1
+    got = from_device(l_out)
+    assert got[1] == from_device(l_in)[1] and got[0] == si.ctx_lens[0]
