@@ -241,6 +241,22 @@ def host_cpu_model() -> str:
     return "unknown"
 
 
+_POOLS = {}
+
+
+def _oracle_pool(threads: int):
+    """One thread pool per size, created once (not inside a timed call)."""
+    from concurrent.futures import ThreadPoolExecutor
+    if threads not in _POOLS:
+        _POOLS[threads] = ThreadPoolExecutor(max_workers=threads)
+    return _POOLS[threads]
+
+
+def oracle_threads(threads: int, n_rows: int) -> int:
+    """Host threads the oracle timing uses for n_rows rows: at least four rows each."""
+    return max(1, min(threads, n_rows // 4))
+
+
 def time_oracle_rows(wl, ref, rows: np.ndarray, threads: int = 1):
     """Times the oracle's attention over the given (seq, head) rows; returns (seconds, kv bytes).
 
@@ -251,19 +267,18 @@ def time_oracle_rows(wl, ref, rows: np.ndarray, threads: int = 1):
     import oracle
     ctx = ref["ctx_lens"]
     args = (ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"], wl.scale, wl.dtype)
-    threads = max(1, min(threads, len(rows)))
+    threads = oracle_threads(threads, len(rows))
     if threads == 1:
         t0 = time.perf_counter()
         oracle.paged_attention(*args, select=rows)
         dt = time.perf_counter() - t0
     else:
-        from concurrent.futures import ThreadPoolExecutor
         order = np.argsort(-ctx[rows[:, 0]], kind="stable")
         shares = [np.ascontiguousarray(rows[order[i::threads]]) for i in range(threads)]
-        with ThreadPoolExecutor(max_workers=threads) as ex:
-            t0 = time.perf_counter()
-            list(ex.map(lambda sel: oracle.paged_attention(*args, select=sel), shares))
-            dt = time.perf_counter() - t0
+        ex = _oracle_pool(threads)
+        t0 = time.perf_counter()
+        list(ex.map(lambda sel: oracle.paged_attention(*args, select=sel), shares))
+        dt = time.perf_counter() - t0
     nbytes = int(sum(int(ctx[s]) for s, _ in rows)) * wl.head_dim * wl.esz * 2
     return dt, nbytes
 
@@ -292,7 +307,7 @@ def cpu_baseline(wl, ref, seconds: float):
     host threads, repeated until half the time budget is used (at least
     once), then a random sample of rows on one thread for the other half."""
     rows = all_rows(wl)
-    threads = host_threads()
+    threads = oracle_threads(host_threads(), len(rows))
     total_t, total_b, reps = 0.0, 0, 0
     while reps == 0 or total_t < seconds / 2:
         dt, nb = time_oracle_rows(wl, ref, rows, threads)
@@ -334,7 +349,7 @@ def run_reference(args):
     rng = np.random.default_rng(0)
     # Calibrate the per-row cost on a few rows, then size each step's sample
     # so that warm-up plus timed steps fit the time budget.
-    threads = host_threads()
+    threads = oracle_threads(host_threads(), len(rows))
     probe = rows[rng.choice(len(rows), size=min(4 * threads, len(rows)), replace=False)]
     dt, _ = time_oracle_rows(wl, ref, probe, threads)
     per_row = dt / len(probe)
@@ -355,9 +370,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / args.steps / frac,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, args, {"sample_rows_per_step": n, "rows_per_step": len(rows)}),
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "cpu": host_cpu_model(),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle_threads(threads, n), "kind": "oracle",
+                         "cpu": host_cpu_model(),
                          "sample": f"{n} of {len(rows)} attention rows per step (random), C, fp64, dealt to "
-                                   f"{threads} host threads; ms_per_step scaled to all rows"},
+                                   f"{oracle_threads(threads, n)} host threads; ms_per_step scaled to all rows"},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -395,3 +395,43 @@ def test_advance_records_a_slot_out_of_step():
     assert pk.DEVERR_NAMES[kind] == "context" and idx == 1
     got = from_device(l_out)
     assert got[1] == from_device(l_in)[1] and got[0] == si.ctx_lens[0]
+
+
+@pytest.mark.parametrize("G,d,B", [(1, 64, 8), (8, 128, 32), (4, 64, 16), (2, 128, 8)])
+def test_advance_shapes_against_the_oracle(G, d, B):
+    """The one-launch resident step over head sizes, group sizes and block
+    sizes, with lengths at the edges (a fresh sequence, block and stage
+    boundaries, a partition boundary): every step equals append + attention
+    bit for bit, and the last step matches the oracle's attention over the
+    block manager's tables."""
+    from workloads import Workload
+    lens = np.array([1, B - 1, B, 63, 64, 200, 511, 1200], dtype=np.int64)
+    N = int(sum(-(-int(c + 8) // B) for c in lens) + 16)
+    wl = Workload(f"adv{G}_{d}_{B}", len(lens), 2 * G, 2, d, B, "bf16", N, lens, seed=G * 11 + d + B)
+    wl.enable_memo()
+    steps = 6
+    a = DecodeState(wl, "cuda", extra_tokens=steps)
+    b = DecodeState(wl, "cuda", extra_tokens=steps)
+    S, maxb = wl.num_seqs, a.max_blocks
+    ta, la = (torch.from_numpy(x).cuda() for x in a.bm.export_tables(range(S), maxb))
+    tb, lb = ta.clone(), [la.clone(), torch.full_like(la, -7)]
+    for i in range(steps):
+        sa, sb = a.prepare_step(i), b.prepare_step(i)
+        da, db = a.upload(sa), b.upload(sb)
+        part = 64 if i % 2 else 0
+        items = torch.from_numpy(pk.pk_attention_work_items(sa.ctx_lens, part)).cuda()
+        ws = a.alloc_workspace(sa.max_context_len, part)
+        out_a, out_b = a.new_out(), b.new_out()
+        pk.pk_reshape_and_cache_append(da["k"], da["v"], da["slots"], a.k_cache, a.v_cache, ta, la)
+        pk.pk_paged_attention_decode(out_a, da["q"], a.k_cache, a.v_cache, ta, la, wl.scale, sa.max_context_len,
+                                     part, ws, work_items=items)
+        pk.pk_paged_attention_decode_advance(out_b, db["q"], db["k"], db["v"], db["slots"], b.k_cache, b.v_cache,
+                                             tb, lb[i % 2], lb[(i + 1) % 2], wl.scale, sb.max_context_len, part,
+                                             items, ws)
+        torch.cuda.synchronize()
+        assert pk.pk_get_device_error()[0] == 0, f"step {i}"
+        assert np.array_equal(from_device(out_a), from_device(out_b)), f"step {i}"
+        assert np.array_equal(from_device(tb), sa.tables) and np.array_equal(from_device(lb[(i + 1) % 2]), sa.ctx_lens)
+    ref = oracle.paged_attention(from_device(db["q"]), from_device(b.k_cache), from_device(b.v_cache), sb.tables,
+                                 sb.ctx_lens, wl.scale, wl.dtype)
+    assert_close(from_device(out_b), ref, wl.dtype, f"advance G={G} d={d} B={B}")
