@@ -628,10 +628,12 @@ typedef struct {
     size_t workspace_bytes;
     /* In: nonzero when meta_dev already holds these sequences' block tables
      * and context lengths as left by the previous successful pk_decode_step
-     * with the same seq_ids, max_blocks_per_seq and buffers, and the block
-     * manager has not touched them since (no fork, free, swap or append
-     * outside pk_decode_step). Out: 1 after a successful call, 0 otherwise.
-     * Set it to 0 whenever that does not hold. */
+     * (or pk_decode_step_launch) with the same seq_ids, max_blocks_per_seq
+     * and buffers, and the block manager has not touched them since (no
+     * fork, free, swap or append outside the decode step; none at all
+     * between a step's prepare and its launch). Out: 1 after a successful
+     * launch, 0 after a prepare or a failed call. Set it to 0 whenever that
+     * does not hold. */
     int32_t tables_resident;
     /* Library-managed (zero-initialise): the work plan of the resident steps,
      * its partition size and item count (see pk_attention_plan). */

@@ -713,7 +713,9 @@ class DecodeStepper:
     ``prepare()`` and ``launch_prepared()`` are the two halves of a step
     (pk_decode_step_prepare / pk_decode_step_launch): preparing step t+1
     right after launching step t overlaps its host work with step t on the
-    GPU.
+    GPU. Leave the block manager alone between a prepare and its launch;
+    other changes to it (fork, free, swap) go between steps, followed by
+    ``invalidate()``.
     """
 
     def __init__(self, bm: "BlockManager", seq_ids, num_q_heads: int, scale: float, max_blocks_per_seq: int,
