@@ -380,6 +380,13 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, int32_t partition_size,
                                          const pk_cache_desc *desc);
 
+/* Self-test of the bounded pipeline waits: one CTA waits on an mbarrier
+ * phase that nothing completes, polling at most `polls` times (0: the limit
+ * every pipeline wait of the attention kernels uses), then records
+ * PK_DEVERR_TIMEOUT (index 0) in the device error word and returns -- what a
+ * stuck pipeline stage does instead of hanging. Touches no caller memory. */
+pk_status pk_selftest_wait_timeout(uint32_t polls, void *stream);
+
 /* Reads the device error word of the current device into *code_out (0 = no
  * error; see PK_DEVERR_*) after synchronising `stream`, then clears it. */
 pk_status pk_get_device_error(int32_t *code_out, void *stream);

@@ -1110,6 +1110,21 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded pipeline waits: one thread waits on a phase of an
+// mbarrier that nothing completes, exactly as a stuck pipeline stage would,
+// and records the timeout instead of hanging.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32) wait_timeout_probe_kernel(uint32_t polls) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = pk::smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    pk::mbar_init(b, 1);
+    pk::fence_barrier_init();
+    if (!pk::mbar_wait(b, 0, polls)) pk::record_error(&g_attn_error, PK_DEVERR_TIMEOUT, 0);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Log-sum-exp merge of split-K partials for the CUDA-core kernel (the
 // tensor-core kernel fuses the same merge into its last partition).
 // ---------------------------------------------------------------------------
@@ -1632,6 +1647,12 @@ pk_status pk_paged_attention_decode_append(
                           num_q_heads, max_blocks_per_seq, max_context_len, partition_size,
                           workspace, workspace_bytes, desc, nullptr, work_items, num_items,
                           PK_ATTN_AUTO, stream, k_new, v_new, slot_mapping);
+}
+
+pk_status pk_selftest_wait_timeout(uint32_t polls, void *stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      polls ? polls : pk::kMaxWaitPolls);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
 pk_status pk_paged_attention_decode_advance(

@@ -23,8 +23,10 @@ __device__ __forceinline__ void record_error(int *word, int kind, long long inde
 
 // Upper bound on the polls of one pipeline wait. A wait that legitimately
 // finishes takes microseconds; past this bound the kernel records
-// PK_DEVERR_TIMEOUT and unwinds instead of spinning forever.
-constexpr uint32_t kMaxWaitPolls = 1u << 22;
+// PK_DEVERR_TIMEOUT and unwinds instead of spinning forever. An unsuccessful
+// mbarrier.try_wait suspends for a few microseconds (about 3.8 us measured
+// on GB300), so the bound is about one second.
+constexpr uint32_t kMaxWaitPolls = 1u << 18;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -62,9 +64,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxWaitPolls; ++i)
+// Waits for the phase with the given parity to complete; false after `polls`
+// unsuccessful polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t polls = kMaxWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
