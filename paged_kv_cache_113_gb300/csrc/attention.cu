@@ -391,6 +391,9 @@ struct MmaShape {
                                                                         : MERGE_BYTES);
   static_assert(D % 64 == 0, "head_dim must be a multiple of 64");
   static_assert(BS <= TPS && TPS % BS == 0 && BPS <= 32, "block size must divide the stage");
+  // The producer reads table entries in 32-entry chunks, one stage's blocks
+  // never straddling two chunks.
+  static_assert(32 % BPS == 0, "blocks per stage must divide 32");
 };
 
 // One warp's 16-token tile: scores S^T (16 tokens x 8 query columns) =
