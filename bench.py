@@ -279,7 +279,11 @@ def time_oracle_rows(wl, ref, rows: np.ndarray, threads: int = 1):
         t0 = time.perf_counter()
         list(ex.map(lambda sel: oracle.paged_attention(*args, select=sel), shares))
         dt = time.perf_counter() - t0
-    nbytes = int(sum(int(ctx[s]) for s, _ in rows)) * wl.head_dim * wl.esz * 2
+    # The step's algorithmic K/V bytes counted per query-head row: a KV head's
+    # bytes are shared by its group of Hq / Hk query heads, so each row counts
+    # 1 / group of them (a whole step sums to the same bytes as the GPU arm).
+    group = wl.num_q_heads // wl.num_kv_heads
+    nbytes = int(sum(int(ctx[s]) for s, _ in rows)) * wl.head_dim * wl.esz * 2 // group
     return dt, nbytes
 
 
