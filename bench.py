@@ -650,7 +650,7 @@ def run_e2e(st, wl, E, Ew, args, dev):
     torch.cuda.synchronize()
     stream = stepper.stream
     tot_t, tot_b = 0.0, 0
-    per_step = []
+    per_step, host_launch, host_prepare = [], [], []
     resident = True
     # The overlapped loop of a serving engine: each step's host half (block-
     # manager append, metadata) is prepared while the step before runs on the
@@ -665,7 +665,9 @@ def run_e2e(st, wl, E, Ew, args, dev):
         stepper.v_host.copy_(v)
         t0 = time.perf_counter()
         stepper.launch_prepared()
+        t1 = time.perf_counter()
         stepper.prepare()
+        t2 = time.perf_counter()
         stream.synchronize()
         dt = time.perf_counter() - t0
         st.steps_done += 1
@@ -674,6 +676,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
             tot_t += dt
             tot_b += step_kv_bytes(st, wl)
             per_step.append(dt)
+            host_launch.append(t1 - t0)
+            host_prepare.append(t2 - t1)
     kind, idx = pk.pk_get_device_error()
     if kind:
         raise RuntimeError(f"device error in the e2e steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
@@ -682,6 +686,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
     return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(stepper.h2d_bytes_resident),
             "d2h_bytes_per_step": int(stepper.d2h_bytes), "steps": E, "ms_per_step": 1e3 * tot_t / E,
             "ms_per_step_median": 1e3 * float(np.median(per_step)), "ms_per_step_max": 1e3 * max(per_step),
+            "host_us_median": {"launch": 1e6 * float(np.median(host_launch)),
+                               "prepare_next_overlapped": 1e6 * float(np.median(host_prepare))},
             "includes": "pk_decode_step_launch of the prepared step (device-resident block tables, its "
                         "own stream, zero-copy; one CUDA graph on steady steps: H2D of the slots, the "
                         "scatter reading the new K/V from pinned host memory and advancing the tables, the "
