@@ -618,7 +618,10 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
  * aligned. With q_dev, k_dev, v_dev and out_dev all NULL (zero-copy mode) the
  * host buffers must be pinned, device-mapped memory: the kernels read q and
  * the new K/V from, and write the output to, them directly -- the same bytes
- * cross the host link, inside the kernels rather than as separate copies. */
+ * cross the host link, inside the kernels rather than as separate copies. The
+ * device mapping of each such host address (and of meta_host) is looked up
+ * once and kept in the library-managed state: a host buffer freed and pinned
+ * again at the same address needs pk_decode_step_release first. */
 typedef struct {
     const void *q_host;  /* [S, Hq, d] queries of the step                     */
     const void *k_host;  /* [S, Hk, d] the step's new keys                      */

@@ -774,6 +774,7 @@ class DecodeStepper:
                            ctypes.c_void_p(k_cache.data_ptr()), ctypes.c_void_p(v_cache.data_ptr()),
                            ctypes.byref(self.desc), ctypes.byref(self.buffers))
         self._stream_arg = ctypes.c_void_p(self.stream.cuda_stream)
+        self._own_inputs = True  # the buffers struct points at q_host / k_host / v_host
         self._prepare_fn = lib().pk_decode_step_prepare
         self._prepare_args = (bm._h, _np_ptr(self.ids), S, self.Hq, self.maxb, self.partition,
                               ctypes.byref(self.desc), ctypes.byref(self.buffers))
@@ -784,8 +785,15 @@ class DecodeStepper:
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size()
 
     def _bind(self, stream, q_host, k_host, v_host):
-        for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
-            setattr(self.buffers, name, (getattr(self, name) if t is None else t).data_ptr())
+        if q_host is None and k_host is None and v_host is None:
+            if not self._own_inputs:  # back to the stepper's own buffers
+                for name in ("q_host", "k_host", "v_host"):
+                    setattr(self.buffers, name, getattr(self, name).data_ptr())
+                self._own_inputs = True
+        else:
+            for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host)):
+                setattr(self.buffers, name, (getattr(self, name) if t is None else t).data_ptr())
+            self._own_inputs = False
         if self._order_after_caller:
             # Work the caller enqueued before (the prefill, a copy after a
             # fork) must finish before the step's kernels touch the pool.

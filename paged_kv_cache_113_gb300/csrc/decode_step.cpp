@@ -103,7 +103,29 @@ struct StepState {
   size_t meta_copy = 0;
   int32_t num_seqs = 0, max_blocks = 0;
   int lens_cur = 0;  // device buffer holding the current lengths: 0 = lens, 1 = lens_b
+  // Device mappings of zero-copy host buffers, looked up once per address.
+  const void *map_host[8] = {};
+  void *map_dev[8] = {};
+  int map_next = 0;
 };
+
+// The device address of pinned host memory `h` (zero-copy), from the state's
+// small cache or the runtime; false if `h` is not mapped host memory.
+bool mapped(StepState *st, const void *h, void **d) {
+  for (int i = 0; i < 8; ++i)
+    if (st->map_host[i] == h && h) {
+      *d = st->map_dev[i];
+      return true;
+    }
+  if (cudaHostGetDevicePointer(d, const_cast<void *>(h), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  st->map_host[st->map_next] = h;
+  st->map_dev[st->map_next] = *d;
+  st->map_next = (st->map_next + 1) % 8;
+  return true;
+}
 
 void drop_slot(GraphSlot &g) {
   if (g.exec) cudaGraphExecDestroy(g.exec);  // freed once a launch in flight completes
@@ -233,14 +255,9 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   const bool zero_copy = !b->q_dev && !b->k_dev && !b->v_dev && !b->out_dev;
   if (!zero_copy && (!b->q_dev || !b->k_dev || !b->v_dev || !b->out_dev)) return PK_ERR_INVALID_ARG;
   void *qd = b->q_dev, *kd = b->k_dev, *vd = b->v_dev, *od = b->out_dev;
-  if (zero_copy &&
-      (cudaHostGetDevicePointer(&qd, const_cast<void *>(b->q_host), 0) != cudaSuccess ||
-       cudaHostGetDevicePointer(&kd, const_cast<void *>(b->k_host), 0) != cudaSuccess ||
-       cudaHostGetDevicePointer(&vd, const_cast<void *>(b->v_host), 0) != cudaSuccess ||
-       cudaHostGetDevicePointer(&od, b->out_host, 0) != cudaSuccess)) {
-    cudaGetLastError();
+  if (zero_copy && (!mapped(st, b->q_host, &qd) || !mapped(st, b->k_host, &kd) ||
+                    !mapped(st, b->v_host, &vd) || !mapped(st, b->out_host, &od)))
     return PK_ERR_INVALID_ARG;  // not pinned, mapped host memory
-  }
   const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int h = st->half;
@@ -275,11 +292,9 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   bool slots_mapped = false;
   if (zero_copy && resident) {
     void *p = nullptr;
-    if (cudaHostGetDevicePointer(&p, const_cast<uint8_t *>(mh + m.slots), 0) == cudaSuccess) {
+    if (mapped(st, mh + m.slots, &p)) {  // else copy the slots as in the copying mode
       dslots = static_cast<const int64_t *>(p);
       slots_mapped = true;
-    } else {
-      cudaGetLastError();  // not mapped: copy the slots as in the copying mode
     }
   }
   const bool copy_meta = !(slots_mapped && npairs == 0 && !st->new_part);
@@ -319,10 +334,11 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
       return PK_ERR_CUDA;
     return PK_OK;
   };
-  // After the step's work (never captured into a graph): the staging half is
-  // free again once the stream passes this point.
-  auto mark_half = [&]() -> pk_status {
-    if (cudaEventRecord(st->done[h], s) != cudaSuccess) return PK_ERR_CUDA;
+  // After the step's work: the staging half is free again once the stream
+  // passes this point. A captured graph records the event itself (an
+  // external event node), so a replay is a single call.
+  auto mark_half = [&](bool recorded) -> pk_status {
+    if (!recorded && cudaEventRecord(st->done[h], s) != cudaSuccess) return PK_ERR_CUDA;
     st->lens_cur = resident ? st->lens_cur ^ 1 : 0;
     b->tables_resident = 1;
     return PK_OK;
@@ -339,7 +355,9 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
       st->stream = s;
       bool ok = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
       if (ok) {
-        const bool enq = enqueue_inputs() && enqueue_device() == PK_OK;
+        const bool enq = enqueue_inputs() && enqueue_device() == PK_OK &&
+                         cudaEventRecordWithFlags(st->done[h], s, cudaEventRecordExternal) ==
+                             cudaSuccess;
         cudaGraph_t cg = nullptr;
         ok = cudaStreamEndCapture(s, &cg) == cudaSuccess && enq && cg;
         g.graph = cg;
@@ -385,14 +403,14 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
           g.src[k] = srcs[k];
         }
       if (cudaGraphLaunch(g.exec, s) != cudaSuccess) return PK_ERR_CUDA;
-      return mark_half();
+      return mark_half(true);
     }
   }
 
   if (!enqueue_inputs()) return PK_ERR_CUDA;
   const pk_status r = enqueue_device();
   if (r != PK_OK) return r;
-  return mark_half();
+  return mark_half(false);
 }
 
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
