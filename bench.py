@@ -124,6 +124,44 @@ def measured_hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
+def read_stream_peak(dev, gib: int = 4, reps: int = 5) -> dict:
+    """A read-only bandwidth reference measured in this run: the library's
+    pure read stream (pk_read_stream) over a buffer far larger than L2,
+    against the copy benchmark's read + write."""
+    import torch
+    import paged_kv_cache_113_gb300 as pk
+    x = torch.ones(gib << 28, dtype=torch.float32, device=dev)   # gib GiB
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = x.numel() * 4
+    st = torch.cuda.current_stream(dev).cuda_stream
+
+    def run():
+        rc = pk.lib().pk_read_stream(ctypes_ptr(x), nbytes, ctypes_ptr(sink), st)
+        if rc != 0:
+            raise RuntimeError(f"pk_read_stream: status {rc}")
+    for _ in range(2):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = reps * nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del x, sink
+    torch.cuda.empty_cache()
+    return {"value": gbs, "unit": "GB/s", "kernel": f"read_stream_kernel over {gib} GiB (each 16-byte vector once)"}
+
+
+def ctypes_ptr(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def source_hash():
     h = hashlib.sha256()
     for rel in SRC_FOR_TRAFFIC:
@@ -559,6 +597,7 @@ def run_ours(args):
     value = job_throughput(world, total_bytes, t_step)
     attn_gbs = total_bytes / t_attn / 1e9
     peak, peak_kind = measured_hbm_peak()
+    read_peak = read_stream_peak(dev) if rank == 0 else None
 
     e2e = None
     if E:
@@ -588,6 +627,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": mean_ms, "steps_per_s": 1e3 / mean_ms,
             "pct_of_peak": 100.0 * value / world / peak, "peak_kind": peak_kind,
+            "pct_of_nominal_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": workload_config(wl, args, {
@@ -611,6 +651,8 @@ def run_ours(args):
                          "bytes_per_launch": total_bytes / args.steps, "ms_per_launch": 1e3 * t_attn / args.steps},
             "attention_gbs": attn_gbs,
             "attention_unique_gbs": total_unique / t_attn / 1e9,
+            "read_stream_peak": (dict(read_peak, attention_frac=attn_gbs / read_peak["value"])
+                                 if read_peak else None),
             "gpu_launches": n_launch,
             "wall_s_timed_region": wall,
             "clocks": clocks,

@@ -380,6 +380,13 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, int32_t partition_size,
                                          const pk_cache_desc *desc);
 
+/* A pure read stream over `bytes` (a multiple of 16; device memory, 16-byte
+ * aligned): every 16-byte vector is loaded once and the loads are folded so
+ * none can be dropped; *sink (device) is left unchanged in practice. A
+ * reference for the read bandwidth the attention kernels can reach, measured
+ * by the benchmark beside them. Not part of the decode path. */
+pk_status pk_read_stream(const void *buf, size_t bytes, unsigned int *sink, void *stream);
+
 /* Self-test of the bounded pipeline waits: one CTA waits on an mbarrier
  * phase that nothing completes, polling at most `polls` times (0: the limit
  * every pipeline wait of the attention kernels uses), then records

@@ -46,7 +46,7 @@ EXPORTED = (
     "pk_reshape_and_cache", "pk_reshape_and_cache_append", "pk_copy_blocks", "pk_paged_attention_decode",
     "pk_paged_attention_decode_impl", "pk_paged_attention_decode_static", "pk_paged_attention_decode_items",
     "pk_attention_work_items", "pk_attention_plan", "pk_paged_attention_decode_append",
-    "pk_paged_attention_decode_advance", "pk_selftest_wait_timeout",
+    "pk_paged_attention_decode_advance", "pk_selftest_wait_timeout", "pk_read_stream",
     "pk_paged_attention_resolve_partition",
     "pk_paged_attention_workspace_size", "pk_longest_first_order", "pk_get_device_error", "pk_status_string",
     "pk_bm_create", "pk_bm_destroy", "pk_bm_add_seq", "pk_bm_append_slots", "pk_bm_append_batch",
@@ -132,6 +132,7 @@ def lib() -> ctypes.CDLL:
         "pk_paged_attention_decode_append": (i32, [P, P, P, P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P,
                                                    i32, P, sz, D, P]),
         "pk_selftest_wait_timeout": (i32, [ctypes.c_uint32, P]),
+        "pk_read_stream": (i32, [P, sz, P, P]),
         "pk_paged_attention_decode_advance": (i32, [P, P, P, P, P, P, P, P, P, P, f32, i32, i32, i32, i32, i32,
                                                      P, i32, P, sz, D, P]),
         "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),

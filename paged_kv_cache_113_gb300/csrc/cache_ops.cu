@@ -63,6 +63,30 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
   v_cache[s * row_vecs + j] = b;
 }
 
+// A pure read stream, the reference the attention's K/V reads are measured
+// against: every 16-byte vector of the buffer is loaded once (four loads in
+// flight per thread, grid-strided) and folded into one XOR so that no load
+// can be dropped.
+__global__ void __launch_bounds__(256) read_stream_kernel(const uint4 *__restrict__ buf,
+                                                          int64_t n, unsigned int *sink) {
+  constexpr int U = 4;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + (U - 1) * stride < n; i += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = __ldg(buf + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < n; i += stride) {
+    const uint4 a = __ldg(buf + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+  if (acc == 0x9e3779b9u) atomicXor(sink, acc);  // practically never taken; keeps the loads
+}
+
 // grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block.
 // The whole block src is copied to dst ("paged attention deep",
 // "Copy-on-write for shared prefixes").
@@ -230,6 +254,17 @@ pk_status pkx_reshape_and_cache_advance(const void *k, const void *v, const int6
       static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_slots,
       int32_t(row_vecs), block_tables, lens_in, lens_out, max_blocks_per_seq, desc->block_size);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
+pk_status pk_read_stream(const void *buf, size_t bytes, unsigned int *sink, void *stream) {
+  if (!buf || !sink || bytes < 16 || !aligned16(buf)) return PK_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PK_ERR_CUDA;
+  read_stream_kernel<<<sms * 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4 *>(buf), int64_t(bytes / 16), sink);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
