@@ -610,3 +610,12 @@ def test_decode_step_prepare_and_launch_pair_up(L):
     bm.check_invariants()
     L.pk_decode_step_release(ctypes.byref(buf))
     assert not buf.state
+
+
+def test_read_stream_rejects_bad_arguments_before_any_launch(L):
+    buf = np.zeros(64, dtype=np.uint8)
+    sink = np.zeros(1, dtype=np.uint32)
+    assert L.pk_read_stream(None, 64, sink.ctypes.data, None) == pk.PK_ERR_INVALID_ARG
+    assert L.pk_read_stream(buf.ctypes.data, 8, sink.ctypes.data, None) == pk.PK_ERR_INVALID_ARG
+    assert L.pk_read_stream(buf.ctypes.data, 64, None, None) == pk.PK_ERR_INVALID_ARG
+    assert L.pk_read_stream(buf.ctypes.data + 4, 48, sink.ctypes.data, None) == pk.PK_ERR_INVALID_ARG

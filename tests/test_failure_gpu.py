@@ -46,3 +46,14 @@ def test_stuck_wait_times_out_reports_and_leaves_the_context_usable():
     torch.cuda.synchronize()
     assert pk.pk_get_device_error()[0] == 0
     assert_close(from_device(out), ref["out"], wl.dtype, "after the timeout")
+
+
+def test_read_stream_reference_runs_and_leaves_its_sink():
+    x = torch.zeros(1 << 24, dtype=torch.float32, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    import ctypes
+    for nbytes in (x.numel() * 4, 16, 16 * 1000 + 16):
+        assert pk.lib().pk_read_stream(ctypes.c_void_p(x.data_ptr()), nbytes, ctypes.c_void_p(sink.data_ptr()),
+                                       None) == pk.PK_OK
+    torch.cuda.synchronize()
+    assert int(sink.item()) == 0
