@@ -163,10 +163,15 @@ def ctypes_ptr(t):
 
 
 def source_hash():
+    """Hash of the attention kernels' source with // comments and blank lines
+    removed, so that comment edits do not retire the recorded traffic."""
     h = hashlib.sha256()
     for rel in SRC_FOR_TRAFFIC:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -24,8 +24,11 @@
 //                      softmax in registers; the softmax weights enter PV as a
 //                      bf16 hi + lo pair. Split partitions write partials and
 //                      the last one to finish merges them (log-sum-exp).
-//                      In cascade mode it covers each sequence's tokens after
-//                      its group's shared prefix.
+//                      With the step's new K/V it also writes them (the CTA
+//                      holding the token, for its head: the scatter fused in);
+//                      in advance mode it also advances device-resident block
+//                      tables and lengths. In cascade mode it covers each
+//                      sequence's tokens after its group's shared prefix.
 //   attn_cascade_kernel bf16, cascade attention in one launch: prefix CTAs
 //                      (one per KV head, group and prefix partition) stream a
 //                      shared prefix once for all of the group's query
@@ -34,6 +37,8 @@
 //   attn_simt_kernel   fp32 or bf16 on CUDA cores: one warp per token,
 //                      shuffle-reduced dot products, online softmax.
 //   attn_merge_kernel  log-sum-exp merge of the CUDA-core kernel's partials.
+//   wait_timeout_probe_kernel  the bounded pipeline wait on a phase nothing
+//                      completes (pk_selftest_wait_timeout).
 //
 // Host side: the entry points, the automatic partition (pk_paged_attention_
 // resolve_partition: fill the resident CTA slots once), the work-list

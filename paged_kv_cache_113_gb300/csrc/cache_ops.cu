@@ -1,8 +1,10 @@
-// Cache writes of libpagedkv: the slot scatter (pk_reshape_and_cache) and the
-// copy-on-write block copy (pk_copy_blocks), plus the library's status
-// strings and device-error readout.
+// Cache writes of libpagedkv: the slot scatter (pk_reshape_and_cache, and
+// pk_reshape_and_cache_append on resident tables), the copy-on-write block
+// copy (pk_copy_blocks) and the swap copy (pk_swap_blocks), plus the
+// read-stream reference (pk_read_stream), the library's status strings and
+// device-error readout.
 //
-// Both kernels are pure data movement. The pool layout [N, B, Hk, d] makes one
+// The cache kernels are pure data movement. The pool layout [N, B, Hk, d] makes one
 // token's K (all heads) a contiguous Hk*d*esz-byte row, and one block a
 // contiguous B*Hk*d*esz-byte span, so both kernels are 16-byte vector copies.
 #include <cuda_runtime.h>
