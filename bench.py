@@ -675,9 +675,11 @@ def run_ours(args):
 
 def run_e2e(st, wl, E, Ew, args, dev):
     """The same decode steps through the public API from pinned host memory:
-    one pk_decode_step call per step (host block-manager append, table
-    export and launch order, one metadata transfer plus the q/k/v copies, the
-    kernels, the output copy back), then a stream synchronise."""
+    per step pk_decode_step_launch of the prepared step (zero-copy: the
+    kernels read q, the new K/V and the slots from pinned host memory and
+    write the output back to it), pk_decode_step_prepare of the next step
+    (host block-manager append, overlapped with the GPU), then a stream
+    synchronise."""
     import torch
     import paged_kv_cache_113_gb300 as pk
 
@@ -736,10 +738,10 @@ def run_e2e(st, wl, E, Ew, args, dev):
             "host_us_median": {"launch": 1e6 * float(np.median(host_launch)),
                                "prepare_next_overlapped": 1e6 * float(np.median(host_prepare))},
             "includes": "pk_decode_step_launch of the prepared step (device-resident block tables, its "
-                        "own stream, zero-copy; one CUDA graph on steady steps: H2D of the slots, the "
-                        "scatter reading the new K/V from pinned host memory and advancing the tables, the "
-                        "attention reading q from and writing the output to pinned host memory over the "
-                        "host link), then pk_decode_step_prepare of the next step (host block-manager "
+                        "own stream, zero-copy; one CUDA graph of one kernel on steady steps: the scatter "
+                        "reading the slots and the new K/V from pinned host memory and advancing the "
+                        "tables, the attention reading q from and writing the output to pinned host "
+                        "memory over the host link), then pk_decode_step_prepare of the next step (host block-manager "
                         "append, overlapped with the GPU), stream sync",
             "_seconds": tot_t, "_bytes": tot_b}
 
