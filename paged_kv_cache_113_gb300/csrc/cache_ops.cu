@@ -89,14 +89,34 @@ __global__ void __launch_bounds__(256) read_stream_kernel(const uint4 *__restric
   if (acc == 0x9e3779b9u) atomicXor(sink, acc);  // practically never taken; keeps the loads
 }
 
+// Block copies run kCopyThreads threads per CTA, each moving up to kCopyVecs
+// 16-byte vectors of one chunk (32 KiB per CTA).
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecs = 8;
+
+// Copies vectors [beg, end) of a chunk (at most kCopyThreads * kCopyVecs):
+// each thread issues all its loads before its first store, so a chunk costs
+// one memory round trip.
+__device__ __forceinline__ void copy_chunk(const uint4 *from, uint4 *to, int64_t beg, int64_t end) {
+  uint4 v[kCopyVecs];
+#pragma unroll
+  for (int k = 0; k < kCopyVecs; ++k) {
+    const int64_t j = beg + threadIdx.x + int64_t(k) * kCopyThreads;
+    if (j < end) v[k] = from[j];
+  }
+#pragma unroll
+  for (int k = 0; k < kCopyVecs; ++k) {
+    const int64_t j = beg + threadIdx.x + int64_t(k) * kCopyThreads;
+    if (j < end) to[j] = v[k];
+  }
+}
+
 // grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block.
 // The whole block src is copied to dst ("paged attention deep",
 // "Copy-on-write for shared prefixes").
-__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_cache,
-                                                          uint4 *__restrict__ v_cache,
-                                                          const int64_t *__restrict__ pairs,
-                                                          int32_t num_blocks, int64_t block_vecs,
-                                                          int64_t chunk_vecs) {
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
+    uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache, const int64_t *__restrict__ pairs,
+    int32_t num_blocks, int64_t block_vecs, int64_t chunk_vecs) {
   const int64_t src = pairs[2 * blockIdx.x];
   const int64_t dst = pairs[2 * blockIdx.x + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -105,30 +125,16 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
     return;
   }
   uint4 *pool = blockIdx.y == 0 ? k_cache : v_cache;
-  const uint4 *from = pool + src * block_vecs;
-  uint4 *to = pool + dst * block_vecs;
   const int64_t beg = int64_t(blockIdx.z) * chunk_vecs;
-  const int64_t end = min(block_vecs, beg + chunk_vecs);
-  int64_t j = beg + threadIdx.x;
-  // Four independent 16-byte loads in flight per thread.
-  for (; j + 3 * int64_t(blockDim.x) < end; j += 4 * int64_t(blockDim.x)) {
-    const uint4 a = from[j];
-    const uint4 b = from[j + blockDim.x];
-    const uint4 c = from[j + 2 * blockDim.x];
-    const uint4 d = from[j + 3 * blockDim.x];
-    to[j] = a;
-    to[j + blockDim.x] = b;
-    to[j + 2 * blockDim.x] = c;
-    to[j + 3 * blockDim.x] = d;
-  }
-  for (; j < end; j += blockDim.x) to[j] = from[j];
+  copy_chunk(pool + src * block_vecs, pool + dst * block_vecs, beg,
+             min(block_vecs, beg + chunk_vecs));
 }
 
 // grid.x = pair, grid.y = 0 for K / 1 for V, grid.z = chunk of the block:
 // whole block pairs[2p] of one pool goes to block pairs[2p+1] of the other
 // (swap out: device pool -> pinned host pool; swap in: the reverse). The host
 // pool is read or written through its device-visible address.
-__global__ void __launch_bounds__(256) swap_blocks_kernel(
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
     const uint4 *__restrict__ from_k, const uint4 *__restrict__ from_v, uint4 *__restrict__ to_k,
     uint4 *__restrict__ to_v, const int64_t *__restrict__ pairs, int32_t from_blocks,
     int32_t to_blocks, int64_t block_vecs, int64_t chunk_vecs) {
@@ -139,22 +145,10 @@ __global__ void __launch_bounds__(256) swap_blocks_kernel(
       pk::record_error(&g_cache_ops_error, PK_DEVERR_PAIR, blockIdx.x);
     return;
   }
-  const uint4 *from = (blockIdx.y == 0 ? from_k : from_v) + src * block_vecs;
-  uint4 *to = (blockIdx.y == 0 ? to_k : to_v) + dst * block_vecs;
   const int64_t beg = int64_t(blockIdx.z) * chunk_vecs;
-  const int64_t end = min(block_vecs, beg + chunk_vecs);
-  int64_t j = beg + threadIdx.x;
-  for (; j + 3 * int64_t(blockDim.x) < end; j += 4 * int64_t(blockDim.x)) {
-    const uint4 a = from[j];
-    const uint4 b = from[j + blockDim.x];
-    const uint4 c = from[j + 2 * blockDim.x];
-    const uint4 d = from[j + 3 * blockDim.x];
-    to[j] = a;
-    to[j + blockDim.x] = b;
-    to[j + 2 * blockDim.x] = c;
-    to[j + 3 * blockDim.x] = d;
-  }
-  for (; j < end; j += blockDim.x) to[j] = from[j];
+  copy_chunk((blockIdx.y == 0 ? from_k : from_v) + src * block_vecs,
+             (blockIdx.y == 0 ? to_k : to_v) + dst * block_vecs, beg,
+             min(block_vecs, beg + chunk_vecs));
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -281,11 +275,11 @@ pk_status pk_copy_blocks(void *k_cache, void *v_cache, const int64_t *src_dst_pa
   const int64_t block_bytes = int64_t(desc->block_size) * desc->num_kv_heads * desc->head_dim *
                               elem_size(desc->dtype);
   const int64_t block_vecs = block_bytes / 16;
-  const int64_t chunk_vecs = 256 * 8;  // 32 KiB per CTA
+  const int64_t chunk_vecs = int64_t(kCopyThreads) * kCopyVecs;
   const int64_t chunks = (block_vecs + chunk_vecs - 1) / chunk_vecs;
   if (chunks > 65535) return PK_ERR_UNSUPPORTED;
   dim3 grid(num_pairs, 2, unsigned(chunks));
-  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), src_dst_pairs,
       desc->num_blocks, block_vecs, chunk_vecs);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
@@ -312,12 +306,12 @@ pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_hos
   const int64_t block_bytes = int64_t(desc->block_size) * desc->num_kv_heads * desc->head_dim *
                               elem_size(desc->dtype);
   const int64_t block_vecs = block_bytes / 16;
-  const int64_t chunk_vecs = 256 * 8;
+  const int64_t chunk_vecs = int64_t(kCopyThreads) * kCopyVecs;
   const int64_t chunks = (block_vecs + chunk_vecs - 1) / chunk_vecs;
   if (chunks > 65535) return PK_ERR_UNSUPPORTED;
   dim3 grid(num_pairs, 2, unsigned(chunks));
   const bool out = direction == PK_SWAP_OUT;
-  swap_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  swap_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const uint4 *>(out ? k_cache : dk), static_cast<const uint4 *>(out ? v_cache : dv),
       static_cast<uint4 *>(out ? dk : k_cache), static_cast<uint4 *>(out ? dv : v_cache), pairs,
       out ? desc->num_blocks : num_host_blocks, out ? num_host_blocks : desc->num_blocks, block_vecs,
