@@ -619,3 +619,114 @@ def test_read_stream_rejects_bad_arguments_before_any_launch(L):
     assert L.pk_read_stream(buf.ctypes.data, 8, sink.ctypes.data, None) == pk.PK_ERR_INVALID_ARG
     assert L.pk_read_stream(buf.ctypes.data, 64, None, None) == pk.PK_ERR_INVALID_ARG
     assert L.pk_read_stream(buf.ctypes.data + 4, 48, sink.ctypes.data, None) == pk.PK_ERR_INVALID_ARG
+
+
+def test_advance_rejects_bad_arguments_before_any_launch(L):
+    # Host buffers stand in for device pointers: every case below returns from
+    # the argument checks, before anything is read or launched.
+    S, Hq, maxb = 4, 32, 8
+    buf = np.zeros(1 << 16, dtype=np.uint8)
+    base = (buf.ctypes.data + 255) // 256 * 256
+    ptr = [base + 4096 * i for i in range(12)]
+    out, q, kn, vn, slots, kc, vc, tables, lens, lens_out, items, ws = ptr
+    d = _desc()
+
+    def call(**kw):
+        a = dict(out=out, q=q, kn=kn, vn=vn, slots=slots, kc=kc, vc=vc, tables=tables, lens=lens,
+                 lens_out=lens_out, scale=0.088, S=S, Hq=Hq, maxb=maxb, max_ctx=100, part=0,
+                 items=items, n_items=S, ws=ws, ws_bytes=4096)
+        a.update(kw)
+        return L.pk_paged_attention_decode_advance(
+            a["out"], a["q"], a["kn"], a["vn"], a["slots"], a["kc"], a["vc"], a["tables"], a["lens"],
+            a["lens_out"], a["scale"], a["S"], a["Hq"], a["maxb"], a["max_ctx"], a["part"], a["items"],
+            a["n_items"], a["ws"], a["ws_bytes"], ctypes.byref(d), None)
+
+    assert call(S=0) == pk.PK_OK                                  # empty batch: nothing to do
+    assert call(items=None) == pk.PK_ERR_INVALID_ARG              # the work list is required
+    assert call(kn=None) == pk.PK_ERR_INVALID_ARG                 # so are the new K/V and slots
+    assert call(vn=None) == pk.PK_ERR_INVALID_ARG
+    assert call(slots=None) == pk.PK_ERR_INVALID_ARG
+    assert call(lens_out=None) == pk.PK_ERR_INVALID_ARG           # and a separate output length buffer
+    assert call(lens_out=lens) == pk.PK_ERR_INVALID_ARG
+    assert call(tables=None) == pk.PK_ERR_INVALID_ARG
+    assert call(q=q + 4) == pk.PK_ERR_INVALID_ARG                 # 16-byte alignment
+    assert call(kn=kn + 8) == pk.PK_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == pk.PK_ERR_INVALID_ARG
+    assert call(Hq=12) == pk.PK_ERR_INVALID_ARG                   # Hq not a multiple of Hk
+    assert call(part=40) == pk.PK_ERR_INVALID_ARG                 # partition not a multiple of B
+    assert call(n_items=0) == pk.PK_ERR_UNSUPPORTED               # work-list size out of range
+    assert call(n_items=70000) == pk.PK_ERR_UNSUPPORTED
+
+
+def test_other_entry_points_reject_bad_arguments_before_any_launch(L):
+    # As above: host buffers stand in for device memory and no case gets past
+    # the argument checks (none reaches a CUDA call).
+    buf = np.zeros(1 << 16, dtype=np.uint8)
+    base = (buf.ctypes.data + 255) // 256 * 256
+    ptr = [base + 2048 * i for i in range(20)]
+    out, q, kc, vc, tables, lens, items, ws, kn, vn, slots, goff, gmem, gpre, spre, kh, vh, pairs = ptr[:18]
+    d = _desc()                       # 64 blocks of 16 tokens, 8 KV heads, d = 128, bf16
+    f = ctypes.c_float(0.088)
+    byref = ctypes.byref
+
+    def items_call(**kw):
+        a = dict(out=out, q=q, S=4, Hq=32, items=items, n=4, ws=ws)
+        a.update(kw)
+        return L.pk_paged_attention_decode_items(a["out"], a["q"], kc, vc, tables, lens, f, a["S"], a["Hq"],
+                                                  8, 100, 0, a["items"], a["n"], a["ws"], 4096, byref(d),
+                                                  pk.IMPLS["auto"], None)
+
+    assert items_call(S=0) == pk.PK_OK
+    assert items_call(items=None) == pk.PK_ERR_INVALID_ARG
+    assert items_call(out=out + 2) == pk.PK_ERR_INVALID_ARG
+    assert items_call(n=0) == pk.PK_ERR_UNSUPPORTED
+    assert items_call(Hq=12) == pk.PK_ERR_INVALID_ARG
+
+    def append_call(**kw):
+        a = dict(kn=kn, vn=vn, slots=slots, items=items)
+        a.update(kw)
+        return L.pk_paged_attention_decode_append(out, q, a["kn"], a["vn"], a["slots"], kc, vc, tables, lens, f,
+                                                   4, 32, 8, 100, 0, a["items"], 4, ws, 4096, byref(d), None)
+
+    for k in ("kn", "vn", "slots", "items"):
+        assert append_call(**{k: None}) == pk.PK_ERR_INVALID_ARG
+    assert append_call(vn=vn + 8) == pk.PK_ERR_INVALID_ARG
+
+    def static_call(S=4, Hq=32, max_ctx=100, part=0):
+        return L.pk_paged_attention_decode_static(out, q, kc, vc, tables, lens, f, S, Hq, 2048, max_ctx, part,
+                                                  byref(d), None)
+
+    assert static_call(Hq=12) == pk.PK_ERR_INVALID_ARG
+    assert static_call(part=40) == pk.PK_ERR_INVALID_ARG
+    # 64 x 64 heads x 2048 partitions of fp32 partials: far above the fixed scratch.
+    assert static_call(S=64, Hq=64, max_ctx=32768, part=16) == pk.PK_ERR_WORKSPACE
+
+    def cascade_call(**kw):
+        a = dict(q=q, S=4, part=0, goff=goff, ngroups=1, gmax=2, maxpre=64, ws=ws, ws_bytes=0)
+        a.update(kw)
+        return L.pk_cascade_attention_decode(out, a["q"], kc, vc, tables, lens, f, a["S"], 32, 8, 100, a["part"],
+                                             a["goff"], gmem, gpre, spre, a["ngroups"], a["gmax"], a["maxpre"],
+                                             None, a["ws"], a["ws_bytes"], byref(d), None)
+
+    assert cascade_call(S=0, ngroups=0) == pk.PK_OK            # no groups: plain attention, empty batch
+    assert cascade_call(ngroups=-1) == pk.PK_ERR_INVALID_ARG
+    assert cascade_call(gmax=5) == pk.PK_ERR_UNSUPPORTED       # 5 members x G = 4 > 16 query columns
+    assert cascade_call(goff=None) == pk.PK_ERR_INVALID_ARG
+    assert cascade_call(q=q + 4) == pk.PK_ERR_INVALID_ARG
+    assert cascade_call(part=40) == pk.PK_ERR_INVALID_ARG
+    assert cascade_call(ws=None) == pk.PK_ERR_WORKSPACE
+    assert cascade_call(ws_bytes=16) == pk.PK_ERR_WORKSPACE
+
+    def swap_call(**kw):
+        a = dict(kc=kc, kh=kh, nhost=16, n=2, direction=pk.PK_SWAP_OUT, desc=d)
+        a.update(kw)
+        return L.pk_swap_blocks(a["kc"], vc, a["kh"], vh, a["nhost"], pairs, a["n"], a["direction"],
+                                byref(a["desc"]), None)
+
+    assert swap_call(n=0) == pk.PK_OK
+    assert swap_call(n=-1) == pk.PK_ERR_INVALID_ARG
+    assert swap_call(nhost=-1) == pk.PK_ERR_INVALID_ARG
+    assert swap_call(direction=5) == pk.PK_ERR_INVALID_ARG
+    assert swap_call(kh=None) == pk.PK_ERR_INVALID_ARG
+    assert swap_call(kc=kc + 4) == pk.PK_ERR_INVALID_ARG
+    assert swap_call(desc=_desc(dt=7)) == pk.PK_ERR_UNSUPPORTED
