@@ -20,6 +20,11 @@ the kernels and the device->host copy of the output are all inside the timer.
 blocks to a pinned host pool and back, one pk_swap_blocks launch per
 direction, beside a contiguous copy-engine copy of the same bytes.
 ``allocator_sim`` (host) is the allocator policy table on the seeded traces.
+``configs`` (a default single-GPU run of the default workload) times the
+other target configurations the same way, each with its own roofline
+fraction: the 8B-like GQA batch, the 32K-context batch (the planner's
+partitions and the 512-token partitions), and the shared-prefix batch at
+block sizes 8 / 16 / 32, per sequence and as cascade attention.
 
 Metric: algorithmic K/V bytes read per step (sum over sequences of
 context_len * Hk * head_dim * 2 bytes * 2 for K and V) per second.
@@ -80,6 +85,9 @@ def parse_args(argv=None):
                    help="cascade attention: each shared prefix read once per group (prefix workload)")
     p.add_argument("--no-swap", action="store_true", help="skip the swap-out / swap-in bandwidth measurement")
     p.add_argument("--no-allocator-sim", action="store_true", help="skip the allocator policy table")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the target configurations timed beside the default workload (gqa8b, long, prefix)")
+    p.add_argument("--config-steps", type=int, default=100, help="timed steps of each extra configuration")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline time budget")
     p.add_argument("--reference-seconds", type=float, default=90.0, help="reference arm time budget")
     a = p.parse_args(argv)
@@ -430,6 +438,255 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+class StepOptions:
+    """How a decode step is launched (the bench flags that shape the step)."""
+
+    def __init__(self, partition=-1, attn_impl="auto", cascade=False, grid=False, no_order=False, no_fuse=False,
+                 no_graphs=False):
+        self.partition, self.attn_impl, self.cascade = partition, attn_impl, cascade
+        self.grid, self.no_order, self.no_fuse, self.no_graphs = grid, no_order, no_fuse, no_graphs
+
+    @classmethod
+    def from_args(cls, args):
+        return cls(args.partition, args.attn_impl, args.cascade, args.grid, args.no_order, args.no_fuse,
+                   args.no_graphs)
+
+
+class L2Flush:
+    """Evicts L2 between steps: writes 2x L2, then reads 2x L2 so that the
+    next step starts on a cold and clean L2 (no dirty lines to write back)."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+        self.buf.sum()
+
+
+def time_device_steps(st, wl, dev, opt: StepOptions, steps: int, warmup: int, window: int, reserve: int,
+                      flush: L2Flush, world: int = 1, sampler=None):
+    """Device time of ``steps`` decode steps of the state ``st``.
+
+    The host side of a window of steps is prepared and uploaded first; each
+    window step is captured as CUDA graphs (copy_blocks when pairs exist; the
+    attention, with the step's scatter fused in by default) and the timed
+    steps cycle through the window. Each step is bracketed by CUDA events on
+    the launching stream, L2 flushed between steps outside the events.
+    ``reserve`` is the number of tokens later phases may still append (it
+    sizes the workspace). Returns the raw sums; the caller reduces over ranks.
+    """
+    import torch
+    import paged_kv_cache_113_gb300 as pk
+
+    R = max(1, min(window, steps + warmup))
+    host_steps = [st.prepare_step() for _ in range(R)]
+    dsteps = [st.upload(si) for si in host_steps]
+    planned = not (opt.cascade or opt.grid or opt.no_order)
+    # The default step: copy-on-write copies (if any), then one attention
+    # launch that also writes the step's new K/V (the scatter fused in).
+    fused = planned and not opt.no_fuse and opt.attn_impl == "auto"
+    if planned:
+        # The default schedule: each step's work list from the host planner
+        # (pk_attention_plan), longest item first.
+        for si, d in zip(host_steps, dsteps):
+            d["partition"], d["items"] = st.plan(si, opt.partition)
+    step_bytes = [wl.kv_bytes(si.ctx_lens) for si in host_steps]
+    step_unique = [unique_kv_bytes(wl, si) for si in host_steps]
+    max_ctx = max(si.max_context_len for si in host_steps) + reserve
+    if planned:
+        ws_bytes = max(st.workspace_bytes(max_ctx, d["partition"]) for d in dsteps)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
+    else:
+        ws = st.alloc_workspace(max_ctx, opt.partition)
+    out = st.new_out()
+    simt = opt.attn_impl == "simt" or wl.dtype == "f32"
+    groups = st.cascade_groups() if opt.cascade else None
+    if groups is not None:
+        ws = st.alloc_cascade_workspace(max_ctx, groups, opt.partition)
+
+    # Kernels one step launches: copy_blocks (if pairs), the scatter, the
+    # attention kernel, and -- for the CUDA-core kernel only -- a separate
+    # split-K merge (the tensor-core kernel merges inside its last partition).
+    def launches(si, d):
+        if groups is not None and groups["num_groups"]:
+            return (1 if len(si.pairs) else 0) + 2  # scatter, cascade kernel (prefix and suffix CTAs)
+        part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, opt.partition)
+        split = part > 0 and math.ceil(si.max_context_len / part) > 1
+        scatter = 0 if fused and not simt else 1
+        return (1 if len(si.pairs) else 0) + scatter + 1 + (1 if split and simt else 0)
+
+    def cache_writes(d):
+        if d["pairs"].shape[0]:
+            pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
+        if not fused:
+            pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
+
+    def attend(d):
+        if groups is not None:
+            st.attention_cascade(d, out, groups, ws, opt.partition, ordered=not opt.no_order)
+        elif fused:
+            pk.pk_paged_attention_decode_append(out, d["q"], d["k"], d["v"], d["slots"], st.k_cache, st.v_cache,
+                                                d["tables"], d["ctx_lens"], wl.scale, d["max_context_len"],
+                                                d["partition"], d["items"], ws)
+        else:
+            st.attention(d, out, ws, opt.partition, opt.attn_impl, ordered=not opt.no_order)
+
+    # warm-up (eager; also performs the library's one-time set-up)
+    for i in range(warmup):
+        flush()
+        cache_writes(dsteps[i % R])
+        attend(dsteps[i % R])
+    torch.cuda.synchronize()
+    kind, _ = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error during warm-up: {pk.DEVERR_NAMES.get(kind)}")
+
+    # Each window step as two CUDA graphs (cache writes; attention + merge), so
+    # the timed region holds GPU work only, as a decode loop would run it.
+    graphs = None
+    if not opt.no_graphs:
+        graphs = []
+        for d in dsteps:
+            g_w, g_a = None, torch.cuda.CUDAGraph()
+            if d["pairs"].shape[0] or not fused:  # nothing to capture when the scatter is fused
+                g_w = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g_w):
+                    cache_writes(d)
+            with torch.cuda.graph(g_a):
+                attend(d)
+            graphs.append((g_w, g_a))
+        torch.cuda.synchronize()
+
+    if sampler is not None:
+        sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    n_launch = 0
+    total_bytes = 0
+    total_unique = 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    clock0 = time.time()
+    for i in range(steps):
+        flush()
+        j = (warmup + i) % R
+        d = dsteps[j]
+        e0, e1, e2 = ev[i]
+        e0.record()
+        if graphs:
+            if graphs[j][0] is not None:
+                graphs[j][0].replay()
+        else:
+            cache_writes(d)
+        e1.record()
+        if graphs:
+            graphs[j][1].replay()
+        else:
+            attend(d)
+        e2.record()
+        n_launch += launches(host_steps[j], d)
+        total_bytes += step_bytes[j]
+        total_unique += step_unique[j]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop(clock0, time.time()) if sampler is not None else None
+    t_step = sum(a.elapsed_time(c) for a, _, c in ev) / 1e3
+    t_attn = sum(b.elapsed_time(c) for _, b, c in ev) / 1e3
+    kind, idx = pk.pk_get_device_error()
+    if kind:
+        raise RuntimeError(f"device error in the timed steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
+    part = st.resolve_partition(max(si.max_context_len for si in host_steps), opt.partition)
+    if planned:
+        parts = sorted({d["partition"] for d in dsteps})
+        part = parts[0] if len(parts) == 1 else parts
+    if groups is not None:
+        part = opt.partition if opt.partition >= 0 else "auto (cascade)"
+    del graphs
+    return {"t_step": t_step, "t_attn": t_attn, "bytes": total_bytes, "unique": total_unique,
+            "launches": n_launch, "wall": wall, "clocks": clocks, "window": R, "partition": part,
+            "fused": fused, "planned": planned, "simt": simt, "graphs": not opt.no_graphs,
+            "groups": None if groups is None else int(groups["num_groups"]),
+            "kernel": ("attn_cascade_kernel" if groups is not None else
+                       "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel")}
+
+
+def traffic_key(wl, cascade: bool, partition: int) -> str:
+    """Key of a workload's entry in the committed ncu traffic table."""
+    k = wl.name if wl.name != "prefix" else f"prefix{wl.block_size}"
+    if partition > 0:
+        k += f"_p{partition}"
+    return k + ("_cascade" if cascade else "")
+
+
+# The target configurations measured beside the headline workload on a
+# default single-GPU run: (workload, block size, partition, cascade).
+EXTRA_CONFIGS = [("gqa8b", None, -1, False), ("long", None, -1, False), ("long", None, 512, False),
+                 ("prefix", 8, -1, False), ("prefix", 8, -1, True), ("prefix", 16, -1, False),
+                 ("prefix", 16, -1, True), ("prefix", 32, -1, False), ("prefix", 32, -1, True)]
+
+
+def run_configs(args, dev, flush, peak: float, peak_kind: str) -> dict:
+    """The target configurations, each a short device-timed run of its own
+    (the headline's step, L2 flushing and events; no e2e, swap or CPU legs),
+    under one clock sampler."""
+    import torch
+    from paged_kv_cache_113_gb300.harness import DecodeState
+    from workloads import make_workload
+
+    sampler = None
+    if not args.no_clocks:
+        sampler = ClockSampler(torch.cuda.current_device(), gpu_uuid(dev))
+        sampler.start()
+    t0, c0 = time.perf_counter(), time.time()
+    rows = []
+    steps = max(1, min(args.steps, args.config_steps))
+    for name, B, part, cascade in EXTRA_CONFIGS:
+        wl = make_workload(name, block_size=B)
+        wl.enable_memo()
+        st = DecodeState(wl, dev, extra_tokens=args.window + 1)
+        opt = StepOptions(partition=part, cascade=cascade)
+        m = time_device_steps(st, wl, dev, opt, steps, args.warmup, args.window, 1, flush)
+        attn_gbs = m["bytes"] / m["t_attn"] / 1e9
+        ms = 1e3 * m["t_step"] / steps
+        rows.append({
+            "workload": name, "block_size": wl.block_size, "num_seqs": wl.num_seqs,
+            "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+            "partition": m["partition"], "partition_requested": "auto" if part == -1 else part,
+            "attention": f"cascade ({m['groups']} shared-prefix groups)" if cascade else "per sequence",
+            "steps": steps, "value": m["bytes"] / m["t_step"] / 1e9, "unit": "GB/s",
+            "ms_per_step": ms, "steps_per_s": 1e3 / ms, "attention_gbs": attn_gbs,
+            "attention_unique_gbs": m["unique"] / m["t_attn"] / 1e9,
+            "kv_bytes_per_step_mean": m["bytes"] / steps, "kv_unique_bytes_per_step_mean": m["unique"] / steps,
+            "gpu_launches": m["launches"],
+            "roofline": {"bound": "hbm", "kernel": m["kernel"], "achieved": attn_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": attn_gbs / peak, "peak_kind": f"{peak_kind} copy bandwidth",
+                         "frac_unique": m["unique"] / m["t_attn"] / 1e9 / peak,
+                         "traffic": ncu_traffic(traffic_key(wl, cascade, part)),
+                         "bytes_per_launch": m["bytes"] / steps, "ms_per_launch": 1e3 * m["t_attn"] / steps},
+        })
+        del st
+        torch.cuda.empty_cache()
+    clocks = sampler.stop(c0, time.time()) if sampler is not None else None
+    return {"note": "each configuration timed as the headline (planned work list, scatter fused in, CUDA "
+                    "graphs, L2 flushed between steps, CUDA events); 'cascade' rows run attn_cascade_kernel "
+                    "with a separate scatter; frac_unique counts each shared block once",
+            "wall_s": time.perf_counter() - t0, "clocks": clocks, "rows": rows}
+
+
+def gpu_uuid(dev):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return None
+
+
 def run_ours(args):
     import torch
     rank, world, local_rank = dist_env()
@@ -454,151 +711,13 @@ def run_ours(args):
     E = 0 if args.no_e2e else max(1, args.e2e_steps)
     Ew = 0 if args.no_e2e else 3
     st = DecodeState(wl, dev, extra_tokens=R + E + Ew + 1)
-    host_steps = [st.prepare_step() for _ in range(R)]
-    dsteps = [st.upload(si) for si in host_steps]
-    planned = not (args.cascade or args.grid or args.no_order)
-    # The default step: copy-on-write copies (if any), then one attention
-    # launch that also writes the step's new K/V (the scatter fused in).
-    fused = planned and not args.no_fuse and args.attn_impl == "auto"
-    if planned:
-        # The default schedule: each step's work list from the host planner
-        # (pk_attention_plan), longest item first.
-        for si, d in zip(host_steps, dsteps):
-            d["partition"], d["items"] = st.plan(si, args.partition)
-    step_bytes = [wl.kv_bytes(si.ctx_lens) for si in host_steps]
-    step_unique = [unique_kv_bytes(wl, si) for si in host_steps]
-    max_ctx = max(si.max_context_len for si in host_steps) + E + Ew + 1
-    if planned:
-        ws_bytes = max(st.workspace_bytes(max_ctx, d["partition"]) for d in dsteps)
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev) if ws_bytes else None
-    else:
-        ws = st.alloc_workspace(max_ctx, args.partition)
-    out = st.new_out()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
-
-    class _Flush:
-        """Evicts L2 between steps: writes 2x L2, then reads 2x L2 so that the
-        next step starts on a cold and clean L2 (no dirty lines to write back)."""
-
-        @staticmethod
-        def zero_():
-            flush_buf.zero_()
-            flush_buf.sum()
-
-    flush = _Flush()
-
-    # Kernels one step launches: copy_blocks (if pairs), the scatter, the
-    # attention kernel, and -- for the CUDA-core kernel only -- a separate
-    # split-K merge (the tensor-core kernel merges inside its last partition).
-    simt = args.attn_impl == "simt" or wl.dtype == "f32"
-
-    def launches(si, d):
-        if groups is not None and groups["num_groups"]:
-            return (1 if len(si.pairs) else 0) + 2  # scatter, cascade kernel (prefix and suffix CTAs)
-        part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, args.partition)
-        split = part > 0 and math.ceil(si.max_context_len / part) > 1
-        scatter = 0 if fused and not simt else 1
-        return (1 if len(si.pairs) else 0) + scatter + 1 + (1 if split and simt else 0)
-
-    def cache_writes(d):
-        if d["pairs"].shape[0]:
-            pk.pk_copy_blocks(st.k_cache, st.v_cache, d["pairs"])
-        if not fused:
-            pk.pk_reshape_and_cache(d["k"], d["v"], d["slots"], st.k_cache, st.v_cache)
-
-    groups = st.cascade_groups() if args.cascade else None
-    if groups is not None:
-        ws = st.alloc_cascade_workspace(max_ctx, groups, args.partition)
-
-    def attend(d):
-        if groups is not None:
-            st.attention_cascade(d, out, groups, ws, args.partition, ordered=not args.no_order)
-        elif fused:
-            pk.pk_paged_attention_decode_append(out, d["q"], d["k"], d["v"], d["slots"], st.k_cache, st.v_cache,
-                                                d["tables"], d["ctx_lens"], wl.scale, d["max_context_len"],
-                                                d["partition"], d["items"], ws)
-        else:
-            st.attention(d, out, ws, args.partition, args.attn_impl, ordered=not args.no_order)
-
-    # warm-up (eager; also performs the library's one-time set-up)
-    for i in range(args.warmup):
-        flush.zero_()
-        cache_writes(dsteps[i % R])
-        attend(dsteps[i % R])
-    torch.cuda.synchronize()
-    kind, _ = pk.pk_get_device_error()
-    if kind:
-        raise RuntimeError(f"device error during warm-up: {pk.DEVERR_NAMES.get(kind)}")
-
-    # Each window step as two CUDA graphs (cache writes; attention + merge), so
-    # the timed region holds GPU work only, as a decode loop would run it.
-    graphs = None
-    if not args.no_graphs:
-        graphs = []
-        for d in dsteps:
-            g_w, g_a = None, torch.cuda.CUDAGraph()
-            if d["pairs"].shape[0] or not fused:  # nothing to capture when the scatter is fused
-                g_w = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g_w):
-                    cache_writes(d)
-            with torch.cuda.graph(g_a):
-                attend(d)
-            graphs.append((g_w, g_a))
-        torch.cuda.synchronize()
-
-    sampler = None
-    if not args.no_clocks:
-        try:
-            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-        except Exception:
-            uuid = None
-        sampler = ClockSampler(local_rank, uuid)
-        sampler.start()
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    n_launch = 0
-    total_bytes = 0
-    total_unique = 0
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    clock0 = time.time()
-    for i in range(args.steps):
-        flush.zero_()
-        j = (args.warmup + i) % R
-        d = dsteps[j]
-        e0, e1, e2 = ev[i]
-        e0.record()
-        if graphs:
-            if graphs[j][0] is not None:
-                graphs[j][0].replay()
-        else:
-            cache_writes(d)
-        e1.record()
-        if graphs:
-            graphs[j][1].replay()
-        else:
-            attend(d)
-        e2.record()
-        n_launch += launches(host_steps[j], d)
-        total_bytes += step_bytes[j]
-        total_unique += step_unique[j]
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    wall = time.perf_counter() - wall0
-    clocks = sampler.stop(clock0, time.time()) if sampler else None
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    attn_ms = [b.elapsed_time(c) for _, b, c in ev]
-    t_step = sum(step_ms) / 1e3
-    t_attn = sum(attn_ms) / 1e3
-    kind, idx = pk.pk_get_device_error()
-    if kind:
-        raise RuntimeError(f"device error in the timed steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
-
-    t_step, t_attn = reduce_max([t_step, t_attn])
+    flush = L2Flush(dev)
+    sampler = None if args.no_clocks else ClockSampler(local_rank, gpu_uuid(dev))
+    opt = StepOptions.from_args(args)
+    m = time_device_steps(st, wl, dev, opt, args.steps, args.warmup, args.window, E + Ew + 1, flush,
+                          world=world, sampler=sampler)
+    total_bytes, total_unique = m["bytes"], m["unique"]
+    t_step, t_attn = reduce_max([m["t_step"], m["t_attn"]])
     value = job_throughput(world, total_bytes, t_step)
     attn_gbs = total_bytes / t_attn / 1e9
     peak, peak_kind = measured_hbm_peak()
@@ -613,19 +732,19 @@ def run_ours(args):
 
     prefix_cache = run_prefix_cache(st, wl) if wl.chat_choice is not None else None
     allocator_sim = None if args.no_allocator_sim else run_allocator_sim()
-    swap = None if args.no_swap or groups is not None else run_swap(st, wl, dev)
+    swap = None if args.no_swap or m["groups"] is not None else run_swap(st, wl, dev)
+
+    configs = None
+    if world == 1 and not args.no_configs and args.workload == "mha7b":
+        del st
+        torch.cuda.empty_cache()
+        configs = run_configs(args, dev, flush, peak, peak_kind)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ref = oracle_state(wl)
         cpu = cpu_baseline(wl, ref, args.cpu_seconds)
 
-    part = st.resolve_partition(max(si.max_context_len for si in host_steps), args.partition)
-    if planned:
-        parts = sorted({d["partition"] for d in dsteps})
-        part = parts[0] if len(parts) == 1 else parts
-    if groups is not None:
-        part = args.partition if args.partition >= 0 else "auto (cascade)"
     mean_ms = 1e3 * t_step / args.steps
     if rank == 0:
         line = {
@@ -636,32 +755,30 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": workload_config(wl, args, {
-                "partition": part, "attn_impl": args.attn_impl, "window_steps": R,
+                "partition": m["partition"], "attn_impl": args.attn_impl, "window_steps": m["window"],
                 "l2": "flushed between steps: 2x L2 written then 2x L2 read (cold, clean L2), outside the step events",
                 "kv_bytes_per_step_mean": total_bytes / args.steps,
                 "kv_unique_bytes_per_step_mean": total_unique / args.steps,
-                "launch": "CUDA graphs per step" if graphs else "eager",
-                "scatter": "fused into the attention launch" if fused else "own kernel",
+                "launch": "CUDA graphs per step" if m["graphs"] else "eager",
+                "scatter": "fused into the attention launch" if m["fused"] else "own kernel",
                 "seq_order": "index" if args.no_order else
-                             ("planned work list, longest item first (host)" if planned else "longest first (host)"),
-                "attention": (f"cascade: {groups['num_groups']} shared-prefix groups, prefix read once per group"
-                              if groups is not None else "per sequence")}),
-            "roofline": {"bound": "hbm",
-                         "kernel": ("attn_cascade_kernel" if groups is not None else
-                                    "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel"),
+                             ("planned work list, longest item first (host)" if m["planned"] else "longest first (host)"),
+                "attention": (f"cascade: {m['groups']} shared-prefix groups, prefix read once per group"
+                              if m["groups"] is not None else "per sequence")}),
+            "roofline": {"bound": "hbm", "kernel": m["kernel"],
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
-                         "traffic": ncu_traffic((wl.name if wl.name != "prefix" else f"prefix{wl.block_size}") +
-                                                ("_cascade" if groups is not None else "")),
+                         "traffic": ncu_traffic(traffic_key(wl, m["groups"] is not None, args.partition)),
                          "bytes_per_launch": total_bytes / args.steps, "ms_per_launch": 1e3 * t_attn / args.steps},
             "attention_gbs": attn_gbs,
             "attention_unique_gbs": total_unique / t_attn / 1e9,
             "read_stream_peak": (dict(read_peak, attention_frac=attn_gbs / read_peak["value"])
                                  if read_peak else None),
-            "gpu_launches": n_launch,
-            "wall_s_timed_region": wall,
-            "clocks": clocks,
+            "gpu_launches": m["launches"],
+            "wall_s_timed_region": m["wall"],
+            "clocks": m["clocks"],
             "e2e": e2e,
+            "configs": configs,
             "swap": swap,
             "prefix_cache": prefix_cache,
             "allocator_sim": allocator_sim,

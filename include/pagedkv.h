@@ -156,6 +156,8 @@ pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_hos
  *     out[s,h,:] = sum_t softmax(x)_t * V[table[s][t/B], t%B, kvh, :]
  *   out           [S, Hq, d], dtype of q (fp32 accumulation inside).
  *   q             [S, Hq, d].
+ *   block_size    B, the listing's block_size argument: must equal
+ *                 desc->block_size (PK_ERR_INVALID_ARG otherwise).
  *   block_tables  int32 [S, max_blocks_per_seq]; entries at or beyond
  *                 ceil(n / B) are never read.
  *   context_lens  int32 [S], each in [1, min(max_context_len, max_blocks*B)];
@@ -172,13 +174,15 @@ pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_hos
  * (PK_DEVERR_CONTEXT); a bad table entry is recorded (PK_DEVERR_BLOCK_ID). */
 pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,
                                     const void *v_cache, const int32_t *block_tables,
-                                    const int32_t *context_lens, float scale, int32_t num_seqs,
-                                    int32_t num_q_heads, int32_t max_blocks_per_seq,
-                                    int32_t max_context_len, int32_t partition_size,
-                                    void *workspace, size_t workspace_bytes,
-                                    const pk_cache_desc *desc, void *stream);
+                                    const int32_t *context_lens, float scale, int32_t block_size,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t max_blocks_per_seq, int32_t max_context_len,
+                                    int32_t partition_size, void *workspace,
+                                    size_t workspace_bytes, const pk_cache_desc *desc,
+                                    void *stream);
 
-/* As pk_paged_attention_decode, plus two scheduling controls:
+/* As pk_paged_attention_decode without the block_size argument (B is
+ * desc->block_size), plus two scheduling controls:
  *   seq_order  optional device int32 [S], a permutation of 0..S-1: the order in
  *              which sequences' work is launched (NULL = index order). Results
  *              do not depend on it; launching the longest sequences first
@@ -311,16 +315,21 @@ pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32
  *     that device (with the device current); make that first call before
  *     any stream capture.
  *   - All calls on a device share the one array, and it keeps the last
- *     call's contents (nothing in it needs to start at zero). Calls whose
- *     work overlaps on the GPU (e.g. on two streams) race on it. */
+ *     call's contents. Each call clears the part that must start at zero
+ *     (its merge tickets, with a cudaMemsetAsync on `stream`, which
+ *     allocates nothing) before its launch; the partials need no clearing.
+ *     Calls whose work overlaps on the GPU (e.g. on two streams) race on it.
+ *   - The array's address is kept per device ordinal for the life of the
+ *     process: it assumes the device's primary context is never reset
+ *     (cudaDeviceReset) while the library is loaded. */
 #define PK_STATIC_WORKSPACE_BYTES ((size_t)64 << 20)
 pk_status pk_paged_attention_decode_static(void *out, const void *q, const void *k_cache,
                                            const void *v_cache, const int32_t *block_tables,
                                            const int32_t *context_lens, float scale,
-                                           int32_t num_seqs, int32_t num_q_heads,
-                                           int32_t max_blocks_per_seq, int32_t max_context_len,
-                                           int32_t partition_size, const pk_cache_desc *desc,
-                                           void *stream);
+                                           int32_t block_size, int32_t num_seqs,
+                                           int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                           int32_t max_context_len, int32_t partition_size,
+                                           const pk_cache_desc *desc, void *stream);
 
 /* Cascade (shared-prefix) decode attention ("PagedAttention" S06, "In
  * production": the shared prefix batched separately from the divergent
@@ -375,7 +384,13 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
  * each, P = ceil(max_context_len / partition), then one 8-byte merge ticket
  * per (sequence, KV head). Tickets are tagged per call, so the workspace
  * needs no clearing; calls whose work overlaps on the GPU must not share a
- * workspace. Host only. */
+ * workspace. A ticket word counts as this call's only when its upper 32 bits
+ * equal the call's tag (a small per-call counter), so memory that held other
+ * data whose upper half happens to equal the tag (for a float left by an
+ * earlier call, a subnormal bit pattern) would be miscounted; a caller that
+ * reuses such memory can zero the ticket words (the last num_seqs x Hk x 8
+ * bytes of the size) first, as the allocation-free entry point does. Host
+ * only. */
 size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, int32_t partition_size,
                                          const pk_cache_desc *desc);

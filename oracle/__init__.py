@@ -311,6 +311,7 @@ def run_workload(wl, step: int = 0, attention: bool = True, select: Optional[np.
     and CoW pairs in op order, the step's ``slots`` and ``cow_pairs``, the
     padded ``tables`` and ``ctx_lens`` after the step, the pools (if
     ``pool``) and the attention output ``out`` (float64, if ``attention``).
+    :func:`continue_workload` runs further steps on the result.
     """
     from workloads import prefill_plan  # seeded inputs only
 
@@ -353,6 +354,23 @@ def run_workload(wl, step: int = 0, attention: bool = True, select: Optional[np.
                 else:
                     k, v = wl.prefill_kv(src[1], n)
                 reshape_and_cache(kc, vc, k, v, slots, wl.num_blocks, wl.block_size)
+    res = {"bm": bm, "prefill_slots": prefill_slots, "prefill_pairs": prefill_pairs, "k_cache": kc, "v_cache": vc}
+    return continue_workload(res, wl, step, attention=attention, select=select)
+
+
+def continue_workload(res: Dict[str, object], wl, step: int, attention: bool = True,
+                      select: Optional[np.ndarray] = None) -> Dict[str, object]:
+    """One more decode step on the state a replay left in ``res``.
+
+    In place: every sequence's length grows by one in index order (the
+    append routine), the step's copy-on-write pairs are copied, the step's
+    K/V (``wl.step_inputs(step)``) are scattered into their slots, and --
+    with ``attention`` -- the step's attention is computed. ``res`` gets the
+    step's ``slots``, ``cow_pairs``, padded ``tables``, ``ctx_lens``, inputs and
+    ``out``; calling it again with the next step index continues the decode.
+    """
+    bm, kc, vc = res["bm"], res["k_cache"], res["v_cache"]
+    pool = kc is not None
     q, kn, vn = wl.step_inputs(step)
     step_slots = np.empty(wl.num_seqs, dtype=np.int64)
     step_pairs = []
@@ -368,10 +386,9 @@ def run_workload(wl, step: int = 0, attention: bool = True, select: Optional[np.
     ctx = np.array([bm.seq_len(s) for s in range(wl.num_seqs)], dtype=np.int64)
     maxb = int(-(-int(ctx.max()) // wl.block_size))
     tables = bm.export_tables(range(wl.num_seqs), maxb)
-    res = {"bm": bm, "prefill_slots": prefill_slots, "prefill_pairs": prefill_pairs,
-           "slots": step_slots, "cow_pairs": np.array(step_pairs, dtype=np.int64).reshape(-1, 2),
-           "tables": tables, "ctx_lens": ctx, "q": q, "k_new": kn, "v_new": vn,
-           "k_cache": kc, "v_cache": vc}
+    res.update({"slots": step_slots, "cow_pairs": np.array(step_pairs, dtype=np.int64).reshape(-1, 2),
+                "tables": tables, "ctx_lens": ctx, "q": q, "k_new": kn, "v_new": vn})
+    res.pop("out", None)
     if attention and pool:
         res["out"] = paged_attention(q, kc, vc, tables, ctx, wl.scale, wl.dtype, select=select)
     return res

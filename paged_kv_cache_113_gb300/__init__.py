@@ -121,7 +121,7 @@ def lib() -> ctypes.CDLL:
         "pk_reshape_and_cache": (i32, [P, P, P, i32, P, P, D, P]),
         "pk_reshape_and_cache_append": (i32, [P, P, P, i32, P, P, D, P, i32, P, P]),
         "pk_copy_blocks": (i32, [P, P, P, i32, D, P]),
-        "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D, P]),
+        "pk_paged_attention_decode": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i32, P, sz, D, P]),
         "pk_paged_attention_decode_impl": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, P, sz, D,
                                                  P, i32, P]),
         "pk_longest_first_order": (i32, [P, i32, P]),
@@ -135,7 +135,7 @@ def lib() -> ctypes.CDLL:
         "pk_read_stream": (i32, [P, sz, P, P]),
         "pk_paged_attention_decode_advance": (i32, [P, P, P, P, P, P, P, P, P, P, f32, i32, i32, i32, i32, i32,
                                                      P, i32, P, sz, D, P]),
-        "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, D, P]),
+        "pk_paged_attention_decode_static": (i32, [P, P, P, P, P, P, f32, i32, i32, i32, i32, i32, i32, D, P]),
         "pk_paged_attention_resolve_partition": (i32, [i32, i32, i32, i32, D]),
         "pk_paged_attention_workspace_size": (sz, [i32, i32, i32, i32, D]),
         "pk_get_device_error": (i32, [P, P]),
@@ -443,8 +443,8 @@ def pk_paged_attention_decode_static(out, q, k_cache, v_cache, block_tables, con
     _check(lib().pk_paged_attention_decode_static(
         _dev(out, "out"), _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32),
-        float(scale), S, Hq, int(block_tables.shape[1]), int(max_context_len), int(partition_size),
-        ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_static")
+        float(scale), int(desc.block_size), S, Hq, int(block_tables.shape[1]), int(max_context_len),
+        int(partition_size), ctypes.byref(desc), _stream(stream)), "pk_paged_attention_decode_static")
 
 
 def pk_cascade_workspace_size(num_seqs, num_q_heads, max_context_len, num_groups, max_prefix_len,

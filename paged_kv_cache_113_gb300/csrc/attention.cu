@@ -1869,11 +1869,13 @@ pk_status pk_cascade_attention_decode(
 
 pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,
                                     const void *v_cache, const int32_t *block_tables,
-                                    const int32_t *context_lens, float scale, int32_t num_seqs,
-                                    int32_t num_q_heads, int32_t max_blocks_per_seq,
-                                    int32_t max_context_len, int32_t partition_size,
-                                    void *workspace, size_t workspace_bytes,
-                                    const pk_cache_desc *desc, void *stream) {
+                                    const int32_t *context_lens, float scale, int32_t block_size,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t max_blocks_per_seq, int32_t max_context_len,
+                                    int32_t partition_size, void *workspace,
+                                    size_t workspace_bytes, const pk_cache_desc *desc,
+                                    void *stream) {
+  if (!desc || block_size != desc->block_size) return PK_ERR_INVALID_ARG;
   return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
                                         scale, num_seqs, num_q_heads, max_blocks_per_seq,
                                         max_context_len, partition_size, workspace,
@@ -1910,7 +1912,8 @@ constexpr int kMaxStaticDevices = 64;
 
 // Device address of g_static_workspace on `device` (which must be current).
 // In host code the array's name is only a host-side stand-in, so the address
-// comes from cudaGetSymbolAddress, looked up once per device and kept.
+// comes from cudaGetSymbolAddress, looked up once per device and kept for the
+// life of the process (valid while the device's primary context is not reset).
 cudaError_t static_workspace_address(int device, void **out) {
   static std::mutex mu;
   static void *addr[kMaxStaticDevices] = {};
@@ -1930,9 +1933,10 @@ cudaError_t static_workspace_address(int device, void **out) {
 
 extern "C" pk_status pk_paged_attention_decode_static(
     void *out, const void *q, const void *k_cache, const void *v_cache,
-    const int32_t *block_tables, const int32_t *context_lens, float scale, int32_t num_seqs,
-    int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_context_len,
+    const int32_t *block_tables, const int32_t *context_lens, float scale, int32_t block_size,
+    int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks_per_seq, int32_t max_context_len,
     int32_t partition_size, const pk_cache_desc *desc, void *stream) {
+  if (!desc || block_size != desc->block_size) return PK_ERR_INVALID_ARG;
   pk_status st = check_common(desc, num_seqs, num_q_heads, max_context_len);
   if (st != PK_OK) return st;
   const int32_t part = pk_paged_attention_resolve_partition(num_seqs, num_q_heads,
@@ -1947,8 +1951,17 @@ extern "C" pk_status pk_paged_attention_decode_static(
     if (cudaGetDevice(&device) != cudaSuccess) return PK_ERR_CUDA;
     if (static_workspace_address(device, &ws) != cudaSuccess) return PK_ERR_CUDA;
   }
-  // Nothing in the scratch needs clearing: every partial the merge reads is
-  // written earlier in the same call.
+  // Every partial the merge reads is written earlier in the same call. The
+  // merge tickets (the last num_seqs x Hk words of the size) are cleared
+  // first: the array keeps whatever earlier calls left, and a leftover word
+  // whose upper half happened to equal this call's ticket tag would be
+  // counted as an arrival. Clearing them allocates nothing.
+  if (need > 0 && num_seqs > 0) {
+    const size_t tickets = size_t(num_seqs) * size_t(desc->num_kv_heads) * 8;
+    if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + (need - tickets), 0, tickets,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return PK_ERR_CUDA;
+  }
   return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
                                         scale, num_seqs, num_q_heads, max_blocks_per_seq,
                                         max_context_len, partition_size, ws,

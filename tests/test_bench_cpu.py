@@ -50,3 +50,14 @@ def test_oracle_timing_counts_the_gpu_arms_bytes():
         _, b1 = bench.time_oracle_rows(wl, ref, rows, 1)
         _, b4 = bench.time_oracle_rows(wl, ref, rows, 4)
         assert b1 == b4 == wl.kv_bytes(ref["ctx_lens"])
+
+
+def test_traffic_keys_of_the_target_configurations():
+    from workloads import make_workload
+    assert bench.traffic_key(make_workload("long"), False, -1) == "long"
+    assert bench.traffic_key(make_workload("long"), False, 512) == "long_p512"
+    assert bench.traffic_key(make_workload("prefix", block_size=16), True, -1) == "prefix16_cascade"
+    assert bench.traffic_key(make_workload("prefix", block_size=8), False, -1) == "prefix8"
+    names = {(w, b, p, c) for w, b, p, c in bench.EXTRA_CONFIGS}
+    assert ("gqa8b", None, -1, False) in names and ("long", None, 512, False) in names
+    assert {b for w, b, _, c in bench.EXTRA_CONFIGS if w == "prefix" and c} == {8, 16, 32}

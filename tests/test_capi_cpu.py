@@ -246,17 +246,20 @@ def test_host_checks_reject_before_launch(L):
     assert L.pk_copy_blocks(null, null, null, 0, ctypes.byref(_desc()), null) == 0
     assert L.pk_copy_blocks(null, null, null, -1, ctypes.byref(_desc()), null) == 1
     d = _desc()
-    args = [null] * 6 + [ctypes.c_float(0.1), 4, 8, 4, 64, -1, null, 0, ctypes.byref(d), null]
+    args = [null] * 6 + [ctypes.c_float(0.1), d.block_size, 4, 8, 4, 64, -1, null, 0, ctypes.byref(d), null]
     assert L.pk_paged_attention_decode(*args) == 1          # null pointers
     a2 = list(args)
-    a2[8] = 12                                              # 12 query heads over 8 KV heads
+    a2[9] = 12                                              # 12 query heads over 8 KV heads
     assert L.pk_paged_attention_decode(*a2) == 1
     a3 = list(args)
-    a3[7] = 0                                               # empty batch is a no-op
+    a3[8] = 0                                               # empty batch is a no-op
     assert L.pk_paged_attention_decode(*a3) == 0
+    a5 = list(a3)
+    a5[7] = d.block_size * 2                                # block_size disagrees with the pool's
+    assert L.pk_paged_attention_decode(*a5) == 1
     odd = _desc(d=96)
     a4 = list(args)
-    a4[14] = ctypes.byref(odd)
+    a4[15] = ctypes.byref(odd)
     assert L.pk_paged_attention_decode(*a4) == 2            # head_dim 96 not compiled
 
 
@@ -692,11 +695,12 @@ def test_other_entry_points_reject_bad_arguments_before_any_launch(L):
         assert append_call(**{k: None}) == pk.PK_ERR_INVALID_ARG
     assert append_call(vn=vn + 8) == pk.PK_ERR_INVALID_ARG
 
-    def static_call(S=4, Hq=32, max_ctx=100, part=0):
-        return L.pk_paged_attention_decode_static(out, q, kc, vc, tables, lens, f, S, Hq, 2048, max_ctx, part,
+    def static_call(S=4, Hq=32, max_ctx=100, part=0, B=16):
+        return L.pk_paged_attention_decode_static(out, q, kc, vc, tables, lens, f, B, S, Hq, 2048, max_ctx, part,
                                                   byref(d), None)
 
     assert static_call(Hq=12) == pk.PK_ERR_INVALID_ARG
+    assert static_call(B=32) == pk.PK_ERR_INVALID_ARG         # block_size disagrees with the pool's
     assert static_call(part=40) == pk.PK_ERR_INVALID_ARG
     # 64 x 64 heads x 2048 partitions of fp32 partials: far above the fixed scratch.
     assert static_call(S=64, Hq=64, max_ctx=32768, part=16) == pk.PK_ERR_WORKSPACE

@@ -9,7 +9,7 @@ import pytest
 import oracle
 import paged_kv_cache_113_gb300 as pk
 from paged_kv_cache_113_gb300.harness import DecodeState, from_device, to_device
-from parity_util import assert_close
+from parity_util import assert_close, oracle_every_row
 from workloads import make_workload
 
 torch = pytest.importorskip("torch")
@@ -199,40 +199,43 @@ def test_scatter_append_records_a_row_out_of_step():
     assert lens.tolist() == [5, 7] and tables.tolist() == [[3, -1], [5, -1]]
 
 
-@pytest.mark.parametrize("name", ["mha7b", "mixed"])
-def test_decode_step_full_size_against_the_oracle(name):
+@pytest.mark.slow
+@pytest.mark.parametrize("name,B", [("mha7b", None), ("gqa8b", None), ("long", None), ("mixed", None),
+                                    ("chat", None), ("prefix", 32)])
+def test_decode_step_full_size_against_the_oracle(name, B):
     """pk_decode_step as the benchmark's e2e leg runs it (full size, planned
-    work list, pinned host buffers): the first step against the oracle on
-    sampled rows, a second (resident) step against the step-by-step path."""
-    wl = make_workload(name)
+    work list, zero-copy from pinned host buffers, the next step prepared
+    while the current one runs): its first two steps -- the first uploads
+    the tables, the second runs on the device-resident tables in advance
+    mode -- against the oracle's two steps on every row, and the pools after
+    them bit for bit."""
+    wl = make_workload(name, block_size=B)
     wl.enable_memo()
     ref = oracle.run_workload(wl, attention=False)
-    rng = np.random.default_rng(3)
-    rows = np.array(sorted({(int(rng.integers(wl.num_seqs)), int(rng.integers(wl.num_q_heads)))
-                            for _ in range(48)} | {(int(np.argmax(wl.ctx_lens)), 0)}), np.int32)
-    want = oracle.paged_attention(ref["q"], ref["k_cache"], ref["v_cache"], ref["tables"], ref["ctx_lens"],
-                                  wl.scale, wl.dtype, select=rows)
     b = DecodeState(wl, "cuda", extra_tokens=4)
     stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
-                               b.k_cache, b.v_cache, max_context_len=int(wl.ctx_lens.max()) + 4)
-    q, k, v = wl.step_inputs(0)
-    stepper.q_host.copy_(_host(q, wl.dtype))
-    stepper.k_host.copy_(_host(k, wl.dtype))
-    stepper.v_host.copy_(_host(v, wl.dtype))
-    got = from_device(stepper.step())
-    assert pk.pk_get_device_error()[0] == 0
-    assert_close(np.stack([got[s, h] for s, h in rows]), np.stack([want[s, h] for s, h in rows]), wl.dtype,
-                 f"{name} pk_decode_step full size")
-    a = DecodeState(wl, "cuda", extra_tokens=4)
-    ref_path = _Stepwise(a)
-    ref_path.step(0)
-    q, k, v = wl.step_inputs(1)
-    stepper.q_host.copy_(_host(q, wl.dtype))
-    stepper.k_host.copy_(_host(k, wl.dtype))
-    stepper.v_host.copy_(_host(v, wl.dtype))
-    out_b = from_device(stepper.step())
-    assert stepper.buffers.tables_resident == 1
-    assert np.array_equal(from_device(ref_path.step(1)), out_b)
+                               b.k_cache, b.v_cache, max_context_len=int(wl.ctx_lens.max()) + 4, zero_copy=True)
+    stepper.prepare()
+    for step in range(2):
+        if step:
+            oracle.continue_workload(ref, wl, step, attention=False)
+        q, k, v = wl.step_inputs(step)
+        stepper.stream.synchronize()
+        stepper.q_host.copy_(_host(q, wl.dtype))
+        stepper.k_host.copy_(_host(k, wl.dtype))
+        stepper.v_host.copy_(_host(v, wl.dtype))
+        stepper.launch_prepared()
+        stepper.prepare()
+        stepper.stream.synchronize()
+        assert pk.pk_get_device_error()[0] == 0
+        if step:
+            assert stepper.buffers.tables_resident == 1
+        got = from_device(stepper.out_host)
+        assert_close(got, oracle_every_row(ref, wl), wl.dtype, f"{name} pk_decode_step step {step}")
+    torch.cuda.synchronize()
+    assert np.array_equal(from_device(b.k_cache), ref["k_cache"]), "K pool differs"
+    assert np.array_equal(from_device(b.v_cache), ref["v_cache"]), "V pool differs"
+    stepper.release()
 
 
 def test_graph_replay_follows_new_host_buffers():

@@ -9,8 +9,9 @@ oracle on the CPU -- and compares:
   max-abs 1e-2, rel-L2 2e-3; fp32: 1e-5 / 2e-6).
 
 Reduced cases (a few sequences of each workload, every row compared) run every
-kernel variant and partitioning; full-size cases run the benchmark's launch
-configuration and compare sampled rows the oracle computes one by one.
+kernel variant and partitioning; full-size cases run the benchmark's timed
+step exactly and compare every row too (the oracle's rows dealt to the host
+cores).
 """
 import numpy as np
 import pytest
@@ -18,7 +19,7 @@ import pytest
 import oracle
 import paged_kv_cache_113_gb300 as pk
 from paged_kv_cache_113_gb300.harness import DecodeState, from_device
-from parity_util import assert_close, as_f64, errors
+from parity_util import assert_close, as_f64, errors, oracle_every_row
 from workloads import Workload, make_workload
 
 torch = pytest.importorskip("torch")
@@ -106,34 +107,57 @@ def test_reduced_workload_all_variants(name, nseq, B):
     _check_all_variants(st, d, ref_out, wl, name)
 
 
-def _sample_rows(wl, ctx, n=48, seed=0):
-    rng = np.random.default_rng(seed)
-    S, Hq = wl.num_seqs, wl.num_q_heads
-    seqs = {int(np.argmax(ctx)), int(np.argmin(ctx)), 0, S - 1}
-    rows = {(s, int(rng.integers(Hq))) for s in seqs}
-    while len(rows) < min(n, S * Hq):
-        rows.add((int(rng.integers(S)), int(rng.integers(Hq))))
-    return np.array(sorted(rows), dtype=np.int32)
-
-
-FULL = [("mha7b", None), ("gqa8b", None), ("long", None), ("prefix", 8), ("prefix", 16), ("prefix", 32),
-        ("chat", None), ("mixed", None)]
+# Full-size workloads: the benchmark's configurations, every row compared.
+FULL = [("mha7b", None, -1), ("gqa8b", None, -1), ("long", None, -1), ("long", None, 512), ("prefix", 8, -1),
+        ("prefix", 16, -1), ("prefix", 32, -1), ("chat", None, -1), ("mixed", None, -1)]
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,B", FULL)
-def test_full_size_sampled(name, B):
-    """Full-size workload in the benchmark's launch configuration (auto)."""
+@pytest.mark.parametrize("name,B,part", FULL)
+def test_full_size_every_row(name, B, part):
+    """A full-size workload through the benchmark's timed step exactly: the
+    step's copy-on-write copies, then the planned work list (pk_attention_plan)
+    with the step's scatter fused into the attention launch
+    (pk_paged_attention_decode_append). Slots, pairs, tables and both whole
+    pools bit for bit against the oracle; every (sequence, query head) row of
+    the output within tolerance. Then, on the same state, the (sequence,
+    partition) grid at the plan's partition gives the same bits, and the
+    grid's own automatic partitioning is again compared row by row.
+    ``part`` -1 is the planner's choice; 512 is the 512-token split the
+    long-context configuration names."""
     wl = make_workload(name, block_size=B)
-    sel = _sample_rows(wl, wl.ctx_lens)
-    st, d, out, ref = _build_pair(wl, select=sel)
+    wl.enable_memo()
+    ref = oracle.run_workload(wl, attention=False)
+    want = oracle_every_row(ref, wl)
+    st = DecodeState(wl, "cuda", extra_tokens=64)
+    si = st.prepare_step(0)
+    assert np.array_equal(si.slots, ref["slots"]), "step slot mapping differs"
+    assert np.array_equal(np.asarray(si.pairs).reshape(-1, 2), ref["cow_pairs"]), "CoW pairs differ"
+    nb = ref["tables"].shape[1]
+    assert np.array_equal(si.tables[:, :nb], ref["tables"]) and (si.tables[:, nb:] == -1).all()
+    assert np.array_equal(si.ctx_lens, ref["ctx_lens"].astype(np.int32))
+    if name == "prefix" and B == 32:
+        assert len(ref["cow_pairs"]) == 96      # the step's copy-on-write copies run too
+    d = st.upload(si)
+    d["partition"], d["items"] = st.plan(si, part)
+    ws = st.alloc_workspace(d["max_context_len"], d["partition"])
+    out = st.new_out()
+    st.run_step_fused(d, out, ws)
+    torch.cuda.synchronize()
+    _no_device_error()
+    assert np.array_equal(from_device(st.k_cache), ref["k_cache"]), "K pool differs"
+    assert np.array_equal(from_device(st.v_cache), ref["v_cache"]), "V pool differs"
     got = from_device(out)
-    rows_got = np.stack([got[s, h] for s, h in sel])
-    rows_ref = np.stack([ref["out"][s, h] for s, h in sel])
-    assert_close(rows_got, rows_ref, wl.dtype, f"{name} full (auto)")
-    # Every row: finite and each output a convex combination of its values.
-    g = as_f64(got, wl.dtype)
-    assert np.isfinite(g).all()
+    assert_close(got, want, wl.dtype, f"{name} B={wl.block_size} planned+fused (partition {d['partition']})")
+    grid = {k: v for k, v in d.items() if k not in ("items", "partition")}
+    same = st.new_out()
+    st.attention(grid, same, ws, d["partition"])
+    auto = st.new_out()
+    st.attention(grid, auto, st.alloc_workspace(d["max_context_len"], -1), -1)
+    torch.cuda.synchronize()
+    _no_device_error()
+    assert np.array_equal(from_device(same), got), "grid launch at the plan's partition differs"
+    assert_close(from_device(auto), want, wl.dtype, f"{name} B={wl.block_size} grid (auto)")
 
 
 def _custom(name, S, Hq, Hk, d, B, lens, N=None, seed=5, dtype="bf16"):
@@ -399,29 +423,6 @@ def test_bad_work_item_is_recorded():
     st.attention(dict(d, items=items), st.new_out(), None, 0, "mma")
     kind, idx = pk.pk_get_device_error()
     assert pk.DEVERR_NAMES[kind] == "order" and idx == 3
-
-
-@pytest.mark.parametrize("name", ["mixed", "long", "gqa8b"])
-def test_planned_work_list_full_size(name):
-    """The host plan (pk_attention_plan) at full size, as the benchmark runs it:
-    sampled rows against the oracle, every row bit for bit against the grid
-    launch at the plan's partition."""
-    wl = make_workload(name)
-    sel = _sample_rows(wl, wl.ctx_lens)
-    st, d, _, ref = _build_pair(wl, select=sel, compare_pool=False)
-    lens = from_device(d["ctx_lens"])
-    part, items = pk.pk_attention_plan(lens, wl.num_q_heads, st.desc, -1)
-    ws = st.alloc_workspace(d["max_context_len"], part)
-    a, b = st.new_out(), st.new_out()
-    st.attention(dict(d, items=torch.from_numpy(items).cuda(), partition=part), a, ws)
-    st.attention(d, b, ws, part)
-    torch.cuda.synchronize()
-    _no_device_error()
-    got = from_device(a)
-    assert np.array_equal(got, from_device(b))
-    rows_got = np.stack([got[s, h] for s, h in sel])
-    rows_ref = np.stack([ref["out"][s, h] for s, h in sel])
-    assert_close(rows_got, rows_ref, wl.dtype, f"{name} planned (partition {part})")
 
 
 FUSED_CASES = [("gqa8b", 40, None, -1), ("gqa8b", 40, None, 256), ("long", 2, None, -1), ("mixed", 40, None, -1),

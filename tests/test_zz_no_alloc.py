@@ -7,21 +7,25 @@ cannot pay for cudaMalloc/cudaFree and their implicit synchronisation. This
 entry point keeps its split-K scratch in a static device array that the
 library holds on every GPU that loads it.
 
-The test calls it through the C ABI twice in a row, on two different
-workloads that both split (the second call finds the first call's data in
-the shared array), and checks each output against pk_paged_attention_decode
-run with a caller-allocated workspace, within the bf16 tolerance the parity
-tests use. It also checks that a request larger than the static array is
-refused before any launch. This file is collected last.
+The test calls it through the C ABI three times in a row, on workloads that
+all split, and shapes the calls so that leftovers matter: the first call
+fills the most scratch, the second call's merge tickets then sit on the
+first call's partial outputs, and the third (another shape) lands on both.
+Each output must equal, bit for bit, pk_paged_attention_decode run with a
+caller-allocated workspace (the same kernel, partitioning and merge order)
+and match the oracle within the bf16 tolerance the parity tests use. It
+also checks that a request larger than the static array is refused before
+any launch. This file is collected last.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import paged_kv_cache_113_gb300 as pk
 from paged_kv_cache_113_gb300.harness import DecodeState, from_device
-from parity_util import TOL, as_f64, errors
+from parity_util import assert_close
 from workloads import make_workload
 
 torch = pytest.importorskip("torch")
@@ -33,12 +37,12 @@ def _p(t):
 
 
 def _call_static(st, d, out, partition):
-    """The new entry point, called through the C ABI."""
+    """The allocation-free entry point, called through the C ABI."""
     L = pk.lib()
     return L.pk_paged_attention_decode_static(
         _p(out), _p(d["q"]), _p(st.k_cache), _p(st.v_cache), _p(d["tables"]), _p(d["ctx_lens"]),
-        ctypes.c_float(st.wl.scale), st.wl.num_seqs, st.wl.num_q_heads, int(d["tables"].shape[1]),
-        d["max_context_len"], partition, ctypes.byref(st.desc),
+        ctypes.c_float(st.wl.scale), st.wl.block_size, st.wl.num_seqs, st.wl.num_q_heads,
+        int(d["tables"].shape[1]), d["max_context_len"], partition, ctypes.byref(st.desc),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
@@ -49,24 +53,39 @@ def _built():
     pk.build()
 
 
-def test_static_scratch_matches_caller_workspace_twice():
-    cases = [(make_workload("long", num_seqs=1), 512), (make_workload("gqa8b", num_seqs=24), 128)]
-    for wl, part in cases:
+def _ticket_offset(st, d, part):
+    """Where a call's merge tickets start in the scratch (after its partials)."""
+    need = st.workspace_bytes(d["max_context_len"], part)
+    return need - st.wl.num_seqs * st.wl.num_kv_heads * 8
+
+
+def test_static_scratch_matches_caller_workspace_three_calls():
+    # (workload, sequences, partition): the first call writes the most
+    # partials; the second's tickets fall inside them; the third differs in
+    # shape again.
+    cases = [("gqa8b", 24, 128), ("long", 1, 512), ("mixed", 6, 256)]
+    written = 0
+    for name, nseq, part in cases:
+        wl = make_workload(name, num_seqs=nseq)
+        wl.enable_memo()
+        ref = oracle.run_workload(wl)
         st = DecodeState(wl, "cuda")
         d = st.upload(st.prepare_step(0))
         need = st.workspace_bytes(d["max_context_len"], part)
         assert 0 < need <= pk.PK_STATIC_WORKSPACE_BYTES      # it splits, and fits the array
+        if written:
+            # This call's tickets lie on scratch an earlier call wrote.
+            assert _ticket_offset(st, d, part) < written
+        written = max(written, need)
         want = st.new_out()
         st.run_step(d, want, st.alloc_workspace(d["max_context_len"], part), part)
         got = torch.full_like(want, float("nan"))
         assert _call_static(st, d, got, part) == 0
         torch.cuda.synchronize()
         assert pk.pk_get_device_error()[0] == 0
-        g, w = as_f64(from_device(got), "bf16"), as_f64(from_device(want), "bf16")
-        assert np.isfinite(g).all()
-        mx, rl = errors(g, w)
-        tmax, trel = TOL["bf16"]
-        assert mx <= tmax and rl <= trel, (wl.name, mx, rl)
+        g = from_device(got)
+        assert np.array_equal(g, from_device(want)), f"{name}: static scratch differs from a caller workspace"
+        assert_close(g, ref["out"], wl.dtype, f"{name} static scratch, partition {part}")
         del st
         torch.cuda.empty_cache()
 
@@ -81,7 +100,7 @@ def test_static_scratch_refuses_oversized_requests():
     L = pk.lib()
     rc = L.pk_paged_attention_decode_static(
         _p(out), _p(d["q"]), _p(st.k_cache), _p(st.v_cache), _p(d["tables"]), _p(d["ctx_lens"]),
-        ctypes.c_float(wl.scale), 64, 32, int(d["tables"].shape[1]), 65536, 16, ctypes.byref(st.desc),
-        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        ctypes.c_float(wl.scale), wl.block_size, 64, 32, int(d["tables"].shape[1]), 65536, 16,
+        ctypes.byref(st.desc), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == pk.PK_ERR_WORKSPACE
     assert pk.pk_get_device_error()[0] == 0
