@@ -225,11 +225,11 @@ def test_decode_step_full_size_against_the_oracle(name, B):
         stepper.k_host.copy_(_host(k, wl.dtype))
         stepper.v_host.copy_(_host(v, wl.dtype))
         stepper.launch_prepared()
+        # Step 1 is prepared after step 0's launch: on resident tables.
+        assert stepper.buffers.tables_resident == 1
         stepper.prepare()
         stepper.stream.synchronize()
         assert pk.pk_get_device_error()[0] == 0
-        if step:
-            assert stepper.buffers.tables_resident == 1
         got = from_device(stepper.out_host)
         assert_close(got, oracle_every_row(ref, wl), wl.dtype, f"{name} pk_decode_step step {step}")
     torch.cuda.synchronize()

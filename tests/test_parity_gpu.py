@@ -136,8 +136,9 @@ def test_full_size_every_row(name, B, part):
     nb = ref["tables"].shape[1]
     assert np.array_equal(si.tables[:, :nb], ref["tables"]) and (si.tables[:, nb:] == -1).all()
     assert np.array_equal(si.ctx_lens, ref["ctx_lens"].astype(np.int32))
+    assert [tuple(p) for p in st.prefill_pairs] == [tuple(p) for p in ref["prefill_pairs"]]
     if name == "prefix" and B == 32:
-        assert len(ref["cow_pairs"]) == 96      # the step's copy-on-write copies run too
+        assert len(ref["prefill_pairs"]) == 96  # the first divergent tokens copied the shared tail blocks
     d = st.upload(si)
     d["partition"], d["items"] = st.plan(si, part)
     ws = st.alloc_workspace(d["max_context_len"], d["partition"])
