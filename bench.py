@@ -507,16 +507,16 @@ def time_device_steps(st, wl, dev, opt: StepOptions, steps: int, warmup: int, wi
     if groups is not None:
         ws = st.alloc_cascade_workspace(max_ctx, groups, opt.partition)
 
-    # Kernels one step launches: copy_blocks (if pairs), the scatter, the
-    # attention kernel, and -- for the CUDA-core kernel only -- a separate
-    # split-K merge (the tensor-core kernel merges inside its last partition).
+    # Kernels one step launches: copy_blocks (if pairs), the scatter (unless
+    # fused into the attention), the attention kernel, and the split-K merge
+    # when the step splits (the cascade kernel's parts always merge).
     def launches(si, d):
         if groups is not None and groups["num_groups"]:
-            return (1 if len(si.pairs) else 0) + 2  # scatter, cascade kernel (prefix and suffix CTAs)
+            return (1 if len(si.pairs) else 0) + 3  # scatter, cascade kernel (prefix and suffix CTAs), merge
         part = d["partition"] if "partition" in d else st.resolve_partition(si.max_context_len, opt.partition)
         split = part > 0 and math.ceil(si.max_context_len / part) > 1
         scatter = 0 if fused and not simt else 1
-        return (1 if len(si.pairs) else 0) + scatter + 1 + (1 if split and simt else 0)
+        return (1 if len(si.pairs) else 0) + scatter + 1 + (1 if split else 0)
 
     def cache_writes(d):
         if d["pairs"].shape[0]:
@@ -612,8 +612,9 @@ def time_device_steps(st, wl, dev, opt: StepOptions, steps: int, warmup: int, wi
             "launches": n_launch, "wall": wall, "clocks": clocks, "window": R, "partition": part,
             "fused": fused, "planned": planned, "simt": simt, "graphs": not opt.no_graphs,
             "groups": None if groups is None else int(groups["num_groups"]),
-            "kernel": ("attn_cascade_kernel" if groups is not None else
-                       "attn_mma_kernel" if not simt else "attn_simt_kernel + attn_merge_kernel")}
+            "kernel": ("attn_cascade_kernel + attn_lse_merge_kernel" if groups is not None else
+                       "attn_mma_kernel (+ attn_lse_merge_kernel when split)" if not simt
+                       else "attn_simt_kernel (+ attn_merge_kernel when split)")}
 
 
 def traffic_key(wl, cascade: bool, partition: int) -> str:

@@ -166,7 +166,11 @@ pk_status pk_swap_blocks(void *k_cache, void *v_cache, void *k_host, void *v_hos
  *   partition_size   0: one partition per sequence (no split-K);
  *                    -1: automatic; > 0: split each context into partitions
  *                    of this many tokens (a multiple of B), merged with a
- *                    log-sum-exp reduction.
+ *                    log-sum-exp reduction. With the tensor-core kernel the
+ *                    merge is a second launch on `stream`, enqueued as the
+ *                    attention launch's programmatic dependent (it starts
+ *                    while the attention drains and waits for it to finish
+ *                    before reading); it runs only when the call splits.
  *   workspace        device scratch of at least
  *                    pk_paged_attention_workspace_size(...) bytes when the
  *                    chosen partitioning splits; may be NULL otherwise.
@@ -315,10 +319,9 @@ pk_status pk_attention_plan(const int32_t *context_lens, int32_t num_seqs, int32
  *     that device (with the device current); make that first call before
  *     any stream capture.
  *   - All calls on a device share the one array, and it keeps the last
- *     call's contents. Each call clears the part that must start at zero
- *     (its merge tickets, with a cudaMemsetAsync on `stream`, which
- *     allocates nothing) before its launch; the partials need no clearing.
- *     Calls whose work overlaps on the GPU (e.g. on two streams) race on it.
+ *     call's contents; nothing in it needs to start at zero (every partial
+ *     the merge reads is written earlier in the same call). Calls whose work
+ *     overlaps on the GPU (e.g. on two streams) race on it.
  *   - The array's address is kept per device ordinal for the life of the
  *     process: it assumes the device's primary context is never reset
  *     (cudaDeviceReset) while the library is loaded. */
@@ -366,8 +369,8 @@ pk_status pk_cascade_attention_decode(
 
 /* Workspace bytes of pk_cascade_attention_decode: fp32 partials
  * [S, Hq, Ppre + Psuf, d + 2] (Ppre = ceil(max_prefix_len / partition),
- * Psuf = ceil(max_context_len / partition)) and one 8-byte merge ticket per
- * (sequence, KV head); 0 on invalid arguments. Host only. */
+ * Psuf = ceil(max_context_len / partition)); 0 on invalid arguments. Host
+ * only. */
 size_t pk_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t max_context_len,
                                  int32_t num_groups, int32_t max_prefix_len,
                                  int32_t partition_size, const pk_cache_desc *desc);
@@ -381,15 +384,9 @@ int32_t pk_paged_attention_resolve_partition(int32_t num_seqs, int32_t num_q_hea
 /* Bytes of split-K workspace pk_paged_attention_decode needs for these
  * arguments (0 when the resolved partitioning does not split). Layout inside:
  * fp32 partial outputs [S, Hq, P, d], then running maxima and sums [S, Hq, P]
- * each, P = ceil(max_context_len / partition), then one 8-byte merge ticket
- * per (sequence, KV head). Tickets are tagged per call, so the workspace
- * needs no clearing; calls whose work overlaps on the GPU must not share a
- * workspace. A ticket word counts as this call's only when its upper 32 bits
- * equal the call's tag (a small per-call counter), so memory that held other
- * data whose upper half happens to equal the tag (for a float left by an
- * earlier call, a subnormal bit pattern) would be miscounted; a caller that
- * reuses such memory can zero the ticket words (the last num_seqs x Hk x 8
- * bytes of the size) first, as the allocation-free entry point does. Host
+ * each, P = ceil(max_context_len / partition). Every partial the merge reads
+ * is written earlier in the same call, so the workspace needs no clearing;
+ * calls whose work overlaps on the GPU must not share a workspace. Host
  * only. */
 size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                          int32_t max_context_len, int32_t partition_size,

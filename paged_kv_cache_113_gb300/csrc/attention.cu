@@ -22,8 +22,8 @@
 //                      O^T += V^T P^T on the tensor cores (mma.sync m16n8k16,
 //                      tokens as M, the group's heads as N), with an online
 //                      softmax in registers; the softmax weights enter PV as a
-//                      bf16 hi + lo pair. Split partitions write partials and
-//                      the last one to finish merges them (log-sum-exp).
+//                      bf16 hi + lo pair. Split partitions write partials,
+//                      merged by attn_lse_merge_kernel.
 //                      With the step's new K/V it also writes them (the CTA
 //                      holding the token, for its head: the scatter fused in);
 //                      in advance mode it also advances device-resident block
@@ -33,9 +33,12 @@
 //                      (one per KV head, group and prefix partition) stream a
 //                      shared prefix once for all of the group's query
 //                      columns; suffix CTAs are attn_mma_kernel's in cascade
-//                      mode.
+//                      mode. Every part writes a partial.
 //   attn_simt_kernel   fp32 or bf16 on CUDA cores: one warp per token,
 //                      shuffle-reduced dot products, online softmax.
+//   attn_lse_merge_kernel  log-sum-exp merge of the tensor-core kernels'
+//                      split rows: launched right after them as their
+//                      programmatic dependent, one warp per row.
 //   attn_merge_kernel  log-sum-exp merge of the CUDA-core kernel's partials.
 //   wait_timeout_probe_kernel  the bounded pipeline wait on a phase nothing
 //                      completes (pk_selftest_wait_timeout).
@@ -52,7 +55,6 @@
 #include <stdint.h>
 
 #include <algorithm>
-#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -88,8 +90,6 @@ struct AttnParams {
   float *ws_m;               // [S, Hq, P] running maxima (log2 domain)
   float *ws_l;               // [S, Hq, P] softmax denominators
   const int32_t *order;      // [S] launch order of the sequences, or null
-  unsigned long long *merge_tickets;  // [S, Hk] arrival tickets of the fused merge, or null
-  uint32_t epoch;            // this call's tag on the tickets
   // Cascade (shared-prefix) attention: the first seq_prefix[s] tokens of
   // sequence s are attended by its group's prefix work; partials of prefix
   // partitions use workspace slots [0, prefix_slots), the rest follow.
@@ -176,22 +176,6 @@ __device__ __forceinline__ bool work_of(const AttnParams &p, const CtaCoord &c, 
   part = c.nz - 1 - c.z;
   s = launch_seq(p, c);
   return true;
-}
-
-// Fused-merge ticket of one (sequence, KV head): returns how many of this
-// call's partitions have arrived, counting the caller. A ticket holds
-// (epoch << 32 | arrivals); a ticket from another call (stale memory, or 0
-// after the previous merge reset it) starts over, so the workspace needs no
-// clearing and a replayed graph finds its tickets reset.
-__device__ __forceinline__ int take_merge_ticket(unsigned long long *t, uint32_t epoch) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(t);
-  for (;;) {
-    const unsigned long long mine = static_cast<unsigned long long>(epoch) << 32;
-    const unsigned long long next = (old >> 32) == epoch ? old + 1 : (mine | 1ull);
-    const unsigned long long seen = atomicCAS(t, old, next);
-    if (seen == old) return int(next & 0xFFFFFFFFull);
-    old = seen;
-  }
 }
 
 // Log-sum-exp merge of the partials of query heads h0 .. h0+nh-1 of
@@ -750,29 +734,13 @@ __device__ __forceinline__ void mma_cta(const AttnParams &p, const CUtensorMap *
       }
     }
   }
-  if (npre + nsuf > 1 && p.merge_tickets) {
-    // Fused merge: the last part to finish for (s, kvh) merges them all.
-    __threadfence();  // this thread's partials are visible device-wide
-    pk::named_barrier(1, NW * 32);
-    volatile int *flag = reinterpret_cast<volatile int *>(sm_l + NW * kMaxGroup);
-    if (threadIdx.x == 0)
-      *flag = take_merge_ticket(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, p.epoch) ==
-              npre + nsuf;
-    pk::named_barrier(1, NW * 32);
-    if (*flag) {
-      __threadfence();
-      merge_partials<__nv_bfloat16, D>(p, s, kvh * G, G, npre, p.prefix_slots, nsuf, threadIdx.x,
-                                       NW * 32);
-      pk::named_barrier(1, NW * 32);
-      if (threadIdx.x == 0) atomicExch(p.merge_tickets + size_t(s) * p.num_kv_heads + kvh, 0ull);
-    }
-  }
 }
 
 template <int D, int BS, int NW, int STAGES>
 __global__ void __launch_bounds__((NW + 1) * 32)
     attn_mma_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap) {
+  pk::launch_dependents();  // the split-K merge may be scheduled as this grid drains
   mma_cta<D, BS, NW, STAGES>(p, &kmap, &vmap, hw_cta());
 }
 
@@ -785,7 +753,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 // member of the group: up to 16 query columns (members x G heads), two MMA
 // n-tiles. Each column's partial goes to its sequence's prefix slot; the
 // members' suffix work (attn_mma_kernel in cascade mode) fills the other
-// slots, and the last part to finish merges ("PagedAttention" S06, "In
+// slots, and attn_lse_merge_kernel merges them ("PagedAttention" S06, "In
 // production": the shared prefix batched separately from the divergent
 // suffixes).
 // ---------------------------------------------------------------------------
@@ -1021,7 +989,6 @@ __device__ __forceinline__ void prefix_cta(const AttnParams &p, const CUtensorMa
   float *sm_o = reinterpret_cast<float *>(smem_raw + (stages - raw));
   float *sm_m = sm_o + NW * NC * MSTRIDE;
   float *sm_l = sm_m + NW * NC;
-  int *sm_last = reinterpret_cast<int *>(sm_l + NW * NC);
 #pragma unroll
   for (int mt = 0; mt < S::KSTEPS; ++mt)
 #pragma unroll
@@ -1064,32 +1031,6 @@ __device__ __forceinline__ void prefix_cta(const AttnParams &p, const CUtensorMa
       p.ws_l[r] = L;
     }
   }
-  // Each member's part count: its prefix partitions plus its own suffix's.
-  __threadfence();
-  pk::named_barrier(1, NW * 32);
-  if (threadIdx.x < nm) {
-    const int mem = __ldg(p.group_members + g0 + threadIdx.x);
-    const int ctx = context_len(p, mem, false);
-    const int mpre = min(max(__ldg(p.seq_prefix + mem), 0), ctx);
-    const int nparts = (mpre + p.partition - 1) / p.partition +
-                       (ctx - mpre + p.partition - 1) / p.partition;
-    sm_last[threadIdx.x] =
-        take_merge_ticket(p.merge_tickets + size_t(mem) * p.num_kv_heads + kvh, p.epoch) == nparts;
-  }
-  pk::named_barrier(1, NW * 32);
-  for (int j = 0; j < nm; ++j) {
-    if (!sm_last[j]) continue;
-    __threadfence();
-    const int mem = __ldg(p.group_members + g0 + j);
-    const int ctx = context_len(p, mem, false);
-    const int mpre = min(max(__ldg(p.seq_prefix + mem), 0), ctx);
-    const int mnpre = (mpre + p.partition - 1) / p.partition;
-    const int mnsuf = (ctx - mpre + p.partition - 1) / p.partition;
-    merge_partials<__nv_bfloat16, D>(p, mem, kvh * G, G, mnpre, p.prefix_slots, mnsuf, threadIdx.x,
-                                     NW * 32);
-    pk::named_barrier(1, NW * 32);
-    if (threadIdx.x == 0) atomicExch(p.merge_tickets + size_t(mem) * p.num_kv_heads + kvh, 0ull);
-  }
 }
 
 // Cascade attention in one launch: CTAs [0, npre) are prefix CTAs (KV head
@@ -1104,6 +1045,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3)
     attn_cascade_kernel(AttnParams p, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, int num_groups, int npre,
                         int suffix_parts) {
+  pk::launch_dependents();  // the merge may be scheduled as this grid drains
   const int b = int(blockIdx.x);
   const int Hk = p.num_kv_heads;
   if (b < npre) {
@@ -1150,6 +1092,78 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
   }
   if (np == 1) return;  // written directly by the attention kernel
   merge_partials<T, D>(p, s, h, 1, np, 0, 0, threadIdx.x, blockDim.x);
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of the tensor-core kernels' split rows.
+//
+// The per-sequence and cascade attention launches write one partial per part
+// of a split row and nothing else for it. This kernel runs right after them on
+// the same stream, launched as their programmatic dependent: it may be
+// scheduled while the attention drains and waits for it to complete before
+// reading. One warp per (sequence, query head) row, eight rows per CTA; a row
+// with a single part was written by the attention launch and is skipped.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p) {
+  pk::wait_prerequisites();
+  const int lane = int(threadIdx.x & 31);
+  const int row = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
+  if (row >= p.num_seqs * p.num_q_heads) return;
+  const int s = row / p.num_q_heads;
+  const int ctx = context_len(p, s, false);
+  const int pre = p.seq_prefix ? min(max(__ldg(p.seq_prefix + s), 0), ctx) : 0;
+  const int npre = (pre + p.partition - 1) / p.partition;
+  const int np = npre + (ctx - pre + p.partition - 1) / p.partition;
+  if (np <= 1) return;
+  // Part q's workspace slot: the prefix parts first, then the rest.
+  const size_t base = size_t(row) * p.num_partitions;
+  auto slot = [&](int q) { return base + (q < npre ? q : p.prefix_slots + (q - npre)); };
+  // M = max_q m_q: the lanes share the parts, then a warp reduction.
+  float M = -INFINITY;
+  for (int q = lane; q < np; q += 32) M = fmaxf(M, __ldcg(p.ws_m + slot(q)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // L = sum_q l_q 2^(m_q - M), out = sum_q acc_q 2^(m_q - M) / L, in part
+  // order; each lane owns four columns and loads eight parts at a time.
+  constexpr int COLS = D / 4;  // lanes with columns
+  const bool cols = lane < COLS;
+  float L = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  constexpr int U = 8;
+  for (int q0 = 0; q0 < np; q0 += U) {
+    float mq[U], lq[U];
+    float4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = q0 + u;
+      if (q < np) {
+        const size_t sl = slot(q);
+        mq[u] = __ldcg(p.ws_m + sl);
+        lq[u] = __ldcg(p.ws_l + sl);
+        x[u] = cols ? __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + sl * D) + lane)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (q0 + u < np) {
+        const float w = exp2f(mq[u] - M);
+        L = fmaf(lq[u], w, L);
+        acc.x = fmaf(x[u].x, w, acc.x);
+        acc.y = fmaf(x[u].y, w, acc.y);
+        acc.z = fmaf(x[u].z, w, acc.z);
+        acc.w = fmaf(x[u].w, w, acc.w);
+      }
+    }
+  }
+  if (cols) {
+    const float inv = 1.0f / L;
+    __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                          size_t(row) * D + 4 * lane);
+    o[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    o[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1316,6 +1330,27 @@ pk_status launch_merge(const AttnParams &p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
+// attn_lse_merge_kernel after a tensor-core attention launch on `stream`, as
+// its programmatic dependent (an ordinary launch where that is refused).
+template <int D>
+pk_status launch_lse_merge(const AttnParams &p, cudaStream_t stream) {
+  const int rows = p.num_seqs * p.num_q_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_lse_merge_kernel<D>, p) == cudaSuccess) return PK_OK;
+  cudaGetLastError();
+  attn_lse_merge_kernel<D><<<cfg.gridDim, cfg.blockDim, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
+}
+
 // SMs of the current device (152 on GB300 when no device can be queried).
 int sm_count() {
   int dev = 0, n = 0;
@@ -1411,18 +1446,9 @@ int32_t cascade_partition(int32_t max_context_len, int32_t partition_size, int32
   return int32_t(std::min(part, whole));
 }
 
-// Fused-merge tickets, one 8-byte word per (sequence, KV head), after the
-// partials (only when splitting).
-size_t ticket_bytes(int32_t num_seqs, int32_t num_kv_heads, size_t partials) {
-  return partials ? size_t(num_seqs) * size_t(num_kv_heads) * 8 : 0;
-}
-
-// A distinct non-zero tag per call for the merge tickets.
-uint32_t next_epoch() {
-  static std::atomic<uint32_t> counter{0};
-  uint32_t e = ++counter;
-  while (e == 0) e = ++counter;
-  return e;
+// The tensor-core split-K merge after an attention launch: D dispatch.
+pk_status launch_lse_merge_d(const AttnParams &p, int D, cudaStream_t s) {
+  return D == 128 ? launch_lse_merge<128>(p, s) : launch_lse_merge<64>(p, s);
 }
 
 pk_status check_common(const pk_cache_desc *desc, int32_t num_seqs, int32_t num_q_heads,
@@ -1490,7 +1516,7 @@ size_t pk_paged_attention_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                                             max_context_len, partition_size, desc);
   if (part < 0) return 0;
   const size_t pb = partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
-  return pb + ticket_bytes(num_seqs, desc->num_kv_heads, pb);
+  return pb;
 }
 
 }  // extern "C"
@@ -1547,10 +1573,9 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
   p.num_partitions = int32_t(P);
   if (num_seqs > 65535 || P > 65535) return PK_ERR_UNSUPPORTED;
   const size_t pbytes = partial_bytes(num_seqs, num_q_heads, max_context_len, part, desc->head_dim);
-  const size_t tbytes = ticket_bytes(num_seqs, desc->num_kv_heads, pbytes);
   if (workspace && !aligned16(workspace)) return PK_ERR_WORKSPACE;
   if (P > 1) {
-    if (!workspace || workspace_bytes < pbytes + tbytes) return PK_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < pbytes) return PK_ERR_WORKSPACE;
     const size_t rows = size_t(num_seqs) * num_q_heads * size_t(P);
     p.ws_acc = static_cast<float *>(workspace);
     p.ws_m = p.ws_acc + rows * desc->head_dim;
@@ -1591,10 +1616,6 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
     }
   }
   if (use_mma) {
-    if (P > 1) {
-      p.merge_tickets = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + pbytes);
-      p.epoch = next_epoch();
-    }
     if (D == 128) {
       st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
                   : (B == 16 ? launch_mma<128, 16>(p, *desc, s) : launch_mma<128, 32>(p, *desc, s));
@@ -1607,7 +1628,8 @@ pk_status decode_attention(void *out, const void *q, const void *k_cache, const 
   } else {
     st = D == 128 ? launch_simt<__nv_bfloat16, 128>(p, s) : launch_simt<__nv_bfloat16, 64>(p, s);
   }
-  if (st != PK_OK || P == 1 || use_mma) return st;  // the tensor-core kernel merges itself
+  if (st != PK_OK || P == 1) return st;
+  if (use_mma) return launch_lse_merge_d(p, D, s);
   if (desc->dtype == PK_F32)
     return D == 128 ? launch_merge<float, 128>(p, s) : launch_merge<float, 64>(p, s);
   return D == 128 ? launch_merge<__nv_bfloat16, 128>(p, s) : launch_merge<__nv_bfloat16, 64>(p, s);
@@ -1778,8 +1800,7 @@ size_t pk_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t 
   const int64_t P = (int64_t(max_prefix_len) + part - 1) / part +
                     (int64_t(max_context_len) + part - 1) / part;
   const int64_t rows = int64_t(num_seqs) * num_q_heads * P;
-  return size_t(rows) * (size_t(desc->head_dim) + 2) * sizeof(float) +
-         size_t(num_seqs) * size_t(desc->num_kv_heads) * 8;
+  return size_t(rows) * (size_t(desc->head_dim) + 2) * sizeof(float);
 }
 
 pk_status pk_cascade_attention_decode(
@@ -1838,8 +1859,6 @@ pk_status pk_cascade_attention_decode(
   p.ws_acc = static_cast<float *>(workspace);
   p.ws_m = p.ws_acc + rows * desc->head_dim;
   p.ws_l = p.ws_m + rows;
-  p.merge_tickets = reinterpret_cast<unsigned long long *>(p.ws_l + rows);
-  p.epoch = next_epoch();
   p.order = seq_order;
   p.seq_prefix = seq_prefix_len;
   p.group_offsets = group_offsets;
@@ -1848,23 +1867,25 @@ pk_status pk_cascade_attention_decode(
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, B = desc->block_size;
   // One launch: the prefix CTAs first (the long ones), then the suffix CTAs;
-  // they meet only through the merge tickets.
+  // every part writes a partial, and the merge launch combines them.
   if (Ppre > 0) {
     if (D == 128)
-      return B == 8 ? launch_cascade<128, 8>(p, *desc, num_groups, s)
-                    : (B == 16 ? launch_cascade<128, 16>(p, *desc, num_groups, s)
-                               : launch_cascade<128, 32>(p, *desc, num_groups, s));
-    return B == 8 ? launch_cascade<64, 8>(p, *desc, num_groups, s)
+      st = B == 8 ? launch_cascade<128, 8>(p, *desc, num_groups, s)
+                  : (B == 16 ? launch_cascade<128, 16>(p, *desc, num_groups, s)
+                             : launch_cascade<128, 32>(p, *desc, num_groups, s));
+    else
+      st = B == 8 ? launch_cascade<64, 8>(p, *desc, num_groups, s)
                   : (B == 16 ? launch_cascade<64, 16>(p, *desc, num_groups, s)
                              : launch_cascade<64, 32>(p, *desc, num_groups, s));
-  }
-  if (D == 128)
+  } else if (D == 128) {
     st = B == 8 ? launch_mma<128, 8>(p, *desc, s)
                 : (B == 16 ? launch_mma<128, 16>(p, *desc, s) : launch_mma<128, 32>(p, *desc, s));
-  else
+  } else {
     st = B == 8 ? launch_mma<64, 8>(p, *desc, s)
                 : (B == 16 ? launch_mma<64, 16>(p, *desc, s) : launch_mma<64, 32>(p, *desc, s));
-  return st;
+  }
+  if (st != PK_OK || Ppre + Psuf <= 1) return st;
+  return launch_lse_merge_d(p, D, s);
 }
 
 pk_status pk_paged_attention_decode(void *out, const void *q, const void *k_cache,
@@ -1951,17 +1972,8 @@ extern "C" pk_status pk_paged_attention_decode_static(
     if (cudaGetDevice(&device) != cudaSuccess) return PK_ERR_CUDA;
     if (static_workspace_address(device, &ws) != cudaSuccess) return PK_ERR_CUDA;
   }
-  // Every partial the merge reads is written earlier in the same call. The
-  // merge tickets (the last num_seqs x Hk words of the size) are cleared
-  // first: the array keeps whatever earlier calls left, and a leftover word
-  // whose upper half happened to equal this call's ticket tag would be
-  // counted as an arrival. Clearing them allocates nothing.
-  if (need > 0 && num_seqs > 0) {
-    const size_t tickets = size_t(num_seqs) * size_t(desc->num_kv_heads) * 8;
-    if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + (need - tickets), 0, tickets,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-      return PK_ERR_CUDA;
-  }
+  // Nothing in the scratch needs clearing: every partial the merge reads is
+  // written earlier in the same call.
   return pk_paged_attention_decode_impl(out, q, k_cache, v_cache, block_tables, context_lens,
                                         scale, num_seqs, num_q_heads, max_blocks_per_seq,
                                         max_context_len, partition_size, ws,

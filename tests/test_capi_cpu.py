@@ -232,7 +232,7 @@ def test_partition_resolution_and_workspace_size(L):
     assert pk.pk_paged_attention_resolve_partition(8, 60, 300, -1, d) == -1        # Hq % Hk != 0
     assert pk.pk_paged_attention_resolve_partition(8, 128, 300, -1, d) == -1       # group of 16
     ws = pk.pk_paged_attention_workspace_size(8, 64, 32768, 512, d)
-    assert ws == 8 * 64 * 64 * (128 + 2) * 4 + 8 * 8 * 8       # [S, Hq, P, d+2] fp32 + [S, Hk] tickets
+    assert ws == 8 * 64 * 64 * (128 + 2) * 4                   # [S, Hq, P, d+2] fp32 partials
     assert pk.pk_paged_attention_workspace_size(8, 64, 512, 512, d) == 0           # one partition
     assert pk.pk_paged_attention_workspace_size(8, 64, 32768, 0, d) == 0
 

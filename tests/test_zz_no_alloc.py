@@ -9,10 +9,10 @@ library holds on every GPU that loads it.
 
 The test calls it through the C ABI three times in a row, on workloads that
 all split, and shapes the calls so that leftovers matter: the first call
-fills the most scratch, the second call's merge tickets then sit on the
-first call's partial outputs, and the third (another shape) lands on both.
-Each output must equal, bit for bit, pk_paged_attention_decode run with a
-caller-allocated workspace (the same kernel, partitioning and merge order)
+fills the most scratch, and the second and third (smaller, other shapes)
+then find the earlier calls' partials everywhere they write. Each output
+must equal, bit for bit, pk_paged_attention_decode run with a
+caller-allocated workspace (the same kernels, partitioning and merge order)
 and match the oracle within the bf16 tolerance the parity tests use. It
 also checks that a request larger than the static array is refused before
 any launch. This file is collected last.
@@ -53,16 +53,10 @@ def _built():
     pk.build()
 
 
-def _ticket_offset(st, d, part):
-    """Where a call's merge tickets start in the scratch (after its partials)."""
-    need = st.workspace_bytes(d["max_context_len"], part)
-    return need - st.wl.num_seqs * st.wl.num_kv_heads * 8
-
-
 def test_static_scratch_matches_caller_workspace_three_calls():
     # (workload, sequences, partition): the first call writes the most
-    # partials; the second's tickets fall inside them; the third differs in
-    # shape again.
+    # partials; the second and third, smaller and shaped differently, write
+    # over them.
     cases = [("gqa8b", 24, 128), ("long", 1, 512), ("mixed", 6, 256)]
     written = 0
     for name, nseq, part in cases:
@@ -74,8 +68,7 @@ def test_static_scratch_matches_caller_workspace_three_calls():
         need = st.workspace_bytes(d["max_context_len"], part)
         assert 0 < need <= pk.PK_STATIC_WORKSPACE_BYTES      # it splits, and fits the array
         if written:
-            # This call's tickets lie on scratch an earlier call wrote.
-            assert _ticket_offset(st, d, part) < written
+            assert need < written                               # all of it on scratch an earlier call wrote
         written = max(written, need)
         want = st.new_out()
         st.run_step(d, want, st.alloc_workspace(d["max_context_len"], part), part)
