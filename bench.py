@@ -855,6 +855,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
             "ms_per_step_median": 1e3 * float(np.median(per_step)), "ms_per_step_max": 1e3 * max(per_step),
             "host_us_median": {"launch": 1e6 * float(np.median(host_launch)),
                                "prepare_next_overlapped": 1e6 * float(np.median(host_prepare))},
+            "host_launch_us_median": 1e6 * float(np.median(host_launch)),
+            "host_prepare_us_median": 1e6 * float(np.median(host_prepare)),
             "includes": "pk_decode_step_launch of the prepared step (device-resident block tables, its "
                         "own stream, zero-copy; one CUDA graph of one kernel on steady steps: the scatter "
                         "reading the slots and the new K/V from pinned host memory and advancing the "
