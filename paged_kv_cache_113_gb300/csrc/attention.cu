@@ -1101,43 +1101,53 @@ __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
 // of a split row and nothing else for it. This kernel runs right after them on
 // the same stream, launched as their programmatic dependent: it may be
 // scheduled while the attention drains and waits for it to complete before
-// reading. One warp per (sequence, query head) row, eight rows per CTA; a row
+// reading. A row (sequence, query head) gets `wpr` warps (1, 2, 4 or 8, chosen
+// from the launch's partition count so that a warp merges at most eight
+// parts): each warp merges a contiguous run of the row's parts -- maxima
+// shared over the lanes, then eight parts' loads in flight at a time -- and
+// the row's first warp combines the warps' states from shared memory. A row
 // with a single part was written by the attention launch and is skipped.
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p) {
+__global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p, int wpr) {
+  __shared__ float4 sm_acc[8][D / 4];
+  __shared__ float sm_ml[8][2];
   pk::wait_prerequisites();
-  const int lane = int(threadIdx.x & 31);
-  const int row = int(blockIdx.x) * 8 + int(threadIdx.x >> 5);
-  if (row >= p.num_seqs * p.num_q_heads) return;
-  const int s = row / p.num_q_heads;
-  const int ctx = context_len(p, s, false);
-  const int pre = p.seq_prefix ? min(max(__ldg(p.seq_prefix + s), 0), ctx) : 0;
-  const int npre = (pre + p.partition - 1) / p.partition;
-  const int np = npre + (ctx - pre + p.partition - 1) / p.partition;
-  if (np <= 1) return;
+  const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
+  const int row = int(blockIdx.x) * (8 / wpr) + warp / wpr, sub = warp % wpr;
+  int s = 0, npre = 0, np = 0;
+  if (row < p.num_seqs * p.num_q_heads) {
+    s = row / p.num_q_heads;
+    const int ctx = context_len(p, s, false);
+    const int pre = p.seq_prefix ? min(max(__ldg(p.seq_prefix + s), 0), ctx) : 0;
+    npre = (pre + p.partition - 1) / p.partition;
+    np = npre + (ctx - pre + p.partition - 1) / p.partition;
+  }
+  const bool merge = np > 1;
   // Part q's workspace slot: the prefix parts first, then the rest.
   const size_t base = size_t(row) * p.num_partitions;
   auto slot = [&](int q) { return base + (q < npre ? q : p.prefix_slots + (q - npre)); };
-  // M = max_q m_q: the lanes share the parts, then a warp reduction.
+  const int chunk = (np + wpr - 1) / wpr;
+  const int q0 = min(np, sub * chunk), q1 = min(np, q0 + chunk);
+  // This warp's parts: M = max_q m_q, L = sum_q l_q 2^(m_q - M),
+  // acc = sum_q acc_q 2^(m_q - M), in part order; each lane owns four columns.
   float M = -INFINITY;
-  for (int q = lane; q < np; q += 32) M = fmaxf(M, __ldcg(p.ws_m + slot(q)));
+  if (merge)
+    for (int q = q0 + lane; q < q1; q += 32) M = fmaxf(M, __ldcg(p.ws_m + slot(q)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  // L = sum_q l_q 2^(m_q - M), out = sum_q acc_q 2^(m_q - M) / L, in part
-  // order; each lane owns four columns and loads eight parts at a time.
   constexpr int COLS = D / 4;  // lanes with columns
   const bool cols = lane < COLS;
   float L = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   constexpr int U = 8;
-  for (int q0 = 0; q0 < np; q0 += U) {
+  for (int qb = q0; merge && qb < q1; qb += U) {
     float mq[U], lq[U];
     float4 x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int q = q0 + u;
-      if (q < np) {
+      const int q = qb + u;
+      if (q < q1) {
         const size_t sl = slot(q);
         mq[u] = __ldcg(p.ws_m + sl);
         lq[u] = __ldcg(p.ws_l + sl);
@@ -1147,7 +1157,7 @@ __global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p) {
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (q0 + u < np) {
+      if (qb + u < q1) {
         const float w = exp2f(mq[u] - M);
         L = fmaf(lq[u], w, L);
         acc.x = fmaf(x[u].x, w, acc.x);
@@ -1157,7 +1167,33 @@ __global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p) {
       }
     }
   }
-  if (cols) {
+  if (wpr > 1) {
+    // Combine the row's warps (in warp order) in the row's first warp.
+    if (cols) sm_acc[warp][lane] = acc;
+    if (lane == 0) {
+      sm_ml[warp][0] = M;
+      sm_ml[warp][1] = L;
+    }
+    __syncthreads();
+    if (sub != 0) return;
+    const int w0 = warp;
+    float Mr = -INFINITY;
+    for (int w = 0; w < wpr; ++w) Mr = fmaxf(Mr, sm_ml[w0 + w][0]);
+    L = 0.0f;
+    acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int w = 0; w < wpr; ++w) {
+      const float f = sm_ml[w0 + w][1] > 0.0f ? exp2f(sm_ml[w0 + w][0] - Mr) : 0.0f;
+      L = fmaf(sm_ml[w0 + w][1], f, L);
+      if (cols) {
+        const float4 y = sm_acc[w0 + w][lane];
+        acc.x = fmaf(y.x, f, acc.x);
+        acc.y = fmaf(y.y, f, acc.y);
+        acc.z = fmaf(y.z, f, acc.z);
+        acc.w = fmaf(y.w, f, acc.w);
+      }
+    }
+  }
+  if (merge && cols) {
     const float inv = 1.0f / L;
     __nv_bfloat162 *o = reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                                           size_t(row) * D + 4 * lane);
@@ -1335,8 +1371,12 @@ pk_status launch_merge(const AttnParams &p, cudaStream_t stream) {
 template <int D>
 pk_status launch_lse_merge(const AttnParams &p, cudaStream_t stream) {
   const int rows = p.num_seqs * p.num_q_heads;
+  // Warps per row: enough that a warp merges at most eight parts (at most 8).
+  int wpr = 1;
+  while (wpr < 8 && wpr * 8 < p.num_partitions) wpr *= 2;
+  const int rows_per_cta = 8 / wpr;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((rows + 7) / 8));
+  cfg.gridDim = dim3(unsigned((rows + rows_per_cta - 1) / rows_per_cta));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -1345,9 +1385,9 @@ pk_status launch_lse_merge(const AttnParams &p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_lse_merge_kernel<D>, p) == cudaSuccess) return PK_OK;
+  if (cudaLaunchKernelEx(&cfg, attn_lse_merge_kernel<D>, p, wpr) == cudaSuccess) return PK_OK;
   cudaGetLastError();
-  attn_lse_merge_kernel<D><<<cfg.gridDim, cfg.blockDim, 0, stream>>>(p);
+  attn_lse_merge_kernel<D><<<cfg.gridDim, cfg.blockDim, 0, stream>>>(p, wpr);
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
