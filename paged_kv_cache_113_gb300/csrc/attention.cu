@@ -1112,9 +1112,10 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p, int wpr) {
   __shared__ float4 sm_acc[8][D / 4];
   __shared__ float sm_ml[8][2];
-  pk::wait_prerequisites();
   const int warp = int(threadIdx.x >> 5), lane = int(threadIdx.x & 31);
   const int row = int(blockIdx.x) * (8 / wpr) + warp / wpr, sub = warp % wpr;
+  // The row's part count, from the context and shared-prefix lengths: inputs
+  // the attention launch does not write, so they are read before waiting on it.
   int s = 0, npre = 0, np = 0;
   if (row < p.num_seqs * p.num_q_heads) {
     s = row / p.num_q_heads;
@@ -1123,6 +1124,7 @@ __global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p, int w
     npre = (pre + p.partition - 1) / p.partition;
     np = npre + (ctx - pre + p.partition - 1) / p.partition;
   }
+  pk::wait_prerequisites();  // the attention's partials are complete and visible
   const bool merge = np > 1;
   // Part q's workspace slot: the prefix parts first, then the rest.
   const size_t base = size_t(row) * p.num_partitions;
@@ -1131,17 +1133,47 @@ __global__ void __launch_bounds__(256) attn_lse_merge_kernel(AttnParams p, int w
   const int q0 = min(np, sub * chunk), q1 = min(np, q0 + chunk);
   // This warp's parts: M = max_q m_q, L = sum_q l_q 2^(m_q - M),
   // acc = sum_q acc_q 2^(m_q - M), in part order; each lane owns four columns.
-  float M = -INFINITY;
-  if (merge)
-    for (int q = q0 + lane; q < q1; q += 32) M = fmaxf(M, __ldcg(p.ws_m + slot(q)));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  // Up to U parts (the usual case: wpr gives a warp at most eight) are loaded
+  // in one batch and M is taken from the loaded maxima; more take a first
+  // pass over the maxima, shared by the lanes.
   constexpr int COLS = D / 4;  // lanes with columns
+  constexpr int U = 8;
   const bool cols = lane < COLS;
+  float M = -INFINITY;
   float L = 0.0f;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  constexpr int U = 8;
-  for (int qb = q0; merge && qb < q1; qb += U) {
+  if (merge && q1 - q0 <= U) {
+    float mq[U], lq[U];
+    float4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int q = q0 + u;
+      if (q < q1) {
+        const size_t sl = slot(q);
+        mq[u] = __ldcg(p.ws_m + sl);
+        lq[u] = __ldcg(p.ws_l + sl);
+        x[u] = cols ? __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + sl * D) + lane)
+                    : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        M = fmaxf(M, mq[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (q0 + u < q1) {
+        const float w = exp2f(mq[u] - M);
+        L = fmaf(lq[u], w, L);
+        acc.x = fmaf(x[u].x, w, acc.x);
+        acc.y = fmaf(x[u].y, w, acc.y);
+        acc.z = fmaf(x[u].z, w, acc.z);
+        acc.w = fmaf(x[u].w, w, acc.w);
+      }
+    }
+  } else if (merge) {
+    for (int q = q0 + lane; q < q1; q += 32) M = fmaxf(M, __ldcg(p.ws_m + slot(q)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  }
+  for (int qb = q0; merge && q1 - q0 > U && qb < q1; qb += U) {
     float mq[U], lq[U];
     float4 x[U];
 #pragma unroll
