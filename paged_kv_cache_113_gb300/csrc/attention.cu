@@ -1076,7 +1076,7 @@ __global__ void __launch_bounds__(32) wait_timeout_probe_kernel(uint32_t polls) 
 
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of split-K partials for the CUDA-core kernel (the
-// tensor-core kernel fuses the same merge into its last partition).
+// tensor-core kernels' partials are merged by attn_lse_merge_kernel).
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(128) attn_merge_kernel(AttnParams p) {
