@@ -808,9 +808,10 @@ def run_e2e(st, wl, E, Ew, args, dev):
 
     inputs = [tuple(pinned(x) for x in wl.step_inputs(10_000 + i)) for i in range(E + Ew)]
     max_ctx = int(wl.ctx_lens.max()) + st.steps_done + E + Ew + 1
-    # Zero-copy: each step's inputs sit in the stepper's pinned host buffers
-    # when the step starts; the kernels read them and write the output back
-    # across the host link inside the timed step.
+    # Zero-copy: each step's inputs sit in their own pinned host buffers when
+    # the step starts; the launch points the captured kernels at them, and
+    # the kernels read them and write the output back across the host link
+    # inside the timed step.
     stepper = pk.DecodeStepper(st.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, st.max_blocks,
                                st.k_cache, st.v_cache, args.partition, max_context_len=max_ctx,
                                zero_copy=True)
@@ -827,11 +828,8 @@ def run_e2e(st, wl, E, Ew, args, dev):
     for i in range(E + Ew):
         q, k, v = inputs[i]
         stream.synchronize()
-        stepper.q_host.copy_(q)
-        stepper.k_host.copy_(k)
-        stepper.v_host.copy_(v)
         t0 = time.perf_counter()
-        stepper.launch_prepared()
+        stepper.launch_prepared(q_host=q, k_host=k, v_host=v)
         t1 = time.perf_counter()
         stepper.prepare()
         t2 = time.perf_counter()
@@ -857,11 +855,12 @@ def run_e2e(st, wl, E, Ew, args, dev):
                                "prepare_next_overlapped": 1e6 * float(np.median(host_prepare))},
             "host_launch_us_median": 1e6 * float(np.median(host_launch)),
             "host_prepare_us_median": 1e6 * float(np.median(host_prepare)),
-            "includes": "pk_decode_step_launch of the prepared step (device-resident block tables, its "
-                        "own stream, zero-copy; one CUDA graph of one kernel on steady steps: the scatter "
-                        "reading the slots and the new K/V from pinned host memory and advancing the "
-                        "tables, the attention reading q from and writing the output to pinned host "
-                        "memory over the host link), then pk_decode_step_prepare of the next step (host block-manager "
+            "includes": "pk_decode_step_launch of the prepared step on that step's own pinned input "
+                        "buffers (device-resident block tables, its own stream, zero-copy; on steady steps "
+                        "one CUDA graph of one kernel, re-pointed at the step's buffers: the scatter reading "
+                        "the slots and the new K/V from pinned host memory and advancing the tables, the "
+                        "attention reading q from and writing the output to pinned host memory over the "
+                        "host link), then pk_decode_step_prepare of the next step (host block-manager "
                         "append, overlapped with the GPU), stream sync",
             "_seconds": tot_t, "_bytes": tot_b}
 

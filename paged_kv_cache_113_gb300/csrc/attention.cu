@@ -1538,6 +1538,43 @@ pk_status check_common(const pk_cache_desc *desc, int32_t num_seqs, int32_t num_
 
 }  // namespace
 
+// Library-internal hooks for the decode step's captured graphs (decode_step.cpp):
+// the size of a kernel's parameter block, the number of arguments of an
+// attention kernel (0 for a function that is not one), and re-pointing a
+// parameter block's host-buffer arguments. A graph captured in zero-copy mode
+// reads q and the new K/V from, and writes the output to, the caller's
+// pinned host buffers; a later step that passes other buffers re-points the
+// captured kernel nodes at them instead of capturing again.
+extern "C" size_t pkx_attn_params_size() { return sizeof(AttnParams); }
+
+namespace {
+template <int D, int BS>
+bool is_mma(const void *f) {
+  return f == reinterpret_cast<const void *>(attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>);
+}
+}  // namespace
+
+extern "C" int pkx_attn_kernel_arity(const void *f) {
+  if (is_mma<128, 8>(f) || is_mma<128, 16>(f) || is_mma<128, 32>(f) || is_mma<64, 8>(f) ||
+      is_mma<64, 16>(f) || is_mma<64, 32>(f))
+    return 3;  // (params, K tensor map, V tensor map)
+  if (f == reinterpret_cast<const void *>(attn_lse_merge_kernel<128>) ||
+      f == reinterpret_cast<const void *>(attn_lse_merge_kernel<64>))
+    return 2;  // (params, warps per row)
+  return 0;
+}
+
+// In the parameter block `params` (an AttnParams), each of q, new K, new V and
+// out that equals from[i] becomes to[i] (i = 0..3 in that order).
+extern "C" void pkx_attn_params_rebind(void *params, const void *const from[4],
+                                       const void *const to[4]) {
+  AttnParams *p = static_cast<AttnParams *>(params);
+  if (p->q == from[0]) p->q = to[0];
+  if (p->new_k == from[1]) p->new_k = to[1];
+  if (p->new_v == from[2]) p->new_v = to[2];
+  if (p->out == from[3]) p->out = const_cast<void *>(to[3]);
+}
+
 extern "C" int pkx_take_attention_error(cudaStream_t stream) {
   int code = 0;
   const int zero = 0;

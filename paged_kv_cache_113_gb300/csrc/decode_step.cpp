@@ -26,6 +26,13 @@
 
 #include "pagedkv.h"
 
+// Library-internal hooks of attention.cu for re-pointing captured attention
+// kernels at other host buffers (zero-copy mode).
+extern "C" size_t pkx_attn_params_size();
+extern "C" int pkx_attn_kernel_arity(const void *func);
+extern "C" void pkx_attn_params_rebind(void *params, const void *const from[4],
+                                       const void *const to[4]);
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -73,7 +80,10 @@ int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0);
 // A captured resident step: the copies of q, k, v and the slots, the scatter
 // that advances the device tables, the attention over the unchanged work
 // list and the output copy. Every parameter of those is fixed while the work
-// list is, except the caller's q/k/v host addresses, which are patched.
+// list is, except the caller's host buffers: in copying mode the q/k/v copy
+// nodes' sources are patched; in zero-copy mode the attention kernels read
+// and write the host buffers themselves, and their nodes' pointer arguments
+// are re-pointed.
 struct GraphSlot {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -81,6 +91,11 @@ struct GraphSlot {
   const void *src[3] = {nullptr, nullptr, nullptr};
   const void *out = nullptr;  // the host output buffer the graph writes
   int lens_cur = 0;           // the device length buffer it reads
+  // Zero-copy mode: the kernel nodes (-1: a kernel that cannot be re-pointed)
+  // and the device views of q, k, v and out they were captured with.
+  int nkern = 0;
+  cudaGraphNode_t kern[4] = {};
+  const void *cap_dev[4] = {};
 };
 
 // Library-managed state behind pk_step_buffers.state: the prepared step
@@ -103,16 +118,18 @@ struct StepState {
   size_t meta_copy = 0;
   int32_t num_seqs = 0, max_blocks = 0;
   int lens_cur = 0;  // device buffer holding the current lengths: 0 = lens, 1 = lens_b
-  // Device mappings of zero-copy host buffers, looked up once per address.
-  const void *map_host[8] = {};
-  void *map_dev[8] = {};
+  // Device mappings of zero-copy host buffers, looked up once per address
+  // (enough entries for a caller that cycles through many sets of buffers).
+  static constexpr int kMapCache = 128;
+  const void *map_host[kMapCache] = {};
+  void *map_dev[kMapCache] = {};
   int map_next = 0;
 };
 
 // The device address of pinned host memory `h` (zero-copy), from the state's
-// small cache or the runtime; false if `h` is not mapped host memory.
+// cache or the runtime; false if `h` is not mapped host memory.
 bool mapped(StepState *st, const void *h, void **d) {
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < StepState::kMapCache; ++i)
     if (st->map_host[i] == h && h) {
       *d = st->map_dev[i];
       return true;
@@ -123,7 +140,60 @@ bool mapped(StepState *st, const void *h, void **d) {
   }
   st->map_host[st->map_next] = h;
   st->map_dev[st->map_next] = *d;
-  st->map_next = (st->map_next + 1) % 8;
+  st->map_next = (st->map_next + 1) % StepState::kMapCache;
+  return true;
+}
+
+// Zero-copy graphs: records the attention kernel nodes of a captured step and
+// the device views of q, k, v and out they use (nkern -1 if a kernel node is
+// not an attention kernel, so the graph cannot be re-pointed).
+void find_kernel_nodes(GraphSlot &g, const void *const dev[4]) {
+  g.nkern = 0;
+  size_t n = 0;
+  if (cudaGraphGetNodes(g.graph, nullptr, &n) != cudaSuccess) {
+    g.nkern = -1;
+    return;
+  }
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n && cudaGraphGetNodes(g.graph, nodes.data(), &n) != cudaSuccess) n = 0, g.nkern = -1;
+  for (size_t i = 0; i < n && g.nkern >= 0; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess) {
+      g.nkern = -1;
+    } else if (t == cudaGraphNodeTypeKernel) {
+      cudaKernelNodeParams kp{};
+      if (g.nkern == 4 || cudaGraphKernelNodeGetParams(nodes[i], &kp) != cudaSuccess ||
+          pkx_attn_kernel_arity(kp.func) <= 0)
+        g.nkern = -1;
+      else
+        g.kern[g.nkern++] = nodes[i];
+    }
+  }
+  cudaGetLastError();
+  for (int k = 0; k < 4; ++k) g.cap_dev[k] = dev[k];
+}
+
+// Points the captured attention kernels of a zero-copy graph at the device
+// views `dev` of other host buffers (q, k, v, out), from their captured
+// parameters; false if that is not possible (the graph is then dropped).
+bool repoint_kernels(GraphSlot &g, const void *const dev[4]) {
+  if (g.nkern <= 0) return false;
+  const size_t psize = pkx_attn_params_size();
+  alignas(16) unsigned char blob[1024];
+  if (psize > sizeof(blob)) return false;
+  for (int k = 0; k < g.nkern; ++k) {
+    cudaKernelNodeParams kp{};
+    if (cudaGraphKernelNodeGetParams(g.kern[k], &kp) != cudaSuccess) return false;
+    const int arity = pkx_attn_kernel_arity(kp.func);
+    if (arity <= 0 || arity > 4 || !kp.kernelParams) return false;
+    std::memcpy(blob, kp.kernelParams[0], psize);
+    pkx_attn_params_rebind(blob, g.cap_dev, dev);
+    void *args[4] = {blob, nullptr, nullptr, nullptr};
+    for (int a = 1; a < arity; ++a) args[a] = kp.kernelParams[a];
+    kp.kernelParams = args;
+    kp.extra = nullptr;
+    if (cudaGraphExecKernelNodeSetParams(g.exec, g.kern[k], &kp) != cudaSuccess) return false;
+  }
   return true;
 }
 
@@ -378,6 +448,10 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
             if (mp.dstPtr.ptr == dsts[k]) g.copy_node[k] = nodes[i];
         }
         ok = ok && (zero_copy || (g.copy_node[0] && g.copy_node[1] && g.copy_node[2]));
+        if (ok && zero_copy) {
+          const void *views[4] = {qd, kd, vd, od};
+          find_kernel_nodes(g, views);
+        }
         st->zero_copy = zero_copy;
       }
       if (!ok) {
@@ -390,9 +464,21 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
         g.lens_cur = st->lens_cur;
       }
     }
-    const bool moved = st->zero_copy &&
-                       (g.src[0] != srcs[0] || g.src[1] != srcs[1] || g.src[2] != srcs[2]);
-    if (g.exec && (moved || g.out != b->out_host || st->zero_copy != zero_copy)) {
+    const bool moved = st->zero_copy && (g.src[0] != srcs[0] || g.src[1] != srcs[1] ||
+                                         g.src[2] != srcs[2] || g.out != b->out_host);
+    if (g.exec && moved && st->zero_copy == zero_copy) {
+      // Other host buffers than the graph was captured with: point its
+      // attention kernels at them (from the captured parameters).
+      const void *views[4] = {qd, kd, vd, od};
+      if (repoint_kernels(g, views)) {
+        for (int k = 0; k < 3; ++k) g.src[k] = srcs[k];
+        g.out = b->out_host;
+      } else {
+        cudaGetLastError();
+        drop_graphs(st);  // run it the normal way
+      }
+    }
+    if (g.exec && (g.out != b->out_host || st->zero_copy != zero_copy)) {
       drop_graphs(st);  // other host buffers than the graph's arguments: run it the normal way
     } else if (g.exec) {
       for (int k = 0; k < 3; ++k)

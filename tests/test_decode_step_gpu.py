@@ -238,17 +238,20 @@ def test_decode_step_full_size_against_the_oracle(name, B):
     stepper.release()
 
 
-def test_graph_replay_follows_new_host_buffers():
+@pytest.mark.parametrize("name,zero_copy", [("gqa8b", False), ("gqa8b", True), ("long", True)])
+def test_graph_replay_follows_new_host_buffers(name, zero_copy):
     """Steady steps replay the captured graph; each step passes fresh pinned
-    q/k/v tensors, so the graph's input copies are re-pointed every step.
-    Outputs equal the step-by-step path bit for bit."""
-    wl = make_workload("gqa8b", num_seqs=24)
+    q/k/v tensors, so the graph is re-pointed every step: its input copies
+    (copying mode) or its attention kernels' arguments (zero-copy mode; on
+    `long` the step splits, so the merge kernel is re-pointed too). Outputs
+    equal the step-by-step path bit for bit, and the graphs are kept."""
+    wl = make_workload(name, num_seqs=24 if name == "gqa8b" else 2)
     wl.enable_memo()
     steps = 12
     a = DecodeState(wl, "cuda", extra_tokens=steps)
     b = DecodeState(wl, "cuda", extra_tokens=steps)
     stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
-                               b.k_cache, b.v_cache)
+                               b.k_cache, b.v_cache, zero_copy=zero_copy)
     ref_path = _Stepwise(a)
     for i in range(steps):
         out_a = ref_path.step(i)
