@@ -635,12 +635,15 @@ pk_status pk_bm_stats(const pk_bm *bm, int64_t *live_tokens, int64_t *reserved_s
 /* Buffers of pk_decode_step. Host pointers should be pinned (page-locked) so
  * the copies are asynchronous; device pointers are caller-owned, 16-byte
  * aligned. With q_dev, k_dev, v_dev and out_dev all NULL (zero-copy mode) the
- * host buffers must be pinned, device-mapped memory: the kernels read q and
- * the new K/V from, and write the output to, them directly -- the same bytes
- * cross the host link, inside the kernels rather than as separate copies. The
- * device mapping of each such host address (and of meta_host) is looked up
- * once and kept in the library-managed state: a host buffer freed and pinned
- * again at the same address needs pk_decode_step_release first. */
+ * kernels read q and the new K/V from, and write the output to, the host
+ * buffers directly -- the same bytes cross the host link, inside the kernels
+ * rather than as separate copies. Where the GPU reads host memory through the
+ * host's page tables (a Grace-attached GB300) any host memory serves, at its
+ * own address, and nothing is looked up; elsewhere the host buffers (and
+ * meta_host) must be pinned, device-mapped memory (else PK_ERR_INVALID_ARG),
+ * and the device mapping of each address is looked up once and kept in the
+ * library-managed state: a host buffer freed and pinned again at the same
+ * address then needs pk_decode_step_release first. */
 typedef struct {
     const void *q_host;  /* [S, Hq, d] queries of the step                     */
     const void *k_host;  /* [S, Hk, d] the step's new keys                      */
@@ -712,11 +715,12 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  * stream, and not being captured), a steady resident step -- no
  * copy-on-write pair, the same work list -- runs as one CUDA graph, captured
  * on the first such step of each staging half: the input copies, the slot
- * copy, the scatter, the attention and the output copy; only the q/k/v host
- * addresses are patched when they change (in zero-copy mode, or when
- * out_host changes, the graph is rebuilt instead). The graphs are rebuilt
- * when the work list changes or after a full step. The per-step host work is
- * then the block-manager append and one graph launch. */
+ * copy, the scatter, the attention and the output copy. Other host buffers
+ * than a graph was captured with are patched into it: the q/k/v copies'
+ * sources in copying mode (a new out_host rebuilds the graph instead), the
+ * attention kernels' pointer arguments in zero-copy mode. The graphs are
+ * rebuilt when the work list changes or after a full step. The per-step host
+ * work is then the block-manager append and one graph launch. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,

@@ -124,11 +124,30 @@ struct StepState {
   const void *map_host[kMapCache] = {};
   void *map_dev[kMapCache] = {};
   int map_next = 0;
+  // 1 if the GPU reads host memory through the host's page tables (a
+  // Grace-attached GPU): a host address is then its own device address and
+  // nothing is looked up; -1 until queried.
+  int host_page_tables = -1;
 };
 
-// The device address of pinned host memory `h` (zero-copy), from the state's
-// cache or the runtime; false if `h` is not mapped host memory.
+// The device address of host memory `h` (zero-copy): `h` itself where the GPU
+// uses the host's page tables, else pinned memory's mapping from the state's
+// cache or the runtime; false if `h` is not addressable from the device.
 bool mapped(StepState *st, const void *h, void **d) {
+  if (st->host_page_tables < 0) {
+    int dev = 0, v = 0;
+    st->host_page_tables =
+        cudaGetDevice(&dev) == cudaSuccess &&
+                cudaDeviceGetAttribute(&v, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                                       dev) == cudaSuccess && v
+            ? 1
+            : 0;
+    cudaGetLastError();
+  }
+  if (st->host_page_tables) {
+    *d = const_cast<void *>(h);
+    return h != nullptr;
+  }
   for (int i = 0; i < StepState::kMapCache; ++i)
     if (st->map_host[i] == h && h) {
       *d = st->map_dev[i];
@@ -327,7 +346,7 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
   void *qd = b->q_dev, *kd = b->k_dev, *vd = b->v_dev, *od = b->out_dev;
   if (zero_copy && (!mapped(st, b->q_host, &qd) || !mapped(st, b->k_host, &kd) ||
                     !mapped(st, b->v_host, &vd) || !mapped(st, b->out_host, &od)))
-    return PK_ERR_INVALID_ARG;  // not pinned, mapped host memory
+    return PK_ERR_INVALID_ARG;  // not host memory the device can address
   const MetaLayout m = layout(num_seqs, max_blocks_per_seq);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int h = st->half;

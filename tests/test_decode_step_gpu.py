@@ -265,6 +265,37 @@ def test_graph_replay_follows_new_host_buffers(name, zero_copy):
     assert not stepper.buffers.state and stepper.graph_count == 0
 
 
+def test_zero_copy_unpinned_inputs_are_exact_or_refused():
+    """Zero-copy steps given ordinary (unpinned) host tensors: where the GPU
+    reads host memory through the host's page tables they are used at their
+    own addresses and the outputs equal the step-by-step path bit for bit;
+    elsewhere the launch is refused with an invalid-argument status before any
+    work. Never a wrong output."""
+    wl = make_workload("gqa8b", num_seqs=16)
+    wl.enable_memo()
+    steps = 6
+    a = DecodeState(wl, "cuda", extra_tokens=steps)
+    b = DecodeState(wl, "cuda", extra_tokens=steps)
+    stepper = pk.DecodeStepper(b.bm, range(wl.num_seqs), wl.num_q_heads, wl.scale, b.max_blocks,
+                               b.k_cache, b.v_cache, zero_copy=True)
+    ref_path = _Stepwise(a)
+    for i in range(steps):
+        q, k, v = (_host(x, wl.dtype) for x in wl.step_inputs(i))
+        assert not q.is_pinned()
+        try:
+            stepper.launch(q_host=q, k_host=k, v_host=v)
+        except pk.PagedKVError as e:
+            assert i == 0 and e.status == pk.PK_ERR_INVALID_ARG
+            stepper.release()
+            pytest.skip("this GPU does not read host memory through the host's page tables")
+        stepper.stream.synchronize()
+        out_a = ref_path.step(i)
+        assert np.array_equal(from_device(out_a), from_device(stepper.out_host)), f"step {i}"
+    assert stepper.graph_count == 2
+    assert pk.pk_get_device_error()[0] == 0
+    stepper.release()
+
+
 @pytest.mark.parametrize("name,nseq,B", [("gqa8b", 24, None), ("prefix", 8, 32), ("mixed", 40, None)])
 def test_zero_copy_steps_match_the_copying_steps(name, nseq, B):
     """Zero-copy mode (the kernels read q, k, v from and write out to pinned host
