@@ -391,16 +391,21 @@ def test_chat_prefix_cache_bookkeeping():
     st.bm.check_invariants()
 
 
-@pytest.mark.parametrize("name,nseq,part", [("gqa8b", 40, 256), ("gqa8b", 40, 512), ("long", 2, 4736),
-                                            ("prefix", 8, 512), ("mha7b", 8, 0), ("tiny", None, 16)])
-@pytest.mark.parametrize("impl", ["mma", "simt"])
-def test_work_list_matches_grid_bit_for_bit(name, nseq, part, impl):
+# Every bf16 case on both kernels; the fp32 `tiny` case on the CUDA-core
+# kernel only (the tensor-core kernel is bf16 only).
+_WORK_LIST_CASES = [(c, impl) for c in [("gqa8b", 40, 256), ("gqa8b", 40, 512), ("long", 2, 4736),
+                                        ("prefix", 8, 512), ("mha7b", 8, 0)] for impl in ("mma", "simt")]
+_WORK_LIST_CASES.append((("tiny", None, 16), "simt"))
+
+
+@pytest.mark.parametrize("case,impl", _WORK_LIST_CASES, ids=[f"{c[0]}-{c[2]}-{i}" for c, i in _WORK_LIST_CASES])
+def test_work_list_matches_grid_bit_for_bit(case, impl):
     """The (sequence, partition) work list gives the grid launch's result bit
     for bit (the same partials, merged in the same order) and the oracle's
     within tolerance."""
+    name, nseq, part = case
     wl = make_workload(name, num_seqs=nseq, block_size=8 if name == "prefix" else None)
-    if impl == "mma" and wl.dtype != "bf16":
-        pytest.skip("the tensor-core kernel is bf16 only")
+    assert impl == "simt" or wl.dtype == "bf16"
     st, d, _, ref = _build_pair(wl, compare_pool=False)
     lens = from_device(d["ctx_lens"])
     items = torch.from_numpy(pk.pk_attention_work_items(lens, st.resolve_partition(d["max_context_len"], part))).cuda()
