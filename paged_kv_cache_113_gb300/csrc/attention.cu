@@ -1552,6 +1552,11 @@ template <int D, int BS>
 bool is_mma(const void *f) {
   return f == reinterpret_cast<const void *>(attn_mma_kernel<D, BS, kMmaWarps, kMmaStages>);
 }
+template <typename T, int D>
+bool is_simt(const void *f) {
+  return f == reinterpret_cast<const void *>(attn_simt_kernel<T, D>) ||
+         f == reinterpret_cast<const void *>(attn_merge_kernel<T, D>);
+}
 }  // namespace
 
 extern "C" int pkx_attn_kernel_arity(const void *f) {
@@ -1561,6 +1566,9 @@ extern "C" int pkx_attn_kernel_arity(const void *f) {
   if (f == reinterpret_cast<const void *>(attn_lse_merge_kernel<128>) ||
       f == reinterpret_cast<const void *>(attn_lse_merge_kernel<64>))
     return 2;  // (params, warps per row)
+  if (is_simt<float, 128>(f) || is_simt<float, 64>(f) || is_simt<__nv_bfloat16, 128>(f) ||
+      is_simt<__nv_bfloat16, 64>(f))
+    return 1;  // (params)
   return 0;
 }
 

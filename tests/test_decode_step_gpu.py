@@ -238,14 +238,15 @@ def test_decode_step_full_size_against_the_oracle(name, B):
     stepper.release()
 
 
-@pytest.mark.parametrize("name,zero_copy", [("gqa8b", False), ("gqa8b", True), ("long", True)])
+@pytest.mark.parametrize("name,zero_copy", [("gqa8b", False), ("gqa8b", True), ("long", True), ("tiny", True)])
 def test_graph_replay_follows_new_host_buffers(name, zero_copy):
     """Steady steps replay the captured graph; each step passes fresh pinned
     q/k/v tensors, so the graph is re-pointed every step: its input copies
     (copying mode) or its attention kernels' arguments (zero-copy mode; on
-    `long` the step splits, so the merge kernel is re-pointed too). Outputs
-    equal the step-by-step path bit for bit, and the graphs are kept."""
-    wl = make_workload(name, num_seqs=24 if name == "gqa8b" else 2)
+    `long` the step splits, so the merge kernel is re-pointed too; `tiny` is
+    fp32, the CUDA-core kernel). Outputs equal the step-by-step path bit for
+    bit, and the graphs are kept."""
+    wl = make_workload(name, num_seqs={"gqa8b": 24, "long": 2}.get(name))
     wl.enable_memo()
     steps = 12
     a = DecodeState(wl, "cuda", extra_tokens=steps)
