@@ -253,6 +253,14 @@ pk_status pkx_reshape_and_cache_advance(const void *k, const void *v, const int6
   return cudaGetLastError() == cudaSuccess ? PK_OK : PK_ERR_CUDA;
 }
 
+// Library-internal hook for the decode step's captured graphs
+// (decode_step.cpp): the argument count of the advancing scatter kernel, whose
+// first two arguments are the new keys' and values' addresses; 0 for any
+// other function.
+extern "C" int pkx_scatter_kernel_arity(const void *f) {
+  return f == reinterpret_cast<const void *>(reshape_and_cache_kernel<true>) ? 12 : 0;
+}
+
 pk_status pk_read_stream(const void *buf, size_t bytes, unsigned int *sink, void *stream) {
   if (!buf || !sink || bytes < 16 || !aligned16(buf)) return PK_ERR_INVALID_ARG;
   int dev = 0, sms = 0;

@@ -26,12 +26,13 @@
 
 #include "pagedkv.h"
 
-// Library-internal hooks of attention.cu for re-pointing captured attention
-// kernels at other host buffers (zero-copy mode).
+// Library-internal hooks of attention.cu and cache_ops.cu for re-pointing
+// captured kernels at other host buffers (zero-copy mode).
 extern "C" size_t pkx_attn_params_size();
 extern "C" int pkx_attn_kernel_arity(const void *func);
 extern "C" void pkx_attn_params_rebind(void *params, const void *const from[4],
                                        const void *const to[4]);
+extern "C" int pkx_scatter_kernel_arity(const void *func);
 
 namespace {
 
@@ -91,8 +92,9 @@ struct GraphSlot {
   const void *src[3] = {nullptr, nullptr, nullptr};
   const void *out = nullptr;  // the host output buffer the graph writes
   int lens_cur = 0;           // the device length buffer it reads
-  // Zero-copy mode: the kernel nodes (-1: a kernel that cannot be re-pointed)
-  // and the device views of q, k, v and out they were captured with.
+  // Zero-copy mode: the kernel nodes that read or write the host buffers
+  // (-1: a kernel that cannot be re-pointed) and the device views of q, k, v
+  // and out they were captured with.
   int nkern = 0;
   cudaGraphNode_t kern[4] = {};
   const void *cap_dev[4] = {};
@@ -163,9 +165,10 @@ bool mapped(StepState *st, const void *h, void **d) {
   return true;
 }
 
-// Zero-copy graphs: records the attention kernel nodes of a captured step and
-// the device views of q, k, v and out they use (nkern -1 if a kernel node is
-// not an attention kernel, so the graph cannot be re-pointed).
+// Zero-copy graphs: records the kernel nodes of a captured step (attention,
+// merge, and the CUDA-core path's separate scatter) and the device views of q,
+// k, v and out they use (nkern -1 if a kernel node is none of those, so the
+// graph cannot be re-pointed).
 void find_kernel_nodes(GraphSlot &g, const void *const dev[4]) {
   g.nkern = 0;
   size_t n = 0;
@@ -182,7 +185,7 @@ void find_kernel_nodes(GraphSlot &g, const void *const dev[4]) {
     } else if (t == cudaGraphNodeTypeKernel) {
       cudaKernelNodeParams kp{};
       if (g.nkern == 4 || cudaGraphKernelNodeGetParams(nodes[i], &kp) != cudaSuccess ||
-          pkx_attn_kernel_arity(kp.func) <= 0)
+          (pkx_attn_kernel_arity(kp.func) <= 0 && pkx_scatter_kernel_arity(kp.func) <= 0))
         g.nkern = -1;
       else
         g.kern[g.nkern++] = nodes[i];
@@ -192,23 +195,38 @@ void find_kernel_nodes(GraphSlot &g, const void *const dev[4]) {
   for (int k = 0; k < 4; ++k) g.cap_dev[k] = dev[k];
 }
 
-// Points the captured attention kernels of a zero-copy graph at the device
-// views `dev` of other host buffers (q, k, v, out), from their captured
-// parameters; false if that is not possible (the graph is then dropped).
+// Points the captured kernels of a zero-copy graph at the device views `dev`
+// of other host buffers (q, k, v, out), from their captured parameters; false
+// if that is not possible (the graph is then dropped).
 bool repoint_kernels(GraphSlot &g, const void *const dev[4]) {
   if (g.nkern <= 0) return false;
   const size_t psize = pkx_attn_params_size();
   alignas(16) unsigned char blob[1024];
   if (psize > sizeof(blob)) return false;
+  constexpr int kMaxArgs = 16;
   for (int k = 0; k < g.nkern; ++k) {
     cudaKernelNodeParams kp{};
-    if (cudaGraphKernelNodeGetParams(g.kern[k], &kp) != cudaSuccess) return false;
-    const int arity = pkx_attn_kernel_arity(kp.func);
-    if (arity <= 0 || arity > 4 || !kp.kernelParams) return false;
-    std::memcpy(blob, kp.kernelParams[0], psize);
-    pkx_attn_params_rebind(blob, g.cap_dev, dev);
-    void *args[4] = {blob, nullptr, nullptr, nullptr};
-    for (int a = 1; a < arity; ++a) args[a] = kp.kernelParams[a];
+    if (cudaGraphKernelNodeGetParams(g.kern[k], &kp) != cudaSuccess || !kp.kernelParams)
+      return false;
+    void *args[kMaxArgs] = {};
+    const void *kv[2] = {};
+    int arity = pkx_attn_kernel_arity(kp.func);
+    if (arity > 0) {  // an attention or merge kernel: the parameter block first
+      if (arity > kMaxArgs) return false;
+      std::memcpy(blob, kp.kernelParams[0], psize);
+      pkx_attn_params_rebind(blob, g.cap_dev, dev);
+      args[0] = blob;
+      for (int a = 1; a < arity; ++a) args[a] = kp.kernelParams[a];
+    } else {  // the scatter: its first two arguments are the new K and V
+      arity = pkx_scatter_kernel_arity(kp.func);
+      if (arity < 2 || arity > kMaxArgs) return false;
+      for (int a = 0; a < 2; ++a) {
+        std::memcpy(&kv[a], kp.kernelParams[a], sizeof(kv[a]));
+        if (kv[a] == g.cap_dev[1 + a]) kv[a] = dev[1 + a];
+        args[a] = &kv[a];
+      }
+      for (int a = 2; a < arity; ++a) args[a] = kp.kernelParams[a];
+    }
     kp.kernelParams = args;
     kp.extra = nullptr;
     if (cudaGraphExecKernelNodeSetParams(g.exec, g.kern[k], &kp) != cudaSuccess) return false;
