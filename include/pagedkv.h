@@ -717,10 +717,12 @@ size_t pk_decode_step_meta_bytes(int32_t num_seqs, int32_t max_blocks_per_seq);
  * on the first such step of each staging half: the input copies, the slot
  * copy, the scatter, the attention and the output copy. Other host buffers
  * than a graph was captured with are patched into it: the q/k/v copies'
- * sources in copying mode (a new out_host rebuilds the graph instead), the
- * attention kernels' pointer arguments in zero-copy mode. The graphs are
- * rebuilt when the work list changes or after a full step. The per-step host
- * work is then the block-manager append and one graph launch. */
+ * sources in copying mode (a new out_host rebuilds the graph instead), in
+ * zero-copy mode the host-buffer arguments of the kernels that read or write
+ * them (the attention, its merge, and the CUDA-core path's separate
+ * scatter). The graphs are rebuilt when the work list changes or after a full
+ * step. The per-step host work is then the block-manager append and one graph
+ * launch. */
 pk_status pk_decode_step(pk_bm *bm, const int64_t *seq_ids, int32_t num_seqs, int32_t num_q_heads,
                          float scale, int32_t max_blocks_per_seq, int32_t partition_size,
                          void *k_cache, void *v_cache, const pk_cache_desc *desc,
