@@ -41,6 +41,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import gc
 import json
 import math
 import os
@@ -717,7 +718,7 @@ def run_ours(args):
     wl.enable_memo()
     R = max(1, min(args.window, args.steps + args.warmup))
     E = 0 if args.no_e2e else max(1, args.e2e_steps)
-    Ew = 0 if args.no_e2e else 3
+    Ew = 0 if args.no_e2e else 8
     st = DecodeState(wl, dev, extra_tokens=R + E + Ew + 1)
     flush = L2Flush(dev)
     sampler = None if args.no_clocks else ClockSampler(local_rank, gpu_uuid(dev))
@@ -733,7 +734,12 @@ def run_ours(args):
 
     e2e = None
     if E:
-        e2e = run_e2e(st, wl, E, Ew, args, dev)
+        # On a fresh copy of the workload's state, so that the e2e steps see
+        # the device steps' context lengths rather than ones a window further.
+        st_e2e = DecodeState(wl, dev, extra_tokens=E + Ew + 1)
+        e2e = run_e2e(st_e2e, wl, E, Ew, args, dev)
+        del st_e2e
+        torch.cuda.empty_cache()
         e2e["value"] = job_throughput(world, e2e["_bytes"], reduce_max([e2e["_seconds"]])[0])
         e2e.pop("_seconds")
         e2e.pop("_bytes")
@@ -832,24 +838,31 @@ def run_e2e(st, wl, E, Ew, args, dev):
     # GPU, so a timed step holds its launch, the next step's host half and
     # the synchronise. Step 0's host half is prepared before the warm-up.
     stepper.prepare()
-    for i in range(E + Ew):
-        q, k, v = inputs[i]
-        stream.synchronize()
-        t0 = time.perf_counter()
-        stepper.launch_prepared(q_host=q, k_host=k, v_host=v)
-        t1 = time.perf_counter()
-        stepper.prepare()
-        t2 = time.perf_counter()
-        stream.synchronize()
-        dt = time.perf_counter() - t0
-        st.steps_done += 1
-        if i >= Ew:
-            resident = resident and stepper.graph_count > 0
-            tot_t += dt
-            tot_b += step_kv_bytes(st, wl)
-            per_step.append(dt)
-            host_launch.append(t1 - t0)
-            host_prepare.append(t2 - t1)
+    # No collector pauses inside the timed steps (as timeit does).
+    gc_enabled = gc.isenabled()
+    gc.disable()
+    try:
+        for i in range(E + Ew):
+            q, k, v = inputs[i]
+            stream.synchronize()
+            t0 = time.perf_counter()
+            stepper.launch_prepared(q_host=q, k_host=k, v_host=v)
+            t1 = time.perf_counter()
+            stepper.prepare()
+            t2 = time.perf_counter()
+            stream.synchronize()
+            dt = time.perf_counter() - t0
+            st.steps_done += 1
+            if i >= Ew:
+                resident = resident and stepper.graph_count > 0
+                tot_t += dt
+                tot_b += step_kv_bytes(st, wl)
+                per_step.append(dt)
+                host_launch.append(t1 - t0)
+                host_prepare.append(t2 - t1)
+    finally:
+        if gc_enabled:
+            gc.enable()
     kind, idx = pk.pk_get_device_error()
     if kind:
         raise RuntimeError(f"device error in the e2e steps: {pk.DEVERR_NAMES.get(kind)} at {idx}")
