@@ -837,6 +837,11 @@ def run_e2e(st, wl, E, Ew, args, dev):
     # manager append, metadata) is prepared while the step before runs on the
     # GPU, so a timed step holds its launch, the next step's host half and
     # the synchronise. Step 0's host half is prepared before the warm-up.
+    # Every step appends one token to every sequence, so step i reads the
+    # starting lengths + i + 1 tokens; its bytes are counted up front, keeping
+    # host work out of the loop.
+    lens0 = np.array([st.bm.seq_len(s) for s in range(wl.num_seqs)], dtype=np.int64)
+    step_bytes = [wl.kv_bytes(lens0 + i + 1) for i in range(E + Ew)]
     stepper.prepare()
     # No collector pauses inside the timed steps (as timeit does).
     gc_enabled = gc.isenabled()
@@ -856,7 +861,7 @@ def run_e2e(st, wl, E, Ew, args, dev):
             if i >= Ew:
                 resident = resident and stepper.graph_count > 0
                 tot_t += dt
-                tot_b += step_kv_bytes(st, wl)
+                tot_b += step_bytes[i]
                 per_step.append(dt)
                 host_launch.append(t1 - t0)
                 host_prepare.append(t2 - t1)
@@ -1016,12 +1021,6 @@ def run_allocator_sim(reps: int = 3) -> dict:
         out["traces"][name] = {"capacity_slots": C, "requests": len(trace), "steps": r["summary"]["num_steps"],
                                "policies": rows}
     return out
-
-
-def step_kv_bytes(st, wl) -> int:
-    """K/V bytes the step just run read: the sequences' current lengths."""
-    lens = np.array([st.bm.seq_len(s) for s in range(wl.num_seqs)], dtype=np.int64)
-    return wl.kv_bytes(lens)
 
 
 def main(argv=None):
