@@ -93,10 +93,12 @@ struct GraphSlot {
   const void *out = nullptr;  // the host output buffer the graph writes
   int lens_cur = 0;           // the device length buffer it reads
   // Zero-copy mode: the kernel nodes that read or write the host buffers
-  // (-1: a kernel that cannot be re-pointed) and the device views of q, k, v
-  // and out they were captured with.
+  // (-1: a kernel that cannot be re-pointed), their captured parameters (the
+  // argument pointers refer to the captured graph, which is never changed),
+  // and the device views of q, k, v and out they were captured with.
   int nkern = 0;
   cudaGraphNode_t kern[4] = {};
+  cudaKernelNodeParams kparams[4] = {};
   const void *cap_dev[4] = {};
 };
 
@@ -185,10 +187,13 @@ void find_kernel_nodes(GraphSlot &g, const void *const dev[4]) {
     } else if (t == cudaGraphNodeTypeKernel) {
       cudaKernelNodeParams kp{};
       if (g.nkern == 4 || cudaGraphKernelNodeGetParams(nodes[i], &kp) != cudaSuccess ||
-          (pkx_attn_kernel_arity(kp.func) <= 0 && pkx_scatter_kernel_arity(kp.func) <= 0))
+          !kp.kernelParams ||
+          (pkx_attn_kernel_arity(kp.func) <= 0 && pkx_scatter_kernel_arity(kp.func) <= 0)) {
         g.nkern = -1;
-      else
+      } else {
+        g.kparams[g.nkern] = kp;
         g.kern[g.nkern++] = nodes[i];
+      }
     }
   }
   cudaGetLastError();
@@ -205,9 +210,7 @@ bool repoint_kernels(GraphSlot &g, const void *const dev[4]) {
   if (psize > sizeof(blob)) return false;
   constexpr int kMaxArgs = 16;
   for (int k = 0; k < g.nkern; ++k) {
-    cudaKernelNodeParams kp{};
-    if (cudaGraphKernelNodeGetParams(g.kern[k], &kp) != cudaSuccess || !kp.kernelParams)
-      return false;
+    cudaKernelNodeParams kp = g.kparams[k];
     void *args[kMaxArgs] = {};
     const void *kv[2] = {};
     int arity = pkx_attn_kernel_arity(kp.func);
@@ -505,7 +508,7 @@ pk_status pk_decode_step_launch(int32_t num_seqs, int32_t num_q_heads, float sca
                                          g.src[2] != srcs[2] || g.out != b->out_host);
     if (g.exec && moved && st->zero_copy == zero_copy) {
       // Other host buffers than the graph was captured with: point its
-      // attention kernels at them (from the captured parameters).
+      // kernels at them (from the captured parameters).
       const void *views[4] = {qd, kd, vd, od};
       if (repoint_kernels(g, views)) {
         for (int k = 0; k < 3; ++k) g.src[k] = srcs[k];
