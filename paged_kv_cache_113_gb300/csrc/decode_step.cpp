@@ -82,9 +82,9 @@ int64_t elem_size(pk_dtype t) { return t == PK_F32 ? 4 : (t == PK_BF16 ? 2 : 0);
 // that advances the device tables, the attention over the unchanged work
 // list and the output copy. Every parameter of those is fixed while the work
 // list is, except the caller's host buffers: in copying mode the q/k/v copy
-// nodes' sources are patched; in zero-copy mode the attention kernels read
-// and write the host buffers themselves, and their nodes' pointer arguments
-// are re-pointed.
+// nodes' sources are patched; in zero-copy mode the kernels read and write
+// the host buffers themselves, and their nodes' pointer arguments are
+// re-pointed.
 struct GraphSlot {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
